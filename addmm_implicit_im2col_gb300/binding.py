@@ -1,0 +1,216 @@
+"""Python binding of libimc's C ABI (include/imc.h).
+
+The functions named like the C entry points take raw integer device pointers
+and return the C status code.  ``addmm`` and ``conv2d`` wrap them for torch
+CUDA tensors (PyTorch supplies device memory and the current stream only;
+every step of the computation runs in libimc's kernels).  There is no CPU
+fallback: the library must be built (``python -m addmm_implicit_im2col_gb300.build``)
+and loading it raises otherwise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libimc.so")
+
+IMC_OK = 0
+IMC_ERR_NULL = -1
+IMC_ERR_SHAPE = -2
+IMC_ERR_ARG = -3
+IMC_ERR_ALIAS = -4
+IMC_ERR_CUDA = -5
+IMC_ERR_TIMEOUT = -6
+IMC_ERR_DEVICE = -7
+
+MODES = {"default": 0, "tf32": 1, "simt": 2, "force_tc3": 3, "force_tc1": 4}
+KERNELS = {0: "none", 1: "tc3", 2: "tc1", 3: "simt", 4: "fill"}
+
+# Every symbol the header declares, with (restype, argtypes).
+_i64, _dbl, _vp, _int = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
+SIGNATURES = {
+    "gemm_addmm_f32": (_int, [_vp, _int, _vp, _vp, _vp, _i64, _i64, _i64, _dbl, _dbl, _vp]),
+    "gemm_addmm_f32_ex": (_int, [_vp, _int, _vp, _vp, _vp, _i64, _i64, _i64, _dbl, _dbl, _int,
+                                 _vp]),
+    "conv2d_gemm_f32": (_int, [_vp, _vp, _vp, _vp] + [_i64] * 10 + [_vp]),
+    "conv2d_gemm_f32_ex": (_int, [_vp, _vp, _vp, _vp] + [_i64] * 10 + [_int, _vp]),
+    "conv2d_gemm_f32_nd": (_int, [_vp, _vp, _vp, _vp] + [_i64] * 13 + [_int, _vp]),
+    "imc_status_string": (ctypes.c_char_p, [_int]),
+    "imc_last_kernel": (_int, []),
+    "imc_launch_count": (ctypes.c_uint64, []),
+    "imc_check_device_error": (_int, [_vp]),
+    "imc_version": (_int, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ImcError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})" if what else
+                         f"{status_string(status)} ({status})")
+
+
+def load(path: str | None = None):
+    """Loads libimc.so (once) and declares every exported signature."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError(f"{p} is not built; run python -m addmm_implicit_im2col_gb300.build")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+# ------------------------------------------------------ raw C-ABI mirrors
+def gemm_addmm_f32(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, stream) -> int:
+    return load().gemm_addmm_f32(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, stream)
+
+
+def gemm_addmm_f32_ex(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, stream) -> int:
+    return load().gemm_addmm_f32_ex(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode,
+                                    stream)
+
+
+def conv2d_gemm_f32(x, w, bias, out, B, IC, H, W, OC, KH, KW, stride, pad, dilation,
+                    stream) -> int:
+    return load().conv2d_gemm_f32(x, w, bias, out, B, IC, H, W, OC, KH, KW, stride, pad,
+                                  dilation, stream)
+
+
+def conv2d_gemm_f32_ex(x, w, bias, out, B, IC, H, W, OC, KH, KW, stride, pad, dilation, mode,
+                       stream) -> int:
+    return load().conv2d_gemm_f32_ex(x, w, bias, out, B, IC, H, W, OC, KH, KW, stride, pad,
+                                     dilation, mode, stream)
+
+
+def conv2d_gemm_f32_nd(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, mode,
+                       stream) -> int:
+    return load().conv2d_gemm_f32_nd(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW,
+                                     dH, dW, mode, stream)
+
+
+def status_string(status: int) -> str:
+    return load().imc_status_string(status).decode()
+
+
+def last_kernel() -> str:
+    return KERNELS.get(load().imc_last_kernel(), "unknown")
+
+
+def launch_count() -> int:
+    return int(load().imc_launch_count())
+
+
+def check_device_error(stream=None) -> int:
+    return load().imc_check_device_error(stream)
+
+
+# ------------------------------------------------------- torch-level API
+def _stream_ptr(device):
+    import torch
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_tensor(t, name, ndim=None):
+    import torch
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    if ndim is not None and t.dim() not in ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+
+
+def addmm(self, mat1, mat2, *, beta=1.0, alpha=1.0, mode="default", out=None):
+    """out = beta*self + alpha*(mat1 @ mat2) on the GPU (aten.addmm semantics).
+
+    self is [N] or [M, N]; alpha and beta default to 1.0.  ``mode`` is one of
+    ``MODES``.  Returns ``out`` (allocated with torch when not given).
+    """
+    import torch
+    _check_tensor(mat1, "mat1", (2,))
+    _check_tensor(mat2, "mat2", (2,))
+    _check_tensor(self, "self", (1, 2))
+    M, K = mat1.shape
+    K2, N = mat2.shape
+    if K2 != K:
+        raise ValueError(f"mat2 must be [K, N] = [{K}, N], got {list(mat2.shape)}")
+    self_2d = 0
+    if self is not None:
+        if self.dim() == 2:
+            if list(self.shape) != [M, N]:
+                raise ValueError("a 2-D self must be [M, N]")
+            self_2d = 1
+        elif self.shape[0] != N:
+            raise ValueError("a 1-D self must be [N]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=mat1.device)
+    else:
+        _check_tensor(out, "out", (2,))
+    rc = gemm_addmm_f32_ex(_ptr(self), self_2d, _ptr(mat1), _ptr(mat2), _ptr(out), M, N, K,
+                           float(beta), float(alpha), MODES[mode], _stream_ptr(mat1.device))
+    if rc != IMC_OK:
+        raise ImcError(rc, "gemm_addmm_f32")
+    return out
+
+
+def conv_out_size(n, k, stride, pad, dil) -> int:
+    span = n + 2 * pad - dil * (k - 1) - 1
+    return -1 if span < 0 else span // stride + 1
+
+
+def _pair(v):
+    return (int(v[0]), int(v[1])) if isinstance(v, (tuple, list)) else (int(v), int(v))
+
+
+def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, *, mode="default", out=None):
+    """groups==1 NCHW conv2d via the implicit-im2col GEMM.
+
+    x [B, IC, H, W], w [OC, IC, KH, KW], bias [OC] or None; stride, padding and
+    dilation are ints or (h, w) pairs.  Returns out [B, OC, OH, OW].
+    """
+    import torch
+    _check_tensor(x, "x", (4,))
+    _check_tensor(w, "w", (4,))
+    _check_tensor(bias, "bias", (1,))
+    B, IC, H, W = x.shape
+    OC, IC2, KH, KW = w.shape
+    if IC2 != IC:
+        raise ValueError("weight must be [OC, IC, KH, KW] with the input's IC (groups == 1)")
+    if bias is not None and bias.shape[0] != OC:
+        raise ValueError("bias must be [OC]")
+    sH, sW = _pair(stride)
+    pH, pW = _pair(padding)
+    dH, dW = _pair(dilation)
+    OH = conv_out_size(H, KH, sH, pH, dH)
+    OW = conv_out_size(W, KW, sW, pW, dW)
+    if OH < 1 or OW < 1:
+        raise ValueError("empty convolution output")
+    if out is None:
+        out = torch.empty((B, OC, OH, OW), dtype=torch.float32, device=x.device)
+    else:
+        _check_tensor(out, "out", (4,))
+    rc = conv2d_gemm_f32_nd(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), B, IC, H, W, OC, KH, KW,
+                            sH, sW, pH, pW, dH, dW, MODES[mode], _stream_ptr(x.device))
+    if rc != IMC_OK:
+        raise ImcError(rc, "conv2d_gemm_f32")
+    return out

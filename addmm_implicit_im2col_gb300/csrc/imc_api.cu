@@ -1,0 +1,270 @@
+// C ABI of libimc (include/imc.h): argument checks, kernel choice, launch.
+//
+// Every check runs before anything is enqueued, so a call that fails has
+// launched nothing -- the "throw before leak" rule of the ExecuTorch WebGPU
+// conv2d page (Implementation paragraph: both dispatch grids are computed
+// before any buffer is allocated).  The addmm checks follow the "Add
+// optimized addmm op" page's Implementation and Constraints paragraphs
+// (non-null buffers, mat2 exactly [K,N], self [N] or [M,N], fp32 only -- the
+// last is fixed by the float* types here).  The 65535-workgroup cap those
+// pages state is a WebGPU dispatch limit and is not reproduced.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "imc.h"
+#include "imc_internal.cuh"
+
+namespace imc {
+
+static std::atomic<uint64_t> g_launches{0};
+static thread_local int t_last_kernel = IMC_KERNEL_NONE;
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int g_sm_count[kMaxDevices];
+int g_dev_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+
+// IMC_OK when the current device is compute capability 10.3.
+int check_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return IMC_ERR_DEVICE;
+  }
+  if (dev >= kMaxDevices) return IMC_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return IMC_ERR_DEVICE;
+    }
+    g_sm_count[dev] = sms;
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return g_dev_ok[dev] == 1 ? IMC_OK : IMC_ERR_DEVICE;
+}
+
+bool overlaps(const void* a, uint64_t abytes, const void* b, uint64_t bbytes) {
+  if (!a || !b || abytes == 0 || bbytes == 0) return false;
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+constexpr int64_t kMaxDim = 0x7fffffffLL;
+// Problems smaller than this many multiply-adds run on the SIMT kernel: the
+// tensor-core kernel's fixed set-up (TMEM allocation, pipeline fill) is
+// larger than the whole job there.
+constexpr int64_t kTinyMacs = int64_t(1) << 22;
+
+int finish(cudaError_t e, int kernel) {
+  if (e != cudaSuccess) return IMC_ERR_CUDA;
+  t_last_kernel = kernel;
+  return IMC_OK;
+}
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < kMaxDevices) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_sm_count[dev] > 0) return g_sm_count[dev];
+  }
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace imc
+
+using namespace imc;
+
+extern "C" {
+
+int gemm_addmm_f32_ex(const float* self, int self_2d, const float* mat1, const float* mat2,
+                      float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                      int mode, void* stream) {
+  if (self_2d != 0 && self_2d != 1) return IMC_ERR_ARG;
+  if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return IMC_ERR_ARG;
+  if (!std::isfinite(beta) || !std::isfinite(alpha)) return IMC_ERR_ARG;
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return IMC_ERR_SHAPE;
+  if (M == 0 || N == 0) {
+    t_last_kernel = IMC_KERNEL_NONE;
+    return IMC_OK;
+  }
+  const bool read_self = beta != 0.0;
+  const bool read_ops = alpha != 0.0 && K > 0;
+  if (!out) return IMC_ERR_NULL;
+  if (read_self && !self) return IMC_ERR_NULL;
+  if (read_ops && (!mat1 || !mat2)) return IMC_ERR_NULL;
+
+  const uint64_t out_bytes = (uint64_t)M * (uint64_t)N * 4u;
+  if (read_ops && (overlaps(out, out_bytes, mat1, (uint64_t)M * K * 4u) ||
+                   overlaps(out, out_bytes, mat2, (uint64_t)K * N * 4u)))
+    return IMC_ERR_ALIAS;
+  if (read_self) {
+    const uint64_t self_bytes = (uint64_t)(self_2d ? M * N : N) * 4u;
+    const bool exact_inplace = self_2d && (const void*)self == (const void*)out;
+    if (!exact_inplace && overlaps(out, out_bytes, self, self_bytes)) return IMC_ERR_ALIAS;
+  }
+  const int dev = check_device();
+  if (dev != IMC_OK) return dev;
+
+  GemmArgs a;
+  a.self = self;
+  a.mat1 = mat1;
+  a.mat2 = mat2;
+  a.out = out;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.alpha = (float)alpha;
+  a.beta = (float)beta;
+  a.self_2d = self_2d;
+  a.read_self = read_self ? 1 : 0;
+  a.vec_out = (N % 4 == 0) && aligned16(out) && (!read_self || aligned16(self)) ? 1 : 0;
+  cudaStream_t s = (cudaStream_t)stream;
+
+  if (!read_ops) return finish(launch_fill_gemm(a, s), IMC_KERNEL_FILL);
+
+  const bool tc_ok = tc_gemm_supported(a);
+  const bool force_tc = mode == IMC_MODE_FORCE_TC3 || mode == IMC_MODE_FORCE_TC1;
+  if (force_tc && !tc_ok) return IMC_ERR_SHAPE;
+  bool use_tc = force_tc || (mode != IMC_MODE_SIMT && tc_ok && (double)M * N * K >= (double)kTinyMacs);
+  if (!use_tc) return finish(launch_simt_gemm(a, s), IMC_KERNEL_SIMT);
+  const bool three = mode == IMC_MODE_DEFAULT || mode == IMC_MODE_FORCE_TC3;
+  return finish(launch_tc_gemm(a, three, s), three ? IMC_KERNEL_TC3 : IMC_KERNEL_TC1);
+}
+
+int gemm_addmm_f32(const float* self, int self_2d, const float* mat1, const float* mat2,
+                   float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                   void* stream) {
+  return gemm_addmm_f32_ex(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha,
+                           IMC_MODE_DEFAULT, stream);
+}
+
+int conv2d_gemm_f32_nd(const float* x, const float* w, const float* bias, float* out, int64_t B,
+                       int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
+                       int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW,
+                       int mode, void* stream) {
+  if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return IMC_ERR_ARG;
+  if (B < 0 || IC < 0 || OC < 0 || H < 1 || W < 1 || KH < 1 || KW < 1) return IMC_ERR_SHAPE;
+  if (sH < 1 || sW < 1 || pH < 0 || pW < 0 || dH < 1 || dW < 1) return IMC_ERR_SHAPE;
+  if (B > kMaxDim || IC > kMaxDim || OC > kMaxDim || H > kMaxDim || W > kMaxDim ||
+      KH > kMaxDim || KW > kMaxDim || sH > kMaxDim || sW > kMaxDim || pH > kMaxDim ||
+      pW > kMaxDim || dH > kMaxDim || dW > kMaxDim)
+    return IMC_ERR_SHAPE;
+  // OH = floor((H + 2*pH - dH*(KH-1) - 1) / sH) + 1, likewise OW.
+  const int64_t spanH = H + 2 * pH - dH * (KH - 1) - 1;
+  const int64_t spanW = W + 2 * pW - dW * (KW - 1) - 1;
+  if (spanH < 0 || spanW < 0) return IMC_ERR_SHAPE;
+  const int64_t OH = spanH / sH + 1, OW = spanW / sW + 1;
+  // Every tensor stays below 2^31 elements (32-bit element offsets inside).
+  const double lim = 2147483647.0;
+  if ((double)B * IC * H * W > lim || (double)OC * IC * KH * KW > lim ||
+      (double)B * OC * OH * OW > lim || (double)IC * KH * KW > lim || (double)B * OH * OW > lim)
+    return IMC_ERR_SHAPE;
+  if (B == 0 || OC == 0) {
+    t_last_kernel = IMC_KERNEL_NONE;
+    return IMC_OK;
+  }
+  const int64_t K = IC * KH * KW;
+  if (!out) return IMC_ERR_NULL;
+  if (K > 0 && (!x || !w)) return IMC_ERR_NULL;
+  const uint64_t out_bytes = (uint64_t)(B * OC * OH * OW) * 4u;
+  if ((K > 0 && (overlaps(out, out_bytes, x, (uint64_t)(B * IC * H * W) * 4u) ||
+                 overlaps(out, out_bytes, w, (uint64_t)(OC * K) * 4u))) ||
+      overlaps(out, out_bytes, bias, (uint64_t)OC * 4u))
+    return IMC_ERR_ALIAS;
+  const int dev = check_device();
+  if (dev != IMC_OK) return dev;
+
+  ConvArgs c;
+  c.x = x;
+  c.w = w;
+  c.bias = bias;
+  c.out = out;
+  c.B = (int)B;
+  c.IC = (int)IC;
+  c.H = (int)H;
+  c.W = (int)W;
+  c.OC = (int)OC;
+  c.KH = (int)KH;
+  c.KW = (int)KW;
+  c.sH = (int)sH;
+  c.sW = (int)sW;
+  c.pH = (int)pH;
+  c.pW = (int)pW;
+  c.dH = (int)dH;
+  c.dW = (int)dW;
+  c.OH = (int)OH;
+  c.OW = (int)OW;
+  c.M = OC;
+  c.N = B * OH * OW;
+  c.K = K;
+  c.vec_out = ((OH * OW) % 4 == 0) && aligned16(out) ? 1 : 0;
+  cudaStream_t s = (cudaStream_t)stream;
+
+  if (K == 0) return finish(launch_fill_conv(c, s), IMC_KERNEL_FILL);
+  const bool tc_ok = tc_conv_supported(c);
+  const bool force_tc = mode == IMC_MODE_FORCE_TC3 || mode == IMC_MODE_FORCE_TC1;
+  if (force_tc && !tc_ok) return IMC_ERR_SHAPE;
+  bool use_tc = force_tc || (mode != IMC_MODE_SIMT && tc_ok && (double)c.M * c.N * c.K >= (double)kTinyMacs);
+  if (!use_tc) return finish(launch_simt_conv(c, s), IMC_KERNEL_SIMT);
+  const bool three = mode == IMC_MODE_DEFAULT || mode == IMC_MODE_FORCE_TC3;
+  return finish(launch_tc_conv(c, three, s), three ? IMC_KERNEL_TC3 : IMC_KERNEL_TC1);
+}
+
+int conv2d_gemm_f32_ex(const float* x, const float* w, const float* bias, float* out, int64_t B,
+                       int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
+                       int64_t stride, int64_t pad, int64_t dilation, int mode, void* stream) {
+  return conv2d_gemm_f32_nd(x, w, bias, out, B, IC, H, W, OC, KH, KW, stride, stride, pad, pad,
+                            dilation, dilation, mode, stream);
+}
+
+int conv2d_gemm_f32(const float* x, const float* w, const float* bias, float* out, int64_t B,
+                    int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
+                    int64_t stride, int64_t pad, int64_t dilation, void* stream) {
+  return conv2d_gemm_f32_nd(x, w, bias, out, B, IC, H, W, OC, KH, KW, stride, stride, pad, pad,
+                            dilation, dilation, IMC_MODE_DEFAULT, stream);
+}
+
+const char* imc_status_string(int status) {
+  switch (status) {
+    case IMC_OK: return "IMC_OK";
+    case IMC_ERR_NULL: return "IMC_ERR_NULL: a required pointer is NULL";
+    case IMC_ERR_SHAPE: return "IMC_ERR_SHAPE: a size is out of range or the output is empty";
+    case IMC_ERR_ARG: return "IMC_ERR_ARG: bad flag, mode or scalar";
+    case IMC_ERR_ALIAS: return "IMC_ERR_ALIAS: the output overlaps an input";
+    case IMC_ERR_CUDA: return "IMC_ERR_CUDA: a CUDA call or kernel launch failed";
+    case IMC_ERR_TIMEOUT: return "IMC_ERR_TIMEOUT: a kernel gave up waiting on a barrier";
+    case IMC_ERR_DEVICE: return "IMC_ERR_DEVICE: no usable compute capability 10.3 device";
+    default: return "IMC_ERR_UNKNOWN";
+  }
+}
+
+int imc_last_kernel(void) { return t_last_kernel; }
+
+uint64_t imc_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int imc_check_device_error(void* stream) {
+  const int dev = check_device();
+  if (dev != IMC_OK) return dev;
+  int v = 0;
+  if (tc_take_watchdog(&v, (cudaStream_t)stream) != cudaSuccess) return IMC_ERR_CUDA;
+  return v != 0 ? IMC_ERR_TIMEOUT : IMC_OK;
+}
+
+int imc_version(void) { return 100; }
+
+}  // extern "C"

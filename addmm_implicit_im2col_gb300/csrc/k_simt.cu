@@ -1,0 +1,202 @@
+// SIMT fp32 FFMA fallback: a shared-memory tiled GEMM with register blocking
+// for shapes the tensor-core path does not take (tiny problems, K or N not a
+// multiple of 4, unaligned operands) and for IMC_MODE_SIMT.
+//
+// This is the design family of the ExecuTorch WebGPU "Add optimized addmm op"
+// page (Implementation paragraph: a workgroup stages tiles of both operands in
+// shared memory, synchronises, and every thread accumulates a 4x4 register
+// sub-tile over the k-tiles), here with a 64x64 output tile, 16-deep k-tiles
+// and 256 threads.  The conv variant samples the im2col operand on the fly as
+// the "et_vk conv2d ... im2col tiled GEMM" page's Implementation paragraph
+// describes (n -> (b, oh, ow), kk -> (ic, kh, kw), out-of-range taps read 0).
+#include "imc_internal.cuh"
+
+namespace imc {
+namespace {
+
+constexpr int BM = 64, BN = 64, BK = 16, THREADS = 256;
+
+struct GemmOperands {
+  GemmArgs a;
+  __device__ __forceinline__ float load_a(int64_t m, int64_t k) const {
+    return a.mat1[m * a.K + k];
+  }
+  __device__ __forceinline__ float load_b(int64_t k, int64_t n) const {
+    return a.mat2[k * a.N + n];
+  }
+  __device__ __forceinline__ void store_row4(int64_t m, int64_t n0, const float* acc) const {
+    float* o = a.out + m * a.N;
+    const float* sp = a.self_2d ? a.self + m * a.N : a.self;
+    if (a.vec_out && n0 + 3 < a.N) {
+      float4 r;
+      float4 sv = a.read_self ? *reinterpret_cast<const float4*>(sp + n0) : make_float4(0, 0, 0, 0);
+      r.x = a.read_self ? fmaf(a.alpha, acc[0], a.beta * sv.x) : a.alpha * acc[0];
+      r.y = a.read_self ? fmaf(a.alpha, acc[1], a.beta * sv.y) : a.alpha * acc[1];
+      r.z = a.read_self ? fmaf(a.alpha, acc[2], a.beta * sv.z) : a.alpha * acc[2];
+      r.w = a.read_self ? fmaf(a.alpha, acc[3], a.beta * sv.w) : a.alpha * acc[3];
+      *reinterpret_cast<float4*>(o + n0) = r;
+      return;
+    }
+    for (int j = 0; j < 4; ++j) {
+      int64_t n = n0 + j;
+      if (n >= a.N) break;
+      o[n] = a.read_self ? fmaf(a.alpha, acc[j], a.beta * sp[n]) : a.alpha * acc[j];
+    }
+  }
+  __device__ __forceinline__ int64_t M() const { return a.M; }
+  __device__ __forceinline__ int64_t N() const { return a.N; }
+  __device__ __forceinline__ int64_t K() const { return a.K; }
+};
+
+struct ConvOperands {
+  ConvArgs c;
+  __device__ __forceinline__ float load_a(int64_t m, int64_t k) const {
+    return c.w[m * c.K + k];  // weight viewed as [OC, IC*KH*KW]
+  }
+  // im2col sample: column n = (b*OH + oh)*OW + ow, row kk = (ic*KH + kh)*KW + kw.
+  __device__ __forceinline__ float load_b(int64_t kk, int64_t n) const {
+    const int ow = (int)(n % c.OW);
+    const int64_t t = n / c.OW;
+    const int oh = (int)(t % c.OH);
+    const int b = (int)(t / c.OH);
+    const int kw = (int)(kk % c.KW);
+    const int64_t u = kk / c.KW;
+    const int kh = (int)(u % c.KH);
+    const int ic = (int)(u / c.KH);
+    const int ih = oh * c.sH - c.pH + kh * c.dH;
+    const int iw = ow * c.sW - c.pW + kw * c.dW;
+    if (ih < 0 || ih >= c.H || iw < 0 || iw >= c.W) return 0.0f;
+    return c.x[(((int64_t)b * c.IC + ic) * c.H + ih) * c.W + iw];
+  }
+  __device__ __forceinline__ void store_row4(int64_t m, int64_t n0, const float* acc) const {
+    const float bv = c.bias ? c.bias[m] : 0.0f;
+    const int64_t P = (int64_t)c.OH * c.OW;
+    for (int j = 0; j < 4; ++j) {
+      int64_t n = n0 + j;
+      if (n >= c.N) break;
+      const int64_t b = n / P, p = n - b * P;
+      c.out[(b * c.OC + m) * P + p] = acc[j] + bv;
+    }
+  }
+  __device__ __forceinline__ int64_t M() const { return c.M; }
+  __device__ __forceinline__ int64_t N() const { return c.N; }
+  __device__ __forceinline__ int64_t K() const { return c.K; }
+};
+
+template <class Ops>
+__global__ __launch_bounds__(THREADS) void k_simt(const Ops ops) {
+  __shared__ __align__(16) float As[BK][BM];
+  __shared__ __align__(16) float Bs[BK][BN];
+  const int t = threadIdx.x;
+  const int tx = t % 16, ty = t / 16;
+  const int64_t M = ops.M(), N = ops.N(), K = ops.K();
+  const int64_t tiles_n = (N + BN - 1) / BN;
+  const int64_t m0 = ((int64_t)blockIdx.x / tiles_n) * BM, n0 = ((int64_t)blockIdx.x % tiles_n) * BN;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+
+  for (int64_t k0 = 0; k0 < K; k0 += BK) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = t + i * THREADS;
+      const int ml = e / BK, kl = e % BK;  // consecutive threads walk k (row-major A)
+      const int64_t m = m0 + ml, k = k0 + kl;
+      As[kl][ml] = (m < M && k < K) ? ops.load_a(m, k) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = t + i * THREADS;
+      const int kl = e / BN, nl = e % BN;  // consecutive threads walk n
+      const int64_t k = k0 + kl, n = n0 + nl;
+      Bs[kl][nl] = (k < K && n < N) ? ops.load_b(k, n) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      const float4 av = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+      const float4 bv = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+      const float ar[4] = {av.x, av.y, av.z, av.w};
+      const float br[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t m = m0 + ty * 4 + i;
+    if (m < M) ops.store_row4(m, n0 + tx * 4, acc[i]);
+  }
+}
+
+__global__ void k_fill_gemm(const GemmArgs a) {
+  const int64_t total = a.M * a.N;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = e % a.N;
+    float v = 0.0f;
+    if (a.read_self) v = a.beta * (a.self_2d ? a.self[e] : a.self[n]);
+    a.out[e] = v;
+  }
+}
+
+__global__ void k_fill_conv(const ConvArgs c) {
+  const int64_t P = (int64_t)c.OH * c.OW;
+  const int64_t total = (int64_t)c.B * c.OC * P;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t oc = (e / P) % c.OC;
+    c.out[e] = c.bias ? c.bias[oc] : 0.0f;
+  }
+}
+
+unsigned fill_blocks(int64_t total) {
+  int64_t b = (total + 255) / 256;
+  int64_t cap = (int64_t)device_sm_count() * 8;
+  return (unsigned)(b < cap ? (b > 0 ? b : 1) : cap);
+}
+
+}  // namespace
+
+// One CTA per 64x64 output tile, linear tile index (no per-dimension grid cap).
+static bool simt_grid(int64_t M, int64_t N, unsigned* blocks) {
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  if (tiles > 0x7fffffffLL) return false;
+  *blocks = (unsigned)tiles;
+  return true;
+}
+
+cudaError_t launch_simt_gemm(const GemmArgs& a, cudaStream_t s) {
+  unsigned grid;
+  if (!simt_grid(a.M, a.N, &grid)) return cudaErrorInvalidConfiguration;
+  k_simt<GemmOperands><<<grid, THREADS, 0, s>>>(GemmOperands{a});
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_simt_conv(const ConvArgs& c, cudaStream_t s) {
+  unsigned grid;
+  if (!simt_grid(c.M, c.N, &grid)) return cudaErrorInvalidConfiguration;
+  k_simt<ConvOperands><<<grid, THREADS, 0, s>>>(ConvOperands{c});
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_gemm(const GemmArgs& a, cudaStream_t s) {
+  k_fill_gemm<<<fill_blocks(a.M * a.N), 256, 0, s>>>(a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_conv(const ConvArgs& c, cudaStream_t s) {
+  k_fill_conv<<<fill_blocks((int64_t)c.B * c.OC * c.OH * c.OW), 256, 0, s>>>(c);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace imc

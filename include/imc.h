@@ -1,0 +1,163 @@
+/*
+ * imc.h -- C ABI of libimc: fp32 addmm and groups==1 NCHW conv2d, both run as
+ * one tiled GEMM with a fused epilogue on NVIDIA sm_103a (GB300).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major fp32
+ *    data owned by the caller.  The library never allocates, frees or keeps a
+ *    pointer to them beyond the call; it may cache CUDA function attributes
+ *    per device.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously on it; no entry point synchronises the host.
+ *  - Every argument is checked before anything is launched.  A call that
+ *    returns an error has enqueued nothing and written nothing.
+ *  - Return value: IMC_OK (0) or one of the negative IMC_ERR_* codes below;
+ *    imc_status_string() names them.  IMC_ERR_CUDA means a CUDA runtime call
+ *    failed (for example a launch error); the CUDA error is left for the
+ *    caller to read with cudaGetLastError().
+ *  - Arithmetic is fp32 in and out.  The default mode (IMC_MODE_DEFAULT)
+ *    keeps fp32 accuracy: each product is split into TF32 pieces
+ *    (3xTF32) on the tensor cores, or computed with fp32 FMA on the SIMT
+ *    fallback.  IMC_MODE_TF32 is an explicitly requested faster mode with
+ *    single TF32 products (about 3 fewer decimal digits).
+ */
+#ifndef IMC_H
+#define IMC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+#define IMC_OK 0
+#define IMC_ERR_NULL (-1)    /* a required pointer is NULL                       */
+#define IMC_ERR_SHAPE (-2)   /* a size is negative / out of range, empty output  */
+#define IMC_ERR_ARG (-3)     /* bad flag or mode value, non-finite alpha / beta  */
+#define IMC_ERR_ALIAS (-4)   /* the output overlaps an input it may not overlap   */
+#define IMC_ERR_CUDA (-5)    /* a CUDA runtime call or kernel launch failed       */
+#define IMC_ERR_TIMEOUT (-6) /* a kernel gave up waiting on one of its barriers   */
+#define IMC_ERR_DEVICE (-7)  /* no usable device of compute capability 10.3       */
+
+/* ------------------------------------------------------------------- modes */
+#define IMC_MODE_DEFAULT 0 /* fp32-accurate: 3xTF32 tensor cores, SIMT when needed */
+#define IMC_MODE_TF32 1    /* explicit 1xTF32 fast mode (SIMT when the shape needs) */
+#define IMC_MODE_SIMT 2    /* force the fp32 FFMA SIMT kernel                       */
+#define IMC_MODE_FORCE_TC3 3 /* force the tcgen05 3xTF32 kernel (IMC_ERR_SHAPE if the
+                                shape cannot take it); for tests and measurement    */
+#define IMC_MODE_FORCE_TC1 4 /* force the tcgen05 1xTF32 kernel, likewise          */
+
+/* ---------------------------------------- kernel ids (imc_last_kernel()) */
+#define IMC_KERNEL_NONE 0 /* nothing launched (empty problem)              */
+#define IMC_KERNEL_TC3 1  /* tcgen05 3xTF32 kernel                         */
+#define IMC_KERNEL_TC1 2  /* tcgen05 1xTF32 kernel                         */
+#define IMC_KERNEL_SIMT 3 /* fp32 FFMA SIMT kernel                         */
+#define IMC_KERNEL_FILL 4 /* epilogue only: K == 0 or alpha == 0           */
+
+/*
+ * gemm_addmm_f32 -- aten.addmm semantics.
+ *
+ * Source: ExecuTorch WebGPU pull request "Add optimized addmm op",
+ * Solution and Implementation paragraphs (out = beta*self + alpha*(mat1 @
+ * mat2); self broadcast from [N] or given as a full [M,N]; mat2 read as
+ * mat2[k*N + n]; AddmmParams carries M, N, K, self_2d, beta, alpha) and its
+ * Constraints paragraph (fp32 only; 2-D operands; mat2 exactly [K,N]).
+ *
+ *   out[i,j] = beta * self(i,j) + alpha * sum_{k<K} mat1[i*K + k] * mat2[k*N + j]
+ *   self(i,j) = self[j]          when self_2d == 0  (self is [N])
+ *             = self[i*N + j]    when self_2d == 1  (self is [M,N])
+ *
+ * Arguments
+ *   self    [N] or [M,N] fp32; may be NULL only when beta == 0.  Not read
+ *           when beta == 0 (NaN / Inf in it do not propagate).
+ *   self_2d 0 or 1 as above; any other value is IMC_ERR_ARG.
+ *   mat1    [M,K] fp32 row-major.   mat2 [K,N] fp32 row-major.
+ *           Neither is read when alpha == 0 or K == 0.
+ *   out     [M,N] fp32 row-major, written in full.  out may equal self when
+ *           self_2d == 1 (in-place addmm); any other overlap of out with an
+ *           input is IMC_ERR_ALIAS.
+ *   M, N, K sizes, each in [0, 2^31).  M == 0 or N == 0: nothing to do, OK.
+ *           K == 0: out = beta*self (the empty sum is 0).
+ *   beta, alpha  finite scalars (the pages default both to 1.0, which the
+ *           Python binding supplies); used in fp32.
+ *   stream  cudaStream_t or NULL.
+ * Kernel choice: the tcgen05 path needs K % 4 == 0, N % 4 == 0 and 16-byte
+ * aligned mat1 / mat2 (TMA row strides); other shapes, and tiny problems,
+ * take the SIMT kernel.  imc_last_kernel() reports which ran.
+ */
+int gemm_addmm_f32(const float* self, int self_2d, const float* mat1, const float* mat2,
+                   float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                   void* stream);
+
+/* gemm_addmm_f32 with an explicit mode (IMC_MODE_*); mode IMC_MODE_DEFAULT
+ * is exactly gemm_addmm_f32.  Any other mode value is IMC_ERR_ARG. */
+int gemm_addmm_f32_ex(const float* self, int self_2d, const float* mat1, const float* mat2,
+                      float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                      int mode, void* stream);
+
+/*
+ * conv2d_gemm_f32 -- groups==1, non-transposed NCHW convolution lowered to
+ * an implicit-im2col GEMM.
+ *
+ * Source: ExecuTorch WebGPU pull request "et_vk conv2d: route standard
+ * (groups==1) conv through an im2col tiled GEMM", Solution paragraph
+ * (M = OC, N = B*OH*OW, K = IC*KH*KW; out-of-range taps read 0.0, which
+ * implements padding) and Implementation paragraph (A = weight viewed as
+ * [OC, K]; B sampled on the fly with n -> (b, oh, ow), kk -> (ic, kh, kw),
+ * ih = oh*sH - pH + kh*dH and likewise iw; bias per row (OC); NCHW output).
+ *
+ *   out[b,oc,oh,ow] = bias[oc] + sum_{ic,kh,kw} w[oc,ic,kh,kw] * x[b,ic,ih,iw]
+ *   OH = floor((H + 2*pad - dilation*(KH-1) - 1) / stride) + 1, likewise OW.
+ *
+ * Arguments
+ *   x     [B,IC,H,W] fp32 contiguous.      w [OC,IC,KH,KW] fp32 contiguous.
+ *   bias  [OC] fp32, or NULL for no bias.  out [B,OC,OH,OW] fp32, written in
+ *         full; it may not overlap x, w or bias (IMC_ERR_ALIAS).
+ *   B, IC, OC >= 0 (B == 0 or OC == 0: nothing to do; IC == 0: out = bias);
+ *   H, W, KH, KW >= 1; stride >= 1, pad >= 0, dilation >= 1, applied to
+ *   both axes; OH, OW must come out >= 1 (else IMC_ERR_SHAPE).  Every
+ *   tensor must hold fewer than 2^31 elements.
+ * Kernel choice: the tcgen05 path gathers the im2col operand itself and has
+ * no alignment rule on x; tiny problems take the SIMT kernel.
+ */
+int conv2d_gemm_f32(const float* x, const float* w, const float* bias, float* out, int64_t B,
+                    int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
+                    int64_t stride, int64_t pad, int64_t dilation, void* stream);
+
+/* conv2d_gemm_f32 with an explicit mode (IMC_MODE_*). */
+int conv2d_gemm_f32_ex(const float* x, const float* w, const float* bias, float* out, int64_t B,
+                       int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
+                       int64_t stride, int64_t pad, int64_t dilation, int mode, void* stream);
+
+/* conv2d_gemm_f32_ex with separate height / width stride, padding and
+ * dilation, as in the per-axis index map ih = oh*sH - pH + kh*dH,
+ * iw = ow*sW - pW + kw*dW of the same Implementation paragraph. */
+int conv2d_gemm_f32_nd(const float* x, const float* w, const float* bias, float* out, int64_t B,
+                       int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
+                       int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW,
+                       int mode, void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* imc_status_string(int status);
+
+/* IMC_KERNEL_* id of the kernel the calling host thread's last successful
+ * call launched. */
+int imc_last_kernel(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t imc_launch_count(void);
+
+/* Synchronises `stream`, then reads and clears the current device's
+ * watchdog word.  Returns IMC_OK, IMC_ERR_TIMEOUT if a kernel gave up on a
+ * barrier wait since the last check, or IMC_ERR_CUDA. */
+int imc_check_device_error(void* stream);
+
+/* Library ABI version (major * 100 + minor). */
+int imc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* IMC_H */

@@ -1,0 +1,153 @@
+"""C-ABI boundary checks that need no GPU.
+
+The library must load, export every function include/imc.h declares, and
+reject bad arguments with the documented status before touching CUDA.  On a
+machine without a GPU a well-formed call must fail loudly (IMC_ERR_DEVICE),
+never fall back to host code.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from addmm_implicit_im2col_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "imc.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("gemm_addmm_f32", "conv2d_gemm_f32", "gemm_addmm_f32_ex", "conv2d_gemm_f32_ex",
+                 "conv2d_gemm_f32_nd", "imc_status_string"):
+        assert want in names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), f"libimc.so does not export {n}"
+        assert n in binding.SIGNATURES, f"binding has no signature for {n}"
+
+
+def test_library_has_no_torch_dependency(lib):
+    # The boundary is plain C: the shared object must not need libtorch.
+    import subprocess
+    out = subprocess.run(["ldd", binding.LIB_PATH], capture_output=True, text=True).stdout
+    assert "torch" not in out and "c10" not in out
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        s = binding.status_string(code)
+        assert s.startswith("IMC_")
+    assert binding.status_string(-99) == "IMC_ERR_UNKNOWN"
+    assert lib.imc_version() >= 100
+
+
+# fake, never dereferenced device addresses (validation runs before any CUDA call)
+P1, P2, P3, P4 = 0x10000000, 0x20000000, 0x30000000, 0x40000000
+
+
+def g(self=P1, self_2d=0, mat1=P2, mat2=P3, out=P4, M=8, N=8, K=8, beta=1.0, alpha=1.0, mode=0):
+    return binding.gemm_addmm_f32_ex(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode,
+                                     None)
+
+
+def test_addmm_argument_errors(lib):
+    assert g(self_2d=2) == binding.IMC_ERR_ARG
+    assert g(mode=7) == binding.IMC_ERR_ARG
+    assert g(mode=-1) == binding.IMC_ERR_ARG
+    assert g(alpha=float("nan")) == binding.IMC_ERR_ARG
+    assert g(beta=float("inf")) == binding.IMC_ERR_ARG
+    assert g(M=-1) == binding.IMC_ERR_SHAPE
+    assert g(K=-5) == binding.IMC_ERR_SHAPE
+    assert g(N=2 ** 31) == binding.IMC_ERR_SHAPE
+    assert g(out=None) == binding.IMC_ERR_NULL
+    assert g(mat1=None) == binding.IMC_ERR_NULL
+    assert g(mat2=None) == binding.IMC_ERR_NULL
+    assert g(self=None) == binding.IMC_ERR_NULL
+    # out overlapping an operand
+    assert g(out=P2 + 16) == binding.IMC_ERR_ALIAS
+    assert g(out=P3) == binding.IMC_ERR_ALIAS
+    # out overlapping a [N] self, or a [M,N] self at an offset
+    assert g(out=P1) == binding.IMC_ERR_ALIAS
+    assert g(self_2d=1, out=P1 + 4) == binding.IMC_ERR_ALIAS
+
+
+def test_addmm_unread_operands_may_be_null(lib):
+    # beta == 0: self is not read; alpha == 0 or K == 0: operands are not read.
+    # These pass validation and then need a device.
+    assert g(self=None, beta=0.0) == binding.IMC_ERR_DEVICE
+    assert g(mat1=None, mat2=None, alpha=0.0) == binding.IMC_ERR_DEVICE
+    assert g(mat1=None, mat2=None, K=0) == binding.IMC_ERR_DEVICE
+    # out may equal self for an in-place [M,N] addmm
+    assert g(self_2d=1, self=P4) == binding.IMC_ERR_DEVICE
+
+
+def test_empty_problems_are_noops(lib):
+    assert g(M=0, out=None, mat1=None, mat2=None, self=None) == binding.IMC_OK
+    assert g(N=0) == binding.IMC_OK
+    assert binding.last_kernel() == "none"
+
+
+def c(x=P1, w=P2, bias=P3, out=P4, B=2, IC=3, H=8, W=8, OC=4, KH=3, KW=3, sH=1, sW=1, pH=1, pW=1,
+      dH=1, dW=1, mode=0):
+    return binding.conv2d_gemm_f32_nd(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH,
+                                      dW, mode, None)
+
+
+def test_conv_argument_errors(lib):
+    assert c(mode=9) == binding.IMC_ERR_ARG
+    assert c(B=-1) == binding.IMC_ERR_SHAPE
+    assert c(H=0) == binding.IMC_ERR_SHAPE
+    assert c(KH=0) == binding.IMC_ERR_SHAPE
+    assert c(sW=0) == binding.IMC_ERR_SHAPE
+    assert c(pH=-1) == binding.IMC_ERR_SHAPE
+    assert c(dW=0) == binding.IMC_ERR_SHAPE
+    assert c(H=2, KH=5, pH=0) == binding.IMC_ERR_SHAPE  # empty output
+    assert c(B=1 << 16, IC=1 << 10, H=64, W=64) == binding.IMC_ERR_SHAPE  # 2^38 elements
+    assert c(out=None) == binding.IMC_ERR_NULL
+    assert c(x=None) == binding.IMC_ERR_NULL
+    assert c(w=None) == binding.IMC_ERR_NULL
+    assert c(out=P1) == binding.IMC_ERR_ALIAS
+    assert c(out=P3 - 8) == binding.IMC_ERR_ALIAS
+    assert c(bias=None) == binding.IMC_ERR_DEVICE  # bias is optional
+    assert c(B=0) == binding.IMC_OK
+    assert c(OC=0) == binding.IMC_OK
+    # the symmetric entry point maps onto the per-axis one
+    assert binding.conv2d_gemm_f32(P1, P2, P3, P4, 2, 3, 8, 8, 4, 3, 3, 0, 1, 1,
+                                   None) == binding.IMC_ERR_SHAPE
+    assert binding.conv2d_gemm_f32_ex(P1, P2, P3, P4, 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 5,
+                                      None) == binding.IMC_ERR_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
+def test_no_gpu_fails_loudly(lib):
+    assert g() == binding.IMC_ERR_DEVICE
+    assert c() == binding.IMC_ERR_DEVICE
+    assert binding.check_device_error(None) == binding.IMC_ERR_DEVICE
+
+
+def test_torch_wrappers_validate_before_calling(lib):
+    x = torch.zeros(2, 3)
+    with pytest.raises(ValueError):
+        binding.addmm(torch.zeros(3), x, torch.zeros(3, 4))  # CPU tensors are refused
+    with pytest.raises(TypeError):
+        binding.addmm(None, [[1.0]], x)

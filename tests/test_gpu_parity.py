@@ -1,0 +1,257 @@
+"""GPU parity: the CUDA path against the fp64 CPU oracle, element by element.
+
+Bound (per element): |gpu - ref| <= c * S + 1e-6 with S = sum_k |a_ik * b_kj|
+(conv: sum over in-range taps of |w * x|), c = 1e-5 for the default
+(fp32-accurate) mode and the SIMT kernel, c = 2e-3 for the explicit 1xTF32
+mode.  Integer-valued inputs (|v| <= 4) make every product and partial sum
+exact in fp32 and TF32, so those cases must match bit for bit.
+
+Every call goes through the C ABI (binding.py marshals torch tensors into it)
+and the tests assert which kernel ran.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from addmm_implicit_im2col_gb300 import binding, build, synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"default": 1e-5, "simt": 1e-5, "force_tc3": 1e-5, "tf32": 2e-3, "force_tc1": 2e-3}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    build.build()
+    binding.load()
+    yield
+    assert binding.check_device_error(None) == binding.IMC_OK, "a kernel hit its wait limit"
+
+
+def dev(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def within(got, ref, S, c, what=""):
+    got = np.asarray(got, np.float64)
+    err = np.abs(got - ref)
+    tol = c * S + 1e-6
+    ratio = float((err / tol).max()) if err.size else 0.0
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    assert ratio <= 1.0, f"{what}: worst |err|/tol = {ratio:.3g}"
+    return ratio
+
+
+def run_addmm(s, a, b, beta, alpha, mode, rows=None):
+    out = binding.addmm(dev(s), dev(a), dev(b), beta=beta, alpha=alpha, mode=mode)
+    torch.cuda.synchronize()
+    kern = binding.last_kernel()
+    got = out.cpu().numpy()
+    ref, S = oracle.addmm(s, a, b, beta=beta, alpha=alpha, rows=rows,
+                          self_2d=(s is not None and s.ndim == 2))
+    if rows is not None:
+        got = got[rows]
+    return got, ref, S, kern
+
+
+EXPECT = {"simt": "simt", "force_tc3": "tc3", "force_tc1": "tc1"}
+
+SMALL_ADDMM = [  # M, N, K: several tiles, ragged M / N / K tails
+    (128, 128, 32), (1, 4, 4), (130, 132, 36), (300, 200, 100), (257, 516, 1028),
+    (64, 80, 96), (384, 768, 64), (600, 260, 356),
+]
+
+
+@pytest.mark.parametrize("mode", ["simt", "force_tc3", "force_tc1"])
+@pytest.mark.parametrize("mnk", SMALL_ADDMM, ids=lambda t: "x".join(map(str, t)))
+def test_addmm_small(mode, mnk):
+    M, N, K = mnk
+    for self_2d, alpha, beta in [(False, 1.0, 1.0), (True, 2.0, 0.5), (True, -0.75, 1.25)]:
+        s, a, b = synth.addmm_inputs(M, N, K, self_2d=self_2d, workload=1000 + M + N + K)
+        got, ref, S, kern = run_addmm(s, a, b, beta, alpha, mode)
+        assert kern == EXPECT[mode]
+        within(got, ref, S, TOL[mode], f"{mode} {mnk} self_2d={self_2d}")
+
+
+@pytest.mark.parametrize("mode", ["simt", "force_tc3", "force_tc1"])
+@pytest.mark.parametrize("mnk", [(128, 128, 32), (200, 260, 132), (513, 1024, 2048)],
+                         ids=lambda t: "x".join(map(str, t)))
+def test_addmm_integer_inputs_are_bit_exact(mode, mnk):
+    M, N, K = mnk
+    spec = ("I", -4, 4)
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=True, workload=77, mat1=spec, mat2=spec,
+                                 self_=spec)
+    got, ref, _, kern = run_addmm(s, a, b, 1.0, 1.0, mode)
+    assert kern == EXPECT[mode]
+    assert np.array_equal(got.astype(np.float64), ref), f"max diff {np.abs(got - ref).max()}"
+
+
+def test_addmm_unaligned_shapes_take_simt():
+    for M, N, K in [(70, 33, 40), (70, 40, 33), (5, 7, 3)]:
+        s, a, b = synth.addmm_inputs(M, N, K, self_2d=False, workload=5)
+        got, ref, S, kern = run_addmm(s, a, b, 1.0, 1.0, "default")
+        assert kern == "simt"
+        within(got, ref, S, 1e-5, f"{M}x{N}x{K}")
+        with pytest.raises(binding.ImcError):
+            binding.addmm(dev(s), dev(a), dev(b), mode="force_tc3")
+
+
+@pytest.mark.parametrize("mode", ["default", "simt", "force_tc3"])
+def test_addmm_special_cases(mode):
+    M, N, K = 256, 132, 64
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=True, workload=9)
+    # alpha == 0: out = beta*self, operands never read (NaN there is harmless)
+    a_nan = a.copy()
+    a_nan[3, 5] = np.nan
+    out = binding.addmm(dev(s), dev(a_nan), dev(b), beta=1.5, alpha=0.0, mode=mode)
+    assert binding.last_kernel() == "fill"
+    assert np.array_equal(out.cpu().numpy(), (np.float32(1.5) * s))
+    # beta == 0: self never read
+    s_nan = np.full_like(s, np.nan)
+    got = binding.addmm(dev(s_nan), dev(a), dev(b), beta=0.0, alpha=2.0, mode=mode).cpu().numpy()
+    ref, S = oracle.addmm(None, a, b, beta=0.0, alpha=2.0)
+    within(got, ref, S, 1e-5, "beta=0")
+    # identity mat2 returns alpha*mat1 + beta*self
+    eye = np.eye(K, dtype=np.float32)
+    s2 = synth.uniform(synth.stream_key(0, 9, 5), M * K, -1, 1).reshape(M, K)
+    got = binding.addmm(dev(s2), dev(a), dev(eye), beta=0.5, alpha=1.0, mode=mode).cpu().numpy()
+    ref, S = oracle.addmm(s2, a, eye, beta=0.5, alpha=1.0)
+    within(got, ref, S, 1e-5, "identity")
+    # K == 0: empty sum
+    z = binding.addmm(dev(s), torch.empty((M, 0), device="cuda"), torch.empty((0, N), device="cuda"),
+                      beta=2.0, alpha=1.0, mode=mode)
+    assert np.array_equal(z.cpu().numpy(), np.float32(2.0) * s)
+    # in-place: out is self
+    st = dev(s)
+    binding.addmm(st, dev(a), dev(b), beta=1.0, alpha=1.0, mode=mode, out=st)
+    ref, S = oracle.addmm(s, a, b)
+    within(st.cpu().numpy(), ref, S, 1e-5, "in-place")
+
+
+def test_self_broadcast_equals_full_self():
+    M, N, K = 300, 260, 128
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=False, workload=21)
+    for mode in ("simt", "force_tc3"):
+        r1 = binding.addmm(dev(s), dev(a), dev(b), beta=0.5, alpha=1.5, mode=mode)
+        r2 = binding.addmm(dev(np.tile(s, (M, 1))), dev(a), dev(b), beta=0.5, alpha=1.5, mode=mode)
+        assert torch.equal(r1, r2)
+
+
+@pytest.mark.parametrize("name", [n for n in synth.ADDMM_CASES if "rows" not in
+                                  synth.ADDMM_CASES[n]])
+def test_addmm_workloads(name):
+    c, s, a, b = synth.make_addmm_case(name)
+    rows = synth.checked_rows(name, c["M"], 256) if c["M"] > 256 else None
+    for mode in ("default", "tf32"):
+        got, ref, S, kern = run_addmm(s, a, b, c["beta"], c["alpha"], mode, rows=rows)
+        within(got, ref, S, TOL[mode], f"{name} {mode} ({kern})")
+
+
+@pytest.mark.parametrize("name", [n for n in synth.ADDMM_CASES if "rows" in
+                                  synth.ADDMM_CASES[n]])
+def test_addmm_large_workloads_sampled_rows(name):
+    c, s, a, b = synth.make_addmm_case(name)
+    rows = synth.checked_rows(name, c["M"], c["rows"])
+    got, ref, S, kern = run_addmm(s, a, b, c["beta"], c["alpha"], "default", rows=rows)
+    assert kern == "tc3"
+    within(got, ref, S, 1e-5, f"{name}")
+
+
+# ------------------------------------------------------------------- conv
+def run_conv(x, w, bias, stride, pad, dil, mode, channels=None):
+    out = binding.conv2d(dev(x), dev(w), dev(bias), stride, pad, dil, mode=mode)
+    torch.cuda.synchronize()
+    kern = binding.last_kernel()
+    got = out.cpu().numpy()
+    ref, S = oracle.conv2d(x, w, bias, stride, pad, dil, channels=channels)
+    if channels is not None:
+        got = got[:, channels]
+    return got, ref, S, kern
+
+
+SMALL_CONV = [  # B, IC, H, W, OC, KH, KW, stride, pad, dil
+    (2, 3, 9, 9, 4, 3, 3, 1, 1, 1),
+    (1, 3, 64, 64, 128, 7, 7, 4, 3, 1),
+    (2, 16, 20, 20, 130, 3, 3, 1, 1, 1),
+    (2, 32, 14, 14, 64, 3, 3, 1, 2, 2),
+    (3, 8, 17, 13, 200, 5, 3, 2, 1, 1),
+    (1, 5, 12, 40, 36, 3, 2, (2, 3), (1, 0), (1, 2)),
+    (2, 64, 9, 9, 32, 1, 1, 1, 0, 1),
+]
+
+
+def _conv_case(t, workload, spec=None):
+    B, IC, H, W, OC, KH, KW = t[:7]
+    kw = {} if spec is None else dict(x=spec, w=spec, bias=spec)
+    x, w, b = synth.conv_inputs(B, IC, H, W, OC, KH, KW, workload=workload, **kw)
+    return x, w, b, t[7], t[8], t[9]
+
+
+@pytest.mark.parametrize("mode", ["simt", "force_tc3", "force_tc1"])
+@pytest.mark.parametrize("idx", range(len(SMALL_CONV)))
+def test_conv_small(mode, idx):
+    x, w, b, s, p, d = _conv_case(SMALL_CONV[idx], 300 + idx)
+    got, ref, S, kern = run_conv(x, w, b, s, p, d, mode)
+    assert kern == EXPECT[mode]
+    within(got, ref, S, TOL[mode], f"{mode} conv #{idx}")
+    # and without bias
+    got, ref, S, _ = run_conv(x, w, None, s, p, d, mode)
+    within(got, ref, S, TOL[mode], f"{mode} conv #{idx} no bias")
+
+
+@pytest.mark.parametrize("mode", ["simt", "force_tc3", "force_tc1"])
+@pytest.mark.parametrize("idx", [0, 1, 3, 5])
+def test_conv_integer_inputs_are_bit_exact(mode, idx):
+    x, w, b, s, p, d = _conv_case(SMALL_CONV[idx], 400 + idx, spec=("I", -4, 4))
+    got, ref, _, kern = run_conv(x, w, b, s, p, d, mode)
+    assert kern == EXPECT[mode]
+    assert np.array_equal(got.astype(np.float64), ref)
+
+
+def test_conv_1x1_matches_addmm_path():
+    B, IC, H, W, OC = 2, 64, 16, 16, 128
+    x, w, b = synth.conv_inputs(B, IC, H, W, OC, 1, 1, workload=55)
+    conv = binding.conv2d(dev(x), dev(w), dev(b), mode="force_tc3").cpu().numpy()
+    for bi in range(B):
+        bias2d = np.repeat(b[:, None], H * W, axis=1).astype(np.float32)
+        mm = binding.addmm(dev(bias2d), dev(w.reshape(OC, IC)), dev(x[bi].reshape(IC, H * W)),
+                           mode="force_tc3").cpu().numpy()
+        ref, S = oracle.addmm(bias2d, w.reshape(OC, IC), x[bi].reshape(IC, H * W))
+        within(mm, ref, S, 1e-5, "1x1 via addmm")
+        within(conv[bi].reshape(OC, H * W), ref, S, 1e-5, "1x1 via conv")
+
+
+def test_conv_empty_channels_and_bias_only():
+    x = dev(np.ones((0, 3, 8, 8), np.float32))
+    w = dev(np.ones((4, 3, 3, 3), np.float32))
+    out = binding.conv2d(x, w, None, 1, 1, 1)
+    assert out.shape == (0, 4, 8, 8)
+    xz = dev(np.ones((2, 0, 8, 8), np.float32))
+    wz = dev(np.ones((4, 0, 3, 3), np.float32))
+    bias = dev(np.array([1, 2, 3, 4], np.float32))
+    out = binding.conv2d(xz, wz, bias, 1, 1, 1).cpu().numpy()
+    assert binding.last_kernel() == "fill"
+    assert np.array_equal(out, np.broadcast_to(np.array([1, 2, 3, 4], np.float32)[None, :, None,
+                                                                                  None], out.shape))
+
+
+@pytest.mark.parametrize("name", list(synth.CONV_CASES))
+def test_conv_workloads(name):
+    c, x, w, b = synth.make_conv_case(name)
+    for mode in ("default", "tf32"):
+        got, ref, S, kern = run_conv(x, w, b, c["stride"], c["pad"], c["dilation"], mode)
+        assert kern == ("tc3" if mode == "default" else "tc1")
+        within(got, ref, S, TOL[mode], f"{name} {mode}")
+
+
+def test_launch_counter_and_watchdog():
+    n0 = binding.launch_count()
+    s, a, b = synth.addmm_inputs(256, 256, 64, self_2d=False, workload=3)
+    binding.addmm(dev(s), dev(a), dev(b), mode="force_tc3")
+    binding.addmm(dev(s), dev(a), dev(b), mode="simt")
+    torch.cuda.synchronize()
+    assert binding.launch_count() == n0 + 2
+    assert binding.check_device_error(None) == binding.IMC_OK
