@@ -10,9 +10,10 @@
 // (32x32 workgroup tiles, 4x4 register blocking) targets a scalar ALU; here
 // the same tiled GEMM is laid out for sm_103a:
 //
-//  * one persistent CTA per SM walks 128 x BN output tiles;
-//  * operands are staged in a multi-stage ring of 128-byte-swizzled shared
-//    memory tiles: A (mat1 or weight) K-major, B (mat2 or im2col) MN-major;
+//  * one persistent CTA per SM walks 128 x 128 output tiles;
+//  * operands are staged in a multi-stage ring of shared-memory tiles in the
+//    K-major, 128-byte-swizzled layout the tensor core reads (on this GPU a
+//    kind::tf32 MMA only accepts K-major operands);
 //  * one thread issues tcgen05.mma kind::tf32 into an fp32 accumulator in
 //    tensor memory (TMEM), double-buffered so the epilogue of one tile
 //    overlaps the main loop of the next;
@@ -26,10 +27,12 @@
 //    segments: beta*self + alpha*acc (addmm) or acc + bias[oc] scattered to
 //    NCHW (conv).
 //
-// addmm: A and B tiles arrive by TMA (cp.async.bulk.tensor, no multicast);
-// four split warps derive the lo tiles.  conv: four producer warps gather the
-// im2col tile (zero for padding taps and the ragged K / N edges) and the
-// weight rows, and write hi and lo tiles directly.
+// addmm: mat1 and mat2 tiles arrive by TMA (cp.async.bulk.tensor, no
+// multicast).  mat1 is K-major already; mat2 is N-contiguous, so four
+// transform warps transpose its tile into the K-major layout while splitting
+// it (and split mat1 in place).  conv: four producer warps gather the im2col
+// rows (zero for padding taps and the ragged K / N edges) and the weight rows
+// and write hi and lo tiles directly.
 //
 // Every mbarrier wait is bounded (about 2 s): on expiry the kernel records
 // the wait site in a device word, stops all roles, waits for its own copies
@@ -43,15 +46,17 @@
 namespace imc {
 namespace {
 
-constexpr int BM = 128;                 // rows of a tile (TMEM lanes)
-constexpr int BK = 32;                  // fp32 per k-block: one 128-byte swizzle row
-constexpr int UK = 8;                   // K of one tcgen05.mma kind::tf32
+constexpr int BM = 128;                  // rows of a tile (TMEM lanes)
+constexpr int BN = 128;                  // columns of a tile (MMA N)
+constexpr int BK = 32;                   // fp32 per k-block: one 128-byte swizzle row
+constexpr int UK = 8;                    // K of one tcgen05.mma kind::tf32
 constexpr int KSTEPS = BK / UK;
-constexpr int A_TILE_BYTES = BM * BK * 4;  // 16 KB
-constexpr int B_CHUNK_BYTES = BK * 128;    // 32 columns x BK rows, MN-major
-constexpr int EPI_PITCH = 36;              // floats per staged epilogue row
+constexpr int TILE_BYTES = 128 * BK * 4;  // one 128-row K-major operand tile: 16 KB
+constexpr int B_CHUNK_BYTES = BK * 128;   // 32 columns x BK rows of an N-contiguous tile
+constexpr int EPI_PITCH = 36;             // floats per staged epilogue row
 constexpr int EPI_BYTES = 4 * 32 * EPI_PITCH * 4;
 constexpr int MAX_STAGES = 8;
+constexpr uint32_t TMEM_COLS = 2 * BN;    // two accumulator buffers
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
@@ -59,8 +64,8 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 __device__ int g_watchdog;
 
 struct Ctl {
-  uint64_t full[MAX_STAGES];   // operands of a stage are in shared memory
-  uint64_t split[MAX_STAGES];  // addmm 3xTF32: lo tiles of a stage are written
+  uint64_t full[MAX_STAGES];   // raw operands of a stage are in shared memory
+  uint64_t split[MAX_STAGES];  // addmm: the MMA-ready tiles of a stage are written
   uint64_t empty[MAX_STAGES];  // the MMAs reading a stage are done
   uint64_t accf[2];            // accumulator buffer holds a finished tile
   uint64_t acce[2];            // epilogue has drained an accumulator buffer
@@ -68,6 +73,27 @@ struct Ctl {
   uint32_t tmem_base;
   int abort;
 };
+
+// Byte offsets of the tiles inside one pipeline stage.
+struct Layout {
+  int a_hi, b_hi, a_lo, b_lo, b_raw, bytes, stages;
+};
+// addmm, 3xTF32: mat1 tile (TMA, truncated in place = A_hi) | mat2 tile as
+// loaded | A_lo | B_hi | B_lo.   1xTF32: mat1 | mat2 as loaded | B (K-major).
+constexpr Layout kGemm3 = {0, 3 * TILE_BYTES, 2 * TILE_BYTES, 4 * TILE_BYTES, TILE_BYTES,
+                           5 * TILE_BYTES, 2};
+constexpr Layout kGemm1 = {0, 2 * TILE_BYTES, 0, 0, TILE_BYTES, 3 * TILE_BYTES, 4};
+// conv, 3xTF32: A_hi | B_hi | A_lo | B_lo.   1xTF32: A | B.
+constexpr Layout kConv3 = {0, TILE_BYTES, 2 * TILE_BYTES, 3 * TILE_BYTES, 0, 4 * TILE_BYTES, 3};
+constexpr Layout kConv1 = {0, TILE_BYTES, 0, 0, 0, 2 * TILE_BYTES, 6};
+
+constexpr int smem_bytes(const Layout& L) {
+  return 1024 + L.stages * L.bytes + EPI_BYTES + (int)sizeof(Ctl);
+}
+static_assert(smem_bytes(kGemm3) <= 232448 && smem_bytes(kGemm1) <= 232448 &&
+                  smem_bytes(kConv3) <= 232448 && smem_bytes(kConv1) <= 232448,
+              "shared memory");
+static_assert(kGemm1.stages <= MAX_STAGES && kConv1.stages <= MAX_STAGES, "stages");
 
 enum WaitSite {
   kSiteProducerEmpty = 1,
@@ -109,6 +135,31 @@ __device__ __forceinline__ float tf32_lo(float v, float hi) {
   return isfinite(v) ? v - hi : 0.0f;
 }
 
+// Byte offset of element (row, k) in a 128-row, BK-deep K-major tile with the
+// 128-byte swizzle: 8-row groups of 1024 B, 16-byte units XOR-ed with row % 8.
+__device__ __forceinline__ int kmajor_offset(int row, int k) {
+  return (row >> 3) * 1024 + (row & 7) * 128 + ((((k >> 2) ^ (row & 7))) << 4) + (k & 3) * 4;
+}
+
+// Writes 32 consecutive-k values of one tile row: hi (and lo at +lo_delta).
+__device__ __forceinline__ void store_row(uint8_t* tile, int row, const float (&v)[BK], bool three,
+                                          int lo_delta) {
+  uint8_t* base = tile + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+  for (int j = 0; j < BK / 4; ++j) {
+    const int off = (j ^ (row & 7)) << 4;
+    const float4 q = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    if (three) {
+      const float4 h = make_float4(tf32_hi(q.x), tf32_hi(q.y), tf32_hi(q.z), tf32_hi(q.w));
+      *reinterpret_cast<float4*>(base + off) = h;
+      *reinterpret_cast<float4*>(base + lo_delta + off) =
+          make_float4(tf32_lo(q.x, h.x), tf32_lo(q.y, h.y), tf32_lo(q.z, h.z), tf32_lo(q.w, h.w));
+    } else {
+      *reinterpret_cast<float4*>(base + off) = q;
+    }
+  }
+}
+
 // Grouped raster: `group` M-tiles share each N-tile before moving on, so the
 // CTAs resident at one time reuse the same operand panels from L2.
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group, int& mt,
@@ -122,30 +173,14 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
   nt = r / rows;
 }
 
-template <int BN, int STAGES, bool THREE>
-struct Cfg {
-  static constexpr int B_TILE_BYTES = BK * BN * 4;
-  static constexpr int HI_BYTES = A_TILE_BYTES + B_TILE_BYTES;  // A_hi | B_hi
-  static constexpr int STAGE_BYTES = THREE ? 2 * HI_BYTES : HI_BYTES;  // .. | A_lo | B_lo
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + (int)sizeof(Ctl);
-  static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static_assert(STAGES <= MAX_STAGES, "too many stages");
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
-  static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS >= 32 && TMEM_COLS <= 512,
-                "TMEM columns");
-  static_assert(SMEM_BYTES <= 232448, "shared memory");
-};
-
 // ---------------------------------------------------------------- MMA role
 // One thread: for every tile, wait for a free accumulator buffer, then for
 // each k-block wait for its operands, issue KSTEPS (x3 for 3xTF32) MMAs and
 // release the stage with a commit.
-template <int BN, int STAGES, bool THREE>
 __device__ void mma_role(Ctl* ctl, uint8_t* smem, uint32_t tmem, int num_tiles, int num_kb,
-                         bool wait_split) {
-  using C = Cfg<BN, STAGES, THREE>;
+                         const Layout L, bool three, bool wait_split) {
   volatile int* abort = &ctl->abort;
-  const uint32_t idesc = ptx::idesc_tf32(BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+  const uint32_t idesc = ptx::idesc_tf32(BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/false);
   int s = 0;
   uint32_t ph = 0;
   int tl = 0;
@@ -163,20 +198,16 @@ __device__ void mma_role(Ctl* ctl, uint8_t* smem, uint32_t tmem, int num_tiles, 
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t st = ptx::smem_addr(smem + s * C::STAGE_BYTES);
+      const uint32_t st = ptx::smem_addr(smem + s * L.bytes);
 #pragma unroll
       for (int k = 0; k < KSTEPS; ++k) {
-        // A: K-major, 8-row groups 1024 B apart, k-step = 32 B inside the row.
-        // B: MN-major, 32-column chunks B_CHUNK_BYTES apart, k-step = 8 rows.
-        const uint64_t ah = ptx::smem_desc(st + k * 32, 16, 1024, ptx::kSwizzle128B);
-        const uint64_t bh =
-            ptx::smem_desc(st + A_TILE_BYTES + k * 1024, B_CHUNK_BYTES, 1024, ptx::kSwizzle128B);
+        // K-major tiles: 8-row groups 1024 B apart, one k-step = 32 B inside the row.
+        const uint64_t ah = ptx::smem_desc(st + L.a_hi + k * 32, 16, 1024, ptx::kSwizzle128B);
+        const uint64_t bh = ptx::smem_desc(st + L.b_hi + k * 32, 16, 1024, ptx::kSwizzle128B);
         const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
-        if (THREE) {
-          const uint32_t lo = st + C::HI_BYTES;
-          const uint64_t al = ptx::smem_desc(lo + k * 32, 16, 1024, ptx::kSwizzle128B);
-          const uint64_t bl = ptx::smem_desc(lo + A_TILE_BYTES + k * 1024, B_CHUNK_BYTES, 1024,
-                                             ptx::kSwizzle128B);
+        if (three) {
+          const uint64_t al = ptx::smem_desc(st + L.a_lo + k * 32, 16, 1024, ptx::kSwizzle128B);
+          const uint64_t bl = ptx::smem_desc(st + L.b_lo + k * 32, 16, 1024, ptx::kSwizzle128B);
           ptx::mma_tf32(d, al, bh, idesc, acc);
           ptx::mma_tf32(d, ah, bl, idesc, 1u);
           ptx::mma_tf32(d, ah, bh, idesc, 1u);
@@ -185,7 +216,7 @@ __device__ void mma_role(Ctl* ctl, uint8_t* smem, uint32_t tmem, int num_tiles, 
         }
       }
       ptx::mma_commit(&ctl->empty[s]);
-      if (++s == STAGES) {
+      if (++s == L.stages) {
         s = 0;
         ph ^= 1u;
       }
@@ -249,7 +280,7 @@ struct ConvStore {
   __device__ __forceinline__ int64_t N() const { return c.N; }
 };
 
-template <int BN, class Store>
+template <class Store>
 __device__ void epilogue_role(Ctl* ctl, float* stage, uint32_t tmem, int num_tiles, int num_m,
                               int num_n, int group, int q, const Store& st) {
   volatile int* abort = &ctl->abort;
@@ -297,42 +328,44 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+__device__ __forceinline__ void init_barriers(Ctl* ctl, int stages, uint32_t full_count) {
+  for (int s = 0; s < stages; ++s) {
+    ptx::mbar_init(&ctl->full[s], full_count);
+    ptx::mbar_init(&ctl->split[s], 128);
+    ptx::mbar_init(&ctl->empty[s], 1);
+  }
+  for (int b = 0; b < 2; ++b) {
+    ptx::mbar_init(&ctl->accf[b], 1);
+    ptx::mbar_init(&ctl->acce[b], 128);
+  }
+  ptx::mbar_init(&ctl->drain, 1);
+  ctl->abort = 0;
+  ptx::fence_mbar_init();
+}
+
 // ------------------------------------------------------------- addmm kernel
 // warp 0: TMA producer; warp 1: TMEM owner + MMA issuer; warps 2-5: epilogue;
-// warps 6-9 (3xTF32 only): split warps.
-template <int BN, int STAGES, bool THREE>
-__global__ void __launch_bounds__(THREE ? 320 : 192, 1)
+// warps 6-9: transform warps (K-major mat2 tile; hi / lo split in 3xTF32).
+template <bool THREE>
+__global__ void __launch_bounds__(320, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const GemmArgs g, const int num_m, const int num_n, const int group) {
-  using C = Cfg<BN, STAGES, THREE>;
+  constexpr Layout L = THREE ? kGemm3 : kGemm1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  float* epi = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * C::STAGE_BYTES + EPI_BYTES);
+  float* epi = reinterpret_cast<float*>(smem + L.stages * L.bytes);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + L.stages * L.bytes + EPI_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = num_m * num_n;
   const int num_kb = (int)((g.K + BK - 1) / BK);
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&ctl->full[s], 1);
-      ptx::mbar_init(&ctl->split[s], 128);
-      ptx::mbar_init(&ctl->empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&ctl->accf[b], 1);
-      ptx::mbar_init(&ctl->acce[b], 128);
-    }
-    ptx::mbar_init(&ctl->drain, 1);
-    ctl->abort = 0;
-    ptx::fence_mbar_init();
-  }
+  if (threadIdx.x == 0) init_barriers(ctl, L.stages, 1);
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&ctl->tmem_base, C::TMEM_COLS);
+    ptx::tmem_alloc(&ctl->tmem_base, TMEM_COLS);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -351,35 +384,37 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
         tile_coords(t, num_m, num_n, group, mt, nt);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty)) break;
-          uint8_t* st = smem + s * C::STAGE_BYTES;
-          ptx::mbar_arrive_expect_tx(&ctl->full[s], C::HI_BYTES);
-          ptx::tma_load_2d(st, &tmA, &ctl->full[s], kb * BK, mt * BM);
+          uint8_t* st = smem + s * L.bytes;
+          ptx::mbar_arrive_expect_tx(&ctl->full[s], 2 * TILE_BYTES);
+          ptx::tma_load_2d(st + L.a_hi, &tmA, &ctl->full[s], kb * BK, mt * BM);
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c)
-            ptx::tma_load_2d(st + A_TILE_BYTES + c * B_CHUNK_BYTES, &tmB, &ctl->full[s],
+            ptx::tma_load_2d(st + L.b_raw + c * B_CHUNK_BYTES, &tmB, &ctl->full[s],
                              nt * BN + c * 32, kb * BK);
           ++issued;
-          if (++s == STAGES) {
+          if (++s == L.stages) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
       // Every copy issued must have landed before the CTA's shared memory is released.
-      for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
-        drain_wait(&ctl->full[j % STAGES], (uint32_t)((j / STAGES) & 1));
+      for (int j = (issued > L.stages ? issued - L.stages : 0); j < issued; ++j)
+        drain_wait(&ctl->full[j % L.stages], (uint32_t)((j / L.stages) & 1));
     }
   } else if (warp == 1) {
-    if (lane == 0) mma_role<BN, STAGES, THREE>(ctl, smem, tmem, num_tiles, num_kb, THREE);
+    if (lane == 0) mma_role(ctl, smem, tmem, num_tiles, num_kb, L, THREE, true);
     __syncwarp();
   } else if (warp < 6) {
-    epilogue_role<BN>(ctl, epi + (warp - 2) * 32 * EPI_PITCH, tmem, num_tiles, num_m, num_n,
-                      group, warp & 3, GemmStore{g});
-  } else if (THREE) {
-    // Split warps: lo = v - hi for every element of the stage's A and B tiles.
-    // The tiles keep their TMA layout (the split is elementwise); hi is
-    // rewritten in place so the MMA sees exactly the truncated TF32 value.
-    const int tid = threadIdx.x - 192;
+    epilogue_role(ctl, epi + (warp - 2) * 32 * EPI_PITCH, tmem, num_tiles, num_m, num_n, group,
+                  warp & 3, GemmStore{g});
+  } else {
+    // Transform warps.  mat1 tile: split in place (hi) and into A_lo.  mat2
+    // tile (32 k-rows x 128 n, N-contiguous, 128B-swizzled per 32-column
+    // chunk): lane = k; each lane reads 4 consecutive n of its row and writes
+    // them to rows n of the K-major B_hi (and B_lo) tiles.  Both the 16-byte
+    // reads and the 4-byte writes hit 32 distinct banks per warp.
+    const int tid = threadIdx.x - 192, tw = tid >> 5;
     int s = 0;
     uint32_t ph = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -389,26 +424,42 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
           ok = false;
           break;
         }
-        float4* hi = reinterpret_cast<float4*>(smem + s * C::STAGE_BYTES);
-        float4* lo = reinterpret_cast<float4*>(smem + s * C::STAGE_BYTES + C::HI_BYTES);
+        uint8_t* st = smem + s * L.bytes;
+        if (THREE) {
+          float4* ahi = reinterpret_cast<float4*>(st + L.a_hi);
+          float4* alo = reinterpret_cast<float4*>(st + L.a_lo);
 #pragma unroll 4
-        for (int i = tid; i < C::HI_BYTES / 16; i += 128) {
-          const float4 v = hi[i];
-          float4 h, l;
-          h.x = tf32_hi(v.x);
-          h.y = tf32_hi(v.y);
-          h.z = tf32_hi(v.z);
-          h.w = tf32_hi(v.w);
-          l.x = tf32_lo(v.x, h.x);
-          l.y = tf32_lo(v.y, h.y);
-          l.z = tf32_lo(v.z, h.z);
-          l.w = tf32_lo(v.w, h.w);
-          hi[i] = h;
-          lo[i] = l;
+          for (int i = tid; i < TILE_BYTES / 16; i += 128) {
+            const float4 v = ahi[i];
+            const float4 h = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+            ahi[i] = h;
+            alo[i] = make_float4(tf32_lo(v.x, h.x), tf32_lo(v.y, h.y), tf32_lo(v.z, h.z),
+                                 tf32_lo(v.w, h.w));
+          }
+        }
+        const uint8_t* braw = st + L.b_raw;
+        uint8_t* bhi = st + L.b_hi;
+        const int k = lane;
+#pragma unroll 2
+        for (int qd = tw; qd < BN / 4; qd += 4) {  // qd: group of 4 columns n = 4qd .. 4qd+3
+          const float4 v = *reinterpret_cast<const float4*>(
+              braw + (qd >> 3) * B_CHUNK_BYTES + k * 128 + ((((qd & 7) ^ (k & 7))) << 4));
+          const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int off = kmajor_offset(4 * qd + j, k);
+            if (THREE) {
+              const float h = tf32_hi(vv[j]);
+              *reinterpret_cast<float*>(bhi + off) = h;
+              *reinterpret_cast<float*>(bhi + (L.b_lo - L.b_hi) + off) = tf32_lo(vv[j], h);
+            } else {
+              *reinterpret_cast<float*>(bhi + off) = vv[j];
+            }
+          }
         }
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(&ctl->split[s]);
-        if (++s == STAGES) {
+        if (++s == L.stages) {
           s = 0;
           ph ^= 1u;
         }
@@ -421,45 +472,30 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
 // -------------------------------------------------------------- conv kernel
 // warps 0-3: producers (im2col gather of B, weight rows of A, hi/lo split);
 // warp 4: TMEM owner + MMA issuer; warps 5-8: epilogue.
-constexpr int CONV_BN = 128;
-
-template <int STAGES, bool THREE>
+template <bool THREE>
 __global__ void __launch_bounds__(288, 1)
     k_tc_conv(const ConvArgs c, const int num_m, const int num_n, const int group,
               const int a_vec) {
-  constexpr int BN = CONV_BN;
-  using C = Cfg<BN, STAGES, THREE>;
+  constexpr Layout L = THREE ? kConv3 : kConv1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  float* epi = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * C::STAGE_BYTES + EPI_BYTES);
+  float* epi = reinterpret_cast<float*>(smem + L.stages * L.bytes);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + L.stages * L.bytes + EPI_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = num_m * num_n;
   const int K = (int)c.K;
   const int num_kb = (K + BK - 1) / BK;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&ctl->full[s], 128);
-      ptx::mbar_init(&ctl->empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&ctl->accf[b], 1);
-      ptx::mbar_init(&ctl->acce[b], 128);
-    }
-    ptx::mbar_init(&ctl->drain, 1);
-    ctl->abort = 0;
-    ptx::fence_mbar_init();
-  }
+  if (threadIdx.x == 0) init_barriers(ctl, L.stages, 128);
   if (warp == 4) {
-    ptx::tmem_alloc(&ctl->tmem_base, C::TMEM_COLS);
+    ptx::tmem_alloc(&ctl->tmem_base, TMEM_COLS);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -469,7 +505,7 @@ __global__ void __launch_bounds__(288, 1)
   volatile int* abort = &ctl->abort;
 
   if (warp < 4) {
-    const int pt = threadIdx.x;  // owns B column pt of the tile and A row pt
+    const int pt = threadIdx.x;  // owns row pt of the B tile (column n) and row pt of A
     const int P = c.OH * c.OW;
     int s = 0;
     uint32_t ph = 0;
@@ -497,7 +533,7 @@ __global__ void __launch_bounds__(288, 1)
           ok = false;
           break;
         }
-        uint8_t* st = smem + s * C::STAGE_BYTES;
+        uint8_t* st = smem + s * L.bytes;
         const int k0 = kb * BK;
         // ---- B: im2col rows k0 .. k0+31 of column n; kk -> (ic, kh, kw).
         float v[BK];
@@ -521,19 +557,6 @@ __global__ void __launch_bounds__(288, 1)
             }
           }
         }
-        // MN-major 128B-swizzled: chunk pt/32, row j, 16-byte unit (col/4) ^ (j%8).
-        uint8_t* bh = st + A_TILE_BYTES + (pt >> 5) * B_CHUNK_BYTES;
-#pragma unroll
-        for (int j = 0; j < BK; ++j) {
-          const int off = j * 128 + ((((pt & 31) >> 2) ^ (j & 7)) << 4) + (pt & 3) * 4;
-          if (THREE) {
-            const float h = tf32_hi(v[j]);
-            *reinterpret_cast<float*>(bh + off) = h;
-            *reinterpret_cast<float*>(bh + C::HI_BYTES + off) = tf32_lo(v[j], h);
-          } else {
-            *reinterpret_cast<float*>(bh + off) = v[j];
-          }
-        }
         // ---- A: weight row m, columns k0 .. k0+31.
         float a[BK];
         if (a_vec && row_ok && k0 + BK <= K) {
@@ -549,26 +572,11 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
           for (int j = 0; j < BK; ++j) a[j] = (row_ok && k0 + j < K) ? __ldg(wrow + k0 + j) : 0.0f;
         }
-        // K-major 128B-swizzled: 8-row group pt/8, row pt%8, 16-byte unit j ^ (pt%8).
-        uint8_t* ah = st + (pt >> 3) * 1024 + (pt & 7) * 128;
-#pragma unroll
-        for (int j = 0; j < BK / 4; ++j) {
-          const int off = (j ^ (pt & 7)) << 4;
-          const float4 q4 = make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
-          if (THREE) {
-            const float4 h =
-                make_float4(tf32_hi(q4.x), tf32_hi(q4.y), tf32_hi(q4.z), tf32_hi(q4.w));
-            *reinterpret_cast<float4*>(ah + off) = h;
-            *reinterpret_cast<float4*>(ah + C::HI_BYTES + off) =
-                make_float4(tf32_lo(q4.x, h.x), tf32_lo(q4.y, h.y), tf32_lo(q4.z, h.z),
-                            tf32_lo(q4.w, h.w));
-          } else {
-            *reinterpret_cast<float4*>(ah + off) = q4;
-          }
-        }
+        store_row(st + L.b_hi, pt, v, THREE, L.b_lo - L.b_hi);
+        store_row(st + L.a_hi, pt, a, THREE, L.a_lo - L.a_hi);
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(&ctl->full[s]);
-        if (++s == STAGES) {
+        if (++s == L.stages) {
           s = 0;
           ph ^= 1u;
         }
@@ -576,18 +584,18 @@ __global__ void __launch_bounds__(288, 1)
       if (!ok) break;
     }
   } else if (warp == 4) {
-    if (lane == 0) mma_role<BN, STAGES, THREE>(ctl, smem, tmem, num_tiles, num_kb, false);
+    if (lane == 0) mma_role(ctl, smem, tmem, num_tiles, num_kb, L, THREE, false);
     __syncwarp();
   } else {
-    epilogue_role<BN>(ctl, epi + (warp - 5) * 32 * EPI_PITCH, tmem, num_tiles, num_m, num_n,
-                      group, warp & 3, ConvStore{c});
+    epilogue_role(ctl, epi + (warp - 5) * 32 * EPI_PITCH, tmem, num_tiles, num_m, num_n, group,
+                  warp & 3, ConvStore{c});
   }
 
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 4) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -631,47 +639,47 @@ bool encode_2d(CUtensorMap* m, const float* base, uint64_t inner, uint64_t outer
 constexpr int kMaxDev = 64;
 
 template <class KernelPtr>
-cudaError_t prepare(KernelPtr k, int smem_bytes, bool* done_per_device) {
+cudaError_t prepare(KernelPtr k, int smem, bool* done_per_device) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < kMaxDev && done_per_device[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess && dev < kMaxDev) done_per_device[dev] = true;
   return e;
 }
 
-template <int BN, int STAGES, bool THREE>
+template <bool THREE>
 cudaError_t run_gemm(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap& tb,
                      cudaStream_t s) {
-  using C = Cfg<BN, STAGES, THREE>;
+  constexpr int smem = smem_bytes(THREE ? kGemm3 : kGemm1);
   static bool ready[kMaxDev];
-  auto k = k_tc_gemm<BN, STAGES, THREE>;
-  cudaError_t e = prepare(k, C::SMEM_BYTES, ready);
+  auto k = k_tc_gemm<THREE>;
+  cudaError_t e = prepare(k, smem, ready);
   if (e != cudaSuccess) return e;
   const int num_m = (int)((g.M + BM - 1) / BM), num_n = (int)((g.N + BN - 1) / BN);
   const int tiles = num_m * num_n;
   const int sms = device_sm_count();
   const int grid = tiles < sms ? tiles : sms;
   const int group = num_m < 8 ? num_m : 8;
-  k<<<grid, THREE ? 320 : 192, C::SMEM_BYTES, s>>>(ta, tb, g, num_m, num_n, group);
+  k<<<grid, 320, smem, s>>>(ta, tb, g, num_m, num_n, group);
   note_launch();
   return cudaGetLastError();
 }
 
-template <int STAGES, bool THREE>
+template <bool THREE>
 cudaError_t run_conv(const ConvArgs& c, cudaStream_t s) {
-  using C = Cfg<CONV_BN, STAGES, THREE>;
+  constexpr int smem = smem_bytes(THREE ? kConv3 : kConv1);
   static bool ready[kMaxDev];
-  auto k = k_tc_conv<STAGES, THREE>;
-  cudaError_t e = prepare(k, C::SMEM_BYTES, ready);
+  auto k = k_tc_conv<THREE>;
+  cudaError_t e = prepare(k, smem, ready);
   if (e != cudaSuccess) return e;
-  const int num_m = (int)((c.M + BM - 1) / BM), num_n = (int)((c.N + CONV_BN - 1) / CONV_BN);
+  const int num_m = (int)((c.M + BM - 1) / BM), num_n = (int)((c.N + BN - 1) / BN);
   const int tiles = num_m * num_n;
   const int sms = device_sm_count();
   const int grid = tiles < sms ? tiles : sms;
   const int a_vec = (c.K % 4 == 0) && ((reinterpret_cast<uintptr_t>(c.w) & 15u) == 0);
-  k<<<grid, 288, C::SMEM_BYTES, s>>>(c, num_m, num_n, num_m, a_vec);
+  k<<<grid, 288, smem, s>>>(c, num_m, num_n, num_m, a_vec);
   note_launch();
   return cudaGetLastError();
 }
@@ -681,31 +689,26 @@ cudaError_t run_conv(const ConvArgs& c, cudaStream_t s) {
 bool tc_gemm_supported(const GemmArgs& a) {
   const bool aligned = ((reinterpret_cast<uintptr_t>(a.mat1) | reinterpret_cast<uintptr_t>(a.mat2)) &
                         15u) == 0;
-  const double tiles = (double)((a.M + BM - 1) / BM) * (double)((a.N + 127) / 128);
+  const double tiles = (double)((a.M + BM - 1) / BM) * (double)((a.N + BN - 1) / BN);
   return a.K % 4 == 0 && a.N % 4 == 0 && aligned && tiles < 2147483647.0 && encode_fn() != nullptr;
 }
 
 cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, cudaStream_t s) {
   if (!tc_gemm_supported(g)) return cudaErrorNotSupported;
-  const int sms = device_sm_count();
-  const int64_t num_m = (g.M + BM - 1) / BM;
-  const bool wide = num_m * ((g.N + 255) / 256) >= sms;  // enough 128x256 tiles to fill the GPU
   CUtensorMap ta, tb;
   if (!encode_2d(&ta, g.mat1, (uint64_t)g.K, (uint64_t)g.M, BM)) return cudaErrorInvalidValue;
   if (!encode_2d(&tb, g.mat2, (uint64_t)g.N, (uint64_t)g.K, BK)) return cudaErrorInvalidValue;
-  if (three_pass)
-    return wide ? run_gemm<256, 2, true>(g, ta, tb, s) : run_gemm<128, 3, true>(g, ta, tb, s);
-  return wide ? run_gemm<256, 4, false>(g, ta, tb, s) : run_gemm<128, 6, false>(g, ta, tb, s);
+  return three_pass ? run_gemm<true>(g, ta, tb, s) : run_gemm<false>(g, ta, tb, s);
 }
 
 bool tc_conv_supported(const ConvArgs& c) {
-  const double tiles = (double)((c.M + BM - 1) / BM) * (double)((c.N + CONV_BN - 1) / CONV_BN);
+  const double tiles = (double)((c.M + BM - 1) / BM) * (double)((c.N + BN - 1) / BN);
   return tiles < 2147483647.0;
 }
 
 cudaError_t launch_tc_conv(const ConvArgs& c, bool three_pass, cudaStream_t s) {
   if (!tc_conv_supported(c)) return cudaErrorNotSupported;
-  return three_pass ? run_conv<3, true>(c, s) : run_conv<6, false>(c, s);
+  return three_pass ? run_conv<true>(c, s) : run_conv<false>(c, s);
 }
 
 cudaError_t tc_take_watchdog(int* value, cudaStream_t s) {
