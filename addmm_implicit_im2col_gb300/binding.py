@@ -37,6 +37,12 @@ SIGNATURES = {
     "conv2d_gemm_f32": (_int, [_vp, _vp, _vp, _vp] + [_i64] * 10 + [_vp]),
     "conv2d_gemm_f32_ex": (_int, [_vp, _vp, _vp, _vp] + [_i64] * 10 + [_int, _vp]),
     "conv2d_gemm_f32_nd": (_int, [_vp, _vp, _vp, _vp] + [_i64] * 13 + [_int, _vp]),
+    "gemm_addmm_f32_ws": (_int, [_vp, _int, _vp, _vp, _vp, _i64, _i64, _i64, _dbl, _dbl, _int,
+                                 _vp, ctypes.c_size_t, _vp]),
+    "gemm_addmm_f32_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64, _int]),
+    "conv2d_gemm_f32_ws": (_int, [_vp, _vp, _vp, _vp] + [_i64] * 13 + [_int, _vp, ctypes.c_size_t,
+                                                                      _vp]),
+    "conv2d_gemm_f32_workspace_bytes": (ctypes.c_size_t, [_i64] * 13 + [_int]),
     "imc_status_string": (ctypes.c_char_p, [_int]),
     "imc_last_kernel": (_int, []),
     "imc_launch_count": (ctypes.c_uint64, []),
@@ -84,6 +90,16 @@ def gemm_addmm_f32_ex(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode
                                     stream)
 
 
+def gemm_addmm_f32_ws(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, workspace,
+                      workspace_bytes, stream) -> int:
+    return load().gemm_addmm_f32_ws(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode,
+                                    workspace, workspace_bytes, stream)
+
+
+def gemm_addmm_f32_workspace_bytes(M, N, K, mode) -> int:
+    return int(load().gemm_addmm_f32_workspace_bytes(M, N, K, mode))
+
+
 def conv2d_gemm_f32(x, w, bias, out, B, IC, H, W, OC, KH, KW, stride, pad, dilation,
                     stream) -> int:
     return load().conv2d_gemm_f32(x, w, bias, out, B, IC, H, W, OC, KH, KW, stride, pad,
@@ -100,6 +116,18 @@ def conv2d_gemm_f32_nd(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW,
                        stream) -> int:
     return load().conv2d_gemm_f32_nd(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW,
                                      dH, dW, mode, stream)
+
+
+def conv2d_gemm_f32_ws(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, mode,
+                       workspace, workspace_bytes, stream) -> int:
+    return load().conv2d_gemm_f32_ws(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW,
+                                     dH, dW, mode, workspace, workspace_bytes, stream)
+
+
+def conv2d_gemm_f32_workspace_bytes(B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW,
+                                    mode) -> int:
+    return int(load().conv2d_gemm_f32_workspace_bytes(B, IC, H, W, OC, KH, KW, sH, sW, pH, pW,
+                                                      dH, dW, mode))
 
 
 def status_string(status: int) -> str:
@@ -166,8 +194,12 @@ def addmm(self, mat1, mat2, *, beta=1.0, alpha=1.0, mode="default", out=None):
         out = torch.empty((M, N), dtype=torch.float32, device=mat1.device)
     else:
         _check_tensor(out, "out", (2,))
-    rc = gemm_addmm_f32_ex(_ptr(self), self_2d, _ptr(mat1), _ptr(mat2), _ptr(out), M, N, K,
-                           float(beta), float(alpha), MODES[mode], _stream_ptr(mat1.device))
+    # scratch for the transposed mat2 comes from torch's allocator
+    nbytes = gemm_addmm_f32_workspace_bytes(M, N, K, MODES[mode])
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=mat1.device) if nbytes else None
+    rc = gemm_addmm_f32_ws(_ptr(self), self_2d, _ptr(mat1), _ptr(mat2), _ptr(out), M, N, K,
+                           float(beta), float(alpha), MODES[mode], _ptr(ws), nbytes,
+                           _stream_ptr(mat1.device))
     if rc != IMC_OK:
         raise ImcError(rc, "gemm_addmm_f32")
     return out
@@ -209,8 +241,12 @@ def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, *, mode="default", 
         out = torch.empty((B, OC, OH, OW), dtype=torch.float32, device=x.device)
     else:
         _check_tensor(out, "out", (4,))
-    rc = conv2d_gemm_f32_nd(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), B, IC, H, W, OC, KH, KW,
-                            sH, sW, pH, pW, dH, dW, MODES[mode], _stream_ptr(x.device))
+    nbytes = conv2d_gemm_f32_workspace_bytes(B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW,
+                                             MODES[mode])
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=x.device) if nbytes else None
+    rc = conv2d_gemm_f32_ws(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), B, IC, H, W, OC, KH, KW,
+                            sH, sW, pH, pW, dH, dW, MODES[mode], _ptr(ws), nbytes,
+                            _stream_ptr(x.device))
     if rc != IMC_OK:
         raise ImcError(rc, "conv2d_gemm_f32")
     return out

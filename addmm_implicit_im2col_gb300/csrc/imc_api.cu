@@ -89,11 +89,28 @@ int device_sm_count() {
 
 using namespace imc;
 
-extern "C" {
 
-int gemm_addmm_f32_ex(const float* self, int self_2d, const float* mat1, const float* mat2,
-                      float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
-                      int mode, void* stream) {
+namespace {
+
+// Which kernel a well-formed addmm takes.  `tc_ok` is whether the tcgen05
+// path can take the operands (K % 4 == 0, aligned mat1).
+int plan_gemm(int64_t M, int64_t N, int64_t K, double alpha, int mode, bool tc_ok) {
+  if (M == 0 || N == 0) return IMC_KERNEL_NONE;
+  if (alpha == 0.0 || K == 0) return IMC_KERNEL_FILL;
+  const bool force_tc = mode == IMC_MODE_FORCE_TC3 || mode == IMC_MODE_FORCE_TC1;
+  if (force_tc) return tc_ok ? (mode == IMC_MODE_FORCE_TC3 ? IMC_KERNEL_TC3 : IMC_KERNEL_TC1) : -1;
+  if (mode == IMC_MODE_SIMT || !tc_ok || (double)M * N * K < (double)kTinyMacs)
+    return IMC_KERNEL_SIMT;
+  return mode == IMC_MODE_DEFAULT ? IMC_KERNEL_TC3 : IMC_KERNEL_TC1;
+}
+
+// workspace == nullptr and !caller_ws: the transposed-mat2 workspace comes
+// from the device's stream-ordered pool (cudaMallocAsync / cudaFreeAsync on
+// `stream`).  caller_ws: the caller's buffer of ws_bytes is used, nothing is
+// allocated.
+int gemm_impl(const float* self, int self_2d, const float* mat1, const float* mat2, float* out,
+              int64_t M, int64_t N, int64_t K, double beta, double alpha, int mode,
+              void* workspace, size_t ws_bytes, bool caller_ws, void* stream) {
   if (self_2d != 0 && self_2d != 1) return IMC_ERR_ARG;
   if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return IMC_ERR_ARG;
   if (!std::isfinite(beta) || !std::isfinite(alpha)) return IMC_ERR_ARG;
@@ -109,16 +126,15 @@ int gemm_addmm_f32_ex(const float* self, int self_2d, const float* mat1, const f
   if (read_ops && (!mat1 || !mat2)) return IMC_ERR_NULL;
 
   const uint64_t out_bytes = (uint64_t)M * (uint64_t)N * 4u;
-  if (read_ops && (overlaps(out, out_bytes, mat1, (uint64_t)M * K * 4u) ||
-                   overlaps(out, out_bytes, mat2, (uint64_t)K * N * 4u)))
+  const uint64_t mat1_bytes = (uint64_t)M * K * 4u, mat2_bytes = (uint64_t)K * N * 4u;
+  if (read_ops && (overlaps(out, out_bytes, mat1, mat1_bytes) ||
+                   overlaps(out, out_bytes, mat2, mat2_bytes)))
     return IMC_ERR_ALIAS;
+  const uint64_t self_bytes = (uint64_t)(self_2d ? M * N : N) * 4u;
   if (read_self) {
-    const uint64_t self_bytes = (uint64_t)(self_2d ? M * N : N) * 4u;
     const bool exact_inplace = self_2d && (const void*)self == (const void*)out;
     if (!exact_inplace && overlaps(out, out_bytes, self, self_bytes)) return IMC_ERR_ALIAS;
   }
-  const int dev = check_device();
-  if (dev != IMC_OK) return dev;
 
   GemmArgs a;
   a.self = self;
@@ -133,31 +149,83 @@ int gemm_addmm_f32_ex(const float* self, int self_2d, const float* mat1, const f
   a.self_2d = self_2d;
   a.read_self = read_self ? 1 : 0;
   a.vec_out = (N % 4 == 0) && aligned16(out) && (!read_self || aligned16(self)) ? 1 : 0;
+  const bool tc_ok = read_ops && K % 4 == 0 && aligned16(mat1);
+  const int kernel = plan_gemm(M, N, K, alpha, mode, tc_ok);
+  if (kernel < 0) return IMC_ERR_SHAPE;
+  const bool tc = kernel == IMC_KERNEL_TC3 || kernel == IMC_KERNEL_TC1;
+  const size_t need = tc ? tc_gemm_workspace_bytes(N, K, kernel == IMC_KERNEL_TC3) : 0;
+  if (caller_ws && need > 0) {
+    if (!workspace || ws_bytes < need || !aligned16(workspace)) return IMC_ERR_ARG;
+    if (overlaps(workspace, need, out, out_bytes) || overlaps(workspace, need, mat1, mat1_bytes) ||
+        overlaps(workspace, need, mat2, mat2_bytes) ||
+        (read_self && overlaps(workspace, need, self, self_bytes)))
+      return IMC_ERR_ALIAS;
+  }
+  const int dev = check_device();
+  if (dev != IMC_OK) return dev;
   cudaStream_t s = (cudaStream_t)stream;
 
-  if (!read_ops) return finish(launch_fill_gemm(a, s), IMC_KERNEL_FILL);
+  if (kernel == IMC_KERNEL_FILL) return finish(launch_fill_gemm(a, s), kernel);
+  if (kernel == IMC_KERNEL_SIMT) return finish(launch_simt_gemm(a, s), kernel);
+  if (!tc_gemm_supported(a)) return IMC_ERR_DEVICE;  // driver without tensor-map support
+  void* ws = workspace;
+  if (!caller_ws) {
+    if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return IMC_ERR_CUDA;
+  }
+  const cudaError_t e = launch_tc_gemm(a, kernel == IMC_KERNEL_TC3, ws, s);
+  if (!caller_ws) {
+    const cudaError_t f = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess && f != cudaSuccess) return IMC_ERR_CUDA;
+  }
+  return finish(e, kernel);
+}
 
-  const bool tc_ok = tc_gemm_supported(a);
-  const bool force_tc = mode == IMC_MODE_FORCE_TC3 || mode == IMC_MODE_FORCE_TC1;
-  if (force_tc && !tc_ok) return IMC_ERR_SHAPE;
-  bool use_tc = force_tc || (mode != IMC_MODE_SIMT && tc_ok && (double)M * N * K >= (double)kTinyMacs);
-  if (!use_tc) return finish(launch_simt_gemm(a, s), IMC_KERNEL_SIMT);
-  const bool three = mode == IMC_MODE_DEFAULT || mode == IMC_MODE_FORCE_TC3;
-  return finish(launch_tc_gemm(a, three, s), three ? IMC_KERNEL_TC3 : IMC_KERNEL_TC1);
+}  // namespace
+
+extern "C" {
+
+int gemm_addmm_f32_ex(const float* self, int self_2d, const float* mat1, const float* mat2,
+                      float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                      int mode, void* stream) {
+  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, nullptr, 0, false,
+                   stream);
 }
 
 int gemm_addmm_f32(const float* self, int self_2d, const float* mat1, const float* mat2,
                    float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
                    void* stream) {
-  return gemm_addmm_f32_ex(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha,
-                           IMC_MODE_DEFAULT, stream);
+  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, IMC_MODE_DEFAULT,
+                   nullptr, 0, false, stream);
 }
 
-int conv2d_gemm_f32_nd(const float* x, const float* w, const float* bias, float* out, int64_t B,
-                       int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
-                       int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW,
-                       int mode, void* stream) {
-  if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return IMC_ERR_ARG;
+int gemm_addmm_f32_ws(const float* self, int self_2d, const float* mat1, const float* mat2,
+                      float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                      int mode, void* workspace, size_t workspace_bytes, void* stream) {
+  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, workspace,
+                   workspace_bytes, true, stream);
+}
+
+size_t gemm_addmm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode) {
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
+  if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return 0;
+  const int kernel = plan_gemm(M, N, K, 1.0, mode, K % 4 == 0);
+  if (kernel == IMC_KERNEL_TC3) return tc_gemm_workspace_bytes(N, K, true);
+  if (kernel == IMC_KERNEL_TC1) return tc_gemm_workspace_bytes(N, K, false);
+  return 0;
+}
+
+}  // extern "C"
+
+namespace {
+
+struct ConvShape {
+  int64_t OH, OW, K;
+};
+
+// Checks sizes; fills OH, OW, K.  IMC_OK or IMC_ERR_SHAPE.
+int conv_shape(int64_t B, int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
+               int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW,
+               ConvShape* cs) {
   if (B < 0 || IC < 0 || OC < 0 || H < 1 || W < 1 || KH < 1 || KW < 1) return IMC_ERR_SHAPE;
   if (sH < 1 || sW < 1 || pH < 0 || pW < 0 || dH < 1 || dW < 1) return IMC_ERR_SHAPE;
   if (B > kMaxDim || IC > kMaxDim || OC > kMaxDim || H > kMaxDim || W > kMaxDim ||
@@ -168,24 +236,57 @@ int conv2d_gemm_f32_nd(const float* x, const float* w, const float* bias, float*
   const int64_t spanH = H + 2 * pH - dH * (KH - 1) - 1;
   const int64_t spanW = W + 2 * pW - dW * (KW - 1) - 1;
   if (spanH < 0 || spanW < 0) return IMC_ERR_SHAPE;
-  const int64_t OH = spanH / sH + 1, OW = spanW / sW + 1;
+  cs->OH = spanH / sH + 1;
+  cs->OW = spanW / sW + 1;
   // Every tensor stays below 2^31 elements (32-bit element offsets inside).
   const double lim = 2147483647.0;
   if ((double)B * IC * H * W > lim || (double)OC * IC * KH * KW > lim ||
-      (double)B * OC * OH * OW > lim || (double)IC * KH * KW > lim || (double)B * OH * OW > lim)
+      (double)B * OC * cs->OH * cs->OW > lim || (double)IC * KH * KW > lim ||
+      (double)B * cs->OH * cs->OW > lim)
     return IMC_ERR_SHAPE;
+  cs->K = IC * KH * KW;
+  return IMC_OK;
+}
+
+int plan_conv(int64_t M, int64_t N, int64_t K, int mode) {
+  if (M == 0 || N == 0) return IMC_KERNEL_NONE;
+  if (K == 0) return IMC_KERNEL_FILL;
+  if (mode == IMC_MODE_FORCE_TC3) return IMC_KERNEL_TC3;
+  if (mode == IMC_MODE_FORCE_TC1) return IMC_KERNEL_TC1;
+  if (mode == IMC_MODE_SIMT || (double)M * N * K < (double)kTinyMacs) return IMC_KERNEL_SIMT;
+  return mode == IMC_MODE_DEFAULT ? IMC_KERNEL_TC3 : IMC_KERNEL_TC1;
+}
+
+int conv_impl(const float* x, const float* w, const float* bias, float* out, int64_t B,
+              int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW, int64_t sH,
+              int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW, int mode,
+              void* workspace, size_t ws_bytes, bool caller_ws, void* stream) {
+  if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return IMC_ERR_ARG;
+  ConvShape cs;
+  const int sh = conv_shape(B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, &cs);
+  if (sh != IMC_OK) return sh;
   if (B == 0 || OC == 0) {
     t_last_kernel = IMC_KERNEL_NONE;
     return IMC_OK;
   }
-  const int64_t K = IC * KH * KW;
+  const int64_t K = cs.K, OH = cs.OH, OW = cs.OW;
   if (!out) return IMC_ERR_NULL;
   if (K > 0 && (!x || !w)) return IMC_ERR_NULL;
   const uint64_t out_bytes = (uint64_t)(B * OC * OH * OW) * 4u;
-  if ((K > 0 && (overlaps(out, out_bytes, x, (uint64_t)(B * IC * H * W) * 4u) ||
-                 overlaps(out, out_bytes, w, (uint64_t)(OC * K) * 4u))) ||
+  const uint64_t x_bytes = (uint64_t)(B * IC * H * W) * 4u, w_bytes = (uint64_t)(OC * K) * 4u;
+  if ((K > 0 && (overlaps(out, out_bytes, x, x_bytes) || overlaps(out, out_bytes, w, w_bytes))) ||
       overlaps(out, out_bytes, bias, (uint64_t)OC * 4u))
     return IMC_ERR_ALIAS;
+  const int kernel = plan_conv(OC, B * OH * OW, K, mode);
+  const bool tc = kernel == IMC_KERNEL_TC3 || kernel == IMC_KERNEL_TC1;
+  const size_t need = tc ? tc_conv_workspace_bytes(OC, K, kernel == IMC_KERNEL_TC3) : 0;
+  if (caller_ws && need > 0) {
+    if (!workspace || ws_bytes < need || !aligned16(workspace)) return IMC_ERR_ARG;
+    if (overlaps(workspace, need, out, out_bytes) || overlaps(workspace, need, x, x_bytes) ||
+        overlaps(workspace, need, w, w_bytes) ||
+        overlaps(workspace, need, bias, (uint64_t)OC * 4u))
+      return IMC_ERR_ALIAS;
+  }
   const int dev = check_device();
   if (dev != IMC_OK) return dev;
 
@@ -215,14 +316,52 @@ int conv2d_gemm_f32_nd(const float* x, const float* w, const float* bias, float*
   c.vec_out = ((OH * OW) % 4 == 0) && aligned16(out) ? 1 : 0;
   cudaStream_t s = (cudaStream_t)stream;
 
-  if (K == 0) return finish(launch_fill_conv(c, s), IMC_KERNEL_FILL);
-  const bool tc_ok = tc_conv_supported(c);
-  const bool force_tc = mode == IMC_MODE_FORCE_TC3 || mode == IMC_MODE_FORCE_TC1;
-  if (force_tc && !tc_ok) return IMC_ERR_SHAPE;
-  bool use_tc = force_tc || (mode != IMC_MODE_SIMT && tc_ok && (double)c.M * c.N * c.K >= (double)kTinyMacs);
-  if (!use_tc) return finish(launch_simt_conv(c, s), IMC_KERNEL_SIMT);
-  const bool three = mode == IMC_MODE_DEFAULT || mode == IMC_MODE_FORCE_TC3;
-  return finish(launch_tc_conv(c, three, s), three ? IMC_KERNEL_TC3 : IMC_KERNEL_TC1);
+  if (kernel == IMC_KERNEL_FILL) return finish(launch_fill_conv(c, s), kernel);
+  if (kernel == IMC_KERNEL_SIMT) return finish(launch_simt_conv(c, s), kernel);
+  if (!tc_conv_supported(c)) return IMC_ERR_DEVICE;
+  void* ws = workspace;
+  if (!caller_ws) {
+    if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return IMC_ERR_CUDA;
+  }
+  const cudaError_t e = launch_tc_conv(c, kernel == IMC_KERNEL_TC3, ws, s);
+  if (!caller_ws) {
+    const cudaError_t f = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess && f != cudaSuccess) return IMC_ERR_CUDA;
+  }
+  return finish(e, kernel);
+}
+
+}  // namespace
+
+extern "C" {
+
+int conv2d_gemm_f32_nd(const float* x, const float* w, const float* bias, float* out, int64_t B,
+                       int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
+                       int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW,
+                       int mode, void* stream) {
+  return conv_impl(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, mode,
+                   nullptr, 0, false, stream);
+}
+
+int conv2d_gemm_f32_ws(const float* x, const float* w, const float* bias, float* out, int64_t B,
+                       int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
+                       int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW,
+                       int mode, void* workspace, size_t workspace_bytes, void* stream) {
+  return conv_impl(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, mode,
+                   workspace, workspace_bytes, true, stream);
+}
+
+size_t conv2d_gemm_f32_workspace_bytes(int64_t B, int64_t IC, int64_t H, int64_t W, int64_t OC,
+                                       int64_t KH, int64_t KW, int64_t sH, int64_t sW,
+                                       int64_t pH, int64_t pW, int64_t dH, int64_t dW,
+                                       int mode) {
+  if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return 0;
+  ConvShape cs;
+  if (conv_shape(B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, &cs) != IMC_OK) return 0;
+  const int kernel = plan_conv(OC, B * cs.OH * cs.OW, cs.K, mode);
+  if (kernel == IMC_KERNEL_TC3) return tc_conv_workspace_bytes(OC, cs.K, true);
+  if (kernel == IMC_KERNEL_TC1) return tc_conv_workspace_bytes(OC, cs.K, false);
+  return 0;
 }
 
 int conv2d_gemm_f32_ex(const float* x, const float* w, const float* bias, float* out, int64_t B,
@@ -260,11 +399,13 @@ uint64_t imc_launch_count(void) { return g_launches.load(std::memory_order_relax
 int imc_check_device_error(void* stream) {
   const int dev = check_device();
   if (dev != IMC_OK) return dev;
-  int v = 0;
-  if (tc_take_watchdog(&v, (cudaStream_t)stream) != cudaSuccess) return IMC_ERR_CUDA;
-  return v != 0 ? IMC_ERR_TIMEOUT : IMC_OK;
+  int vg = 0, vc = 0;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess ||
+      gemm_take_watchdog(&vg) != cudaSuccess || conv_take_watchdog(&vc) != cudaSuccess)
+    return IMC_ERR_CUDA;
+  return (vg != 0 || vc != 0) ? IMC_ERR_TIMEOUT : IMC_OK;
 }
 
-int imc_version(void) { return 100; }
+int imc_version(void) { return 101; }
 
 }  // extern "C"

@@ -46,14 +46,21 @@ cudaError_t launch_fill_conv(const ConvArgs& a, cudaStream_t s);
 // tcgen05 tensor-core kernels.  three_pass selects 3xTF32 (fp32 accuracy)
 // over a single TF32 product.  Return cudaErrorNotSupported when the shape
 // does not meet the kernel's requirements (the caller falls back to SIMT).
+// The addmm kernel needs a workspace of tc_gemm_workspace_bytes() (16-byte
+// aligned) for the transposed mat2; it is dead once the launch completes.
 bool tc_gemm_supported(const GemmArgs& a);
-cudaError_t launch_tc_gemm(const GemmArgs& a, bool three_pass, cudaStream_t s);
+size_t tc_gemm_workspace_bytes(int64_t N, int64_t K, bool three_pass);
+cudaError_t launch_tc_gemm(const GemmArgs& a, bool three_pass, void* workspace, cudaStream_t s);
+// The conv kernel needs tc_conv_workspace_bytes() for the padded hi / lo
+// weight planes.
 bool tc_conv_supported(const ConvArgs& a);
-cudaError_t launch_tc_conv(const ConvArgs& a, bool three_pass, cudaStream_t s);
+size_t tc_conv_workspace_bytes(int64_t OC, int64_t K, bool three_pass);
+cudaError_t launch_tc_conv(const ConvArgs& a, bool three_pass, void* workspace, cudaStream_t s);
 
-// Reads and clears the watchdog word of the tensor-core kernels on the
-// current device (synchronises `s` first).
-cudaError_t tc_take_watchdog(int* value, cudaStream_t s);
+// Read and clear the watchdog word of the addmm / conv tensor-core kernels on
+// the current device (the caller synchronises first).
+cudaError_t gemm_take_watchdog(int* value);
+cudaError_t conv_take_watchdog(int* value);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

@@ -1,0 +1,410 @@
+// tcgen05 tensor-core addmm: out = beta*self + alpha*(mat1 @ mat2), fp32.
+//
+// Semantics: ExecuTorch WebGPU "Add optimized addmm op", Solution and
+// Implementation paragraphs (mat2 read as mat2[k*N + n]; self broadcast from
+// [N] or given as [M,N]; epilogue beta*self + alpha*acc).  The page's WGSL
+// kernel stages 32x32 slabs of both operands in workgroup memory and loops
+// over ceil(K/32) k-tiles; the same tiled GEMM is laid out here for sm_103a.
+//
+// A kind::tf32 MMA on this GPU reads its shared-memory operands K-major only.
+// mat1 [M,K] already is; mat2 [K,N] is N-contiguous, so a pre-pass
+// (k_prep_b) writes it once per call, transposed, into a caller- or
+// pool-provided workspace: Bt_hi[n][k] and Bt_lo[n][k] (3xTF32) or Bt[n][k]
+// (1xTF32).  The main kernel is then a plain pipeline:
+//
+//   warp 0      TMA producer: mat1 tile (128 x 16), Bt_hi / Bt_lo tiles (BN x 16),
+//               64-byte swizzle, into a 4-stage ring (8 stages for 1xTF32)
+//   warps 6-9   (3xTF32) A_lo = mat1 - tf32(mat1), elementwise into the stage
+//   warp 1      TMEM owner + MMA issuer: per 8-deep k-step
+//               A_lo*B_hi + A_hi*B_lo + A_hi*B_hi into an fp32 TMEM accumulator
+//               (A_hi is the raw mat1 tile: the tensor core drops the 13 low
+//               mantissa bits itself); double-buffered accumulator
+//   warps 2-5   epilogue: tcgen05.ld, 32x32 transpose through shared memory,
+//               beta*self + alpha*acc, 16-byte row-segment stores
+//
+// One persistent CTA per SM walks 128 x BN tiles in a grouped raster; BN (32
+// to 256) is picked per problem to fill the SMs with few waves.  Every
+// barrier wait is bounded (see tc_common.cuh).
+#include <mutex>
+
+#include "imc.h"
+#include "imc_internal.cuh"
+#include "tc_common.cuh"
+
+namespace imc {
+namespace {
+
+using namespace tc;
+
+constexpr int BK = 16;           // fp32 per k-block: one 64-byte swizzle row
+constexpr int KSTEPS = BK / UK;  // 2
+constexpr int BN_MAX = 256;
+constexpr int A_BYTES = BM * BK * 4;      // 8 KB
+constexpr int B_BYTES = BN_MAX * BK * 4;  // 16 KB
+constexpr uint32_t ACC_STRIDE = 256;      // TMEM columns between the two accumulators
+
+struct Layout {
+  int a, a_lo, b_hi, b_lo, bytes, stages;
+};
+constexpr Layout kL3 = {0, A_BYTES, 2 * A_BYTES, 2 * A_BYTES + B_BYTES, 2 * (A_BYTES + B_BYTES), 4};
+constexpr Layout kL1 = {0, 0, A_BYTES, 0, A_BYTES + B_BYTES, 8};
+constexpr int smem_bytes(const Layout& L) {
+  return 1024 + L.stages * L.bytes + EPI_BYTES + (int)sizeof(Ctl);
+}
+static_assert(smem_bytes(kL3) <= 232448 && smem_bytes(kL1) <= 232448, "shared memory");
+static_assert(kL1.stages <= MAX_STAGES, "stages");
+
+__device__ int g_watchdog_gemm;
+
+// ----------------------------------------------------------- mat2 pre-pass
+// Bt_hi[n*K + k] = tf32 part of mat2[k*N + n] and Bt_lo[n*K + k] = the rest
+// (3xTF32), or Bt_hi = mat2 transposed (bt_lo == nullptr).  32x32 tiles through
+// shared memory: reads and writes are 128-byte rows.
+__global__ void __launch_bounds__(256) k_prep_b(const float* __restrict__ mat2, int64_t K,
+                                                int64_t N, float* __restrict__ bt_hi,
+                                                float* __restrict__ bt_lo) {
+  __shared__ float tile[32][33];
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int64_t tiles_n = (N + 31) / 32, tiles = tiles_n * ((K + 31) / 32);
+  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    const int64_t k0 = (t / tiles_n) * 32, n0 = (t % tiles_n) * 32;
+#pragma unroll
+    for (int i = ty; i < 32; i += 8) {
+      const int64_t k = k0 + i, n = n0 + tx;
+      tile[i][tx] = (k < K && n < N) ? __ldg(mat2 + k * N + n) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = ty; i < 32; i += 8) {
+      const int64_t n = n0 + i, k = k0 + tx;
+      if (n < N && k < K) {
+        const float v = tile[tx][i];
+        if (bt_lo) {
+          bt_hi[n * K + k] = tf32_hi(v);
+          bt_lo[n * K + k] = tf32_lo(v);
+        } else {
+          bt_hi[n * K + k] = v;
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------ main kernel
+struct Store {
+  const GemmArgs& g;
+  int64_t m0, n0;
+  // beta * self for the segment (row r, columns c .. c+3 of the tile), read
+  // before any output of the block is written (out may be self: each element
+  // is read before its own write).
+  __device__ __forceinline__ float4 load(int r, int c) const {
+    const int64_t m = m0 + r, n = n0 + c;
+    float4 sv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!g.read_self || m >= g.M || n >= g.N) return sv;
+    const float* sp = g.self + (g.self_2d ? m * g.N : 0) + n;
+    if (g.vec_out) {
+      sv = *reinterpret_cast<const float4*>(sp);  // plain load: self may be out
+    } else {
+      sv.x = sp[0];
+      if (n + 1 < g.N) sv.y = sp[1];
+      if (n + 2 < g.N) sv.z = sp[2];
+      if (n + 3 < g.N) sv.w = sp[3];
+    }
+    return make_float4(g.beta * sv.x, g.beta * sv.y, g.beta * sv.z, g.beta * sv.w);
+  }
+  __device__ __forceinline__ void operator()(int r, int c, float4 v, float4 bs) const {
+    const int64_t m = m0 + r, n = n0 + c;
+    if (m >= g.M || n >= g.N) return;
+    float* o = g.out + m * g.N + n;
+    const float4 o4 = make_float4(fmaf(g.alpha, v.x, bs.x), fmaf(g.alpha, v.y, bs.y),
+                                  fmaf(g.alpha, v.z, bs.z), fmaf(g.alpha, v.w, bs.w));
+    if (g.vec_out) {  // N % 4 == 0 and 16-byte aligned rows: n .. n+3 are in range
+      *reinterpret_cast<float4*>(o) = o4;
+    } else {
+      const float vv[4] = {o4.x, o4.y, o4.z, o4.w};
+      for (int j = 0; j < 4 && n + j < g.N; ++j) o[j] = vv[j];
+    }
+  }
+};
+
+template <bool THREE>
+__global__ void __launch_bounds__(THREE ? 320 : 192, 1)
+    k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBh,
+              const __grid_constant__ CUtensorMap tmBl, const GemmArgs g, const int num_m,
+              const int num_n, const int group, const int bn) {
+  constexpr Layout L = THREE ? kL3 : kL1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  float* epi = reinterpret_cast<float*>(smem + L.stages * L.bytes);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + L.stages * L.bytes + EPI_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = (int)((g.K + BK - 1) / BK);
+  int* wd = &g_watchdog_gemm;
+
+  if (threadIdx.x == 0) init_barriers(ctl, L.stages, 1, 128);
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmBh);
+    if (THREE) ptx::tma_prefetch_desc(&tmBl);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  volatile int* abort = &ctl->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t tx = (uint32_t)(A_BYTES + (THREE ? 2 : 1) * bn * BK * 4);
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(t, num_m, num_n, group, mt, nt);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) break;
+          uint8_t* st = smem + s * L.bytes;
+          ptx::mbar_arrive_expect_tx(&ctl->full[s], tx);
+          ptx::tma_load_2d(st + L.a, &tmA, &ctl->full[s], kb * BK, mt * BM);
+          ptx::tma_load_2d(st + L.b_hi, &tmBh, &ctl->full[s], kb * BK, nt * bn);
+          if (THREE) ptx::tma_load_2d(st + L.b_lo, &tmBl, &ctl->full[s], kb * BK, nt * bn);
+          ++issued;
+          if (++s == L.stages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // Every copy issued must have landed before the CTA's shared memory is released.
+      for (int j = (issued > L.stages ? issued - L.stages : 0); j < issued; ++j)
+        drain_wait(&ctl->full[j % L.stages], (uint32_t)((j / L.stages) & 1));
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_tf32(BM, (uint32_t)bn, false, false);
+      int s = 0, tl = 0;
+      uint32_t ph = 0;
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tl) {
+        const int buf = tl & 1;
+        const uint32_t use = (uint32_t)(tl >> 1);
+        if (!wait_bar(&ctl->acce[buf], (use & 1u) ^ 1u, abort, kSiteMmaAccEmpty, wd)) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)buf * ACC_STRIDE;
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bar(THREE ? &ctl->split[s] : &ctl->full[s], ph, abort, kSiteMmaOperands, wd)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t st = ptx::smem_addr(smem + s * L.bytes);
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ++ks) {
+            const uint64_t ah = sw64_desc(st + L.a, ks), bh = sw64_desc(st + L.b_hi, ks);
+            const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+            if (THREE) {
+              const uint64_t al = sw64_desc(st + L.a_lo, ks), bl = sw64_desc(st + L.b_lo, ks);
+              ptx::mma_tf32(d, al, bh, idesc, acc);  // small terms first
+              ptx::mma_tf32(d, ah, bl, idesc, 1u);
+              ptx::mma_tf32(d, ah, bh, idesc, 1u);
+            } else {
+              ptx::mma_tf32(d, ah, bh, idesc, acc);
+            }
+          }
+          ptx::mma_commit(&ctl->empty[s]);
+          if (++s == L.stages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&ctl->accf[buf]);
+      }
+      // Every MMA issued must be done before TMEM is released.
+      ptx::mma_commit(&ctl->drain);
+      drain_wait(&ctl->drain, 0);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ----------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may read
+    float* stage = epi + (warp - 2) * 32 * EPI_PITCH;
+    int tl = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tl) {
+      const int buf = tl & 1;
+      const uint32_t use = (uint32_t)(tl >> 1);
+      int ok = 1;
+      if (lane == 0)
+        ok = wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      int mt, nt;
+      tile_coords(t, num_m, num_n, group, mt, nt);
+      drain_accumulator(tmem, q, (uint32_t)buf * ACC_STRIDE, bn, stage,
+                        Store{g, (int64_t)mt * BM, (int64_t)nt * bn});
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&ctl->acce[buf]);
+    }
+  } else if (THREE) {
+    // ------------------------------------------------ split warps: A_lo
+    const int tid = threadIdx.x - 192;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      bool ok = true;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!wait_bar(&ctl->full[s], ph, abort, kSiteSplitFull, wd)) {
+          ok = false;
+          break;
+        }
+        const float4* a = reinterpret_cast<const float4*>(smem + s * L.bytes + L.a);
+        float4* alo = reinterpret_cast<float4*>(smem + s * L.bytes + L.a_lo);
+#pragma unroll
+        for (int i = tid; i < A_BYTES / 16; i += 128) alo[i] = tf32_lo4(a[i]);
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(&ctl->split[s]);
+        if (++s == L.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------- host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Row-major fp32 matrix [outer, inner] -> tensor map with a {16, box_outer}
+// box (64-byte rows), 64-byte swizzle, zero fill outside the matrix.
+bool encode_k16(CUtensorMap* m, const float* base, uint64_t inner, uint64_t outer,
+                uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 4};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tile width: the BN (multiple of 32) whose number of waves times BN -- the
+// time of the last wave, in MMA columns -- is smallest; ties go to wider tiles.
+int pick_bn(int64_t M, int64_t N, int sms) {
+  const int64_t num_m = (M + BM - 1) / BM;
+  int best = BN_MAX;
+  int64_t best_cost = INT64_MAX;
+  for (int bn = BN_MAX; bn >= 32; bn -= 32) {
+    const int64_t tiles = num_m * ((N + bn - 1) / bn);
+    const int64_t cost = ((tiles + sms - 1) / sms) * (bn + 16);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+constexpr int kMaxDev = 64;
+
+template <bool THREE>
+cudaError_t run(const GemmArgs& g, const float* bt_hi, const float* bt_lo, cudaStream_t s) {
+  constexpr int smem = smem_bytes(THREE ? kL3 : kL1);
+  static bool ready[kMaxDev];
+  auto k = k_tc_gemm<THREE>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= kMaxDev || !ready[dev]) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev < kMaxDev) ready[dev] = true;
+  }
+  const int sms = device_sm_count();
+  const int bn = pick_bn(g.M, g.N, sms);
+  CUtensorMap ta, tbh, tbl;
+  if (!encode_k16(&ta, g.mat1, (uint64_t)g.K, (uint64_t)g.M, BM) ||
+      !encode_k16(&tbh, bt_hi, (uint64_t)g.K, (uint64_t)g.N, (uint32_t)bn) ||
+      !encode_k16(&tbl, THREE ? bt_lo : bt_hi, (uint64_t)g.K, (uint64_t)g.N, (uint32_t)bn))
+    return cudaErrorInvalidValue;
+  const int num_m = (int)((g.M + BM - 1) / BM), num_n = (int)((g.N + bn - 1) / bn);
+  const int tiles = num_m * num_n;
+  const int grid = tiles < sms ? tiles : sms;
+  const int group = num_m < 8 ? num_m : 8;
+  k<<<grid, THREE ? 320 : 192, smem, s>>>(ta, tbh, tbl, g, num_m, num_n, group, bn);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_gemm_supported(const GemmArgs& a) {
+  const bool aligned = (reinterpret_cast<uintptr_t>(a.mat1) & 15u) == 0;
+  const double tiles = (double)((a.M + BM - 1) / BM) * (double)((a.N + 31) / 32);
+  return a.K % 4 == 0 && aligned && tiles < 2147483647.0 && encode_fn() != nullptr;
+}
+
+size_t tc_gemm_workspace_bytes(int64_t N, int64_t K, bool three_pass) {
+  return (three_pass ? 2u : 1u) * (size_t)N * (size_t)K * sizeof(float);
+}
+
+cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace, cudaStream_t s) {
+  if (!tc_gemm_supported(g) || !workspace) return cudaErrorNotSupported;
+  float* bt_hi = static_cast<float*>(workspace);
+  float* bt_lo = three_pass ? bt_hi + g.N * g.K : nullptr;
+  const int64_t tiles = ((g.N + 31) / 32) * ((g.K + 31) / 32);
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  k_prep_b<<<(unsigned)(tiles < cap ? tiles : cap), dim3(32, 8), 0, s>>>(g.mat2, g.K, g.N, bt_hi,
+                                                                         bt_lo);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return three_pass ? run<true>(g, bt_hi, bt_lo, s) : run<false>(g, bt_hi, nullptr, s);
+}
+
+cudaError_t gemm_take_watchdog(int* value) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_watchdog_gemm, sizeof(int));
+  if (e != cudaSuccess) return e;
+  const int zero = 0;
+  return cudaMemcpyToSymbol(g_watchdog_gemm, &zero, sizeof(int));
+}
+
+}  // namespace imc

@@ -157,6 +157,7 @@ __device__ __forceinline__ void tmem_ld_wait() {
 //   bits 49-51 base offset (0: atoms 1024-byte aligned)
 //   bits 61-63 swizzle: 0 none, 1 128B/32B-atom, 2 128B, 4 64B, 6 32B
 constexpr uint32_t kSwizzle128B = 2;
+constexpr uint32_t kSwizzle64B = 4;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
                                               uint32_t swizzle) {

@@ -1,0 +1,167 @@
+// Device pieces shared by the tcgen05 kernels: bounded barrier waits, the
+// TF32 hi / lo split, K-major swizzled tile addressing, tile rasterisation and
+// the TMEM -> global epilogue.  Each kernel file includes this header once.
+#pragma once
+
+#include <cuda.h>
+
+#include "imc_internal.cuh"
+#include "ptx.cuh"
+
+namespace imc {
+namespace tc {
+
+constexpr int BM = 128;     // rows of one MMA tile (TMEM lanes)
+constexpr int UK = 8;       // K of one tcgen05.mma kind::tf32
+constexpr int EPI_PITCH = 36;  // floats per staged epilogue row
+constexpr int EPI_BYTES = 4 * 32 * EPI_PITCH * 4;
+constexpr int MAX_STAGES = 8;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+
+enum WaitSite {
+  kSiteProducerEmpty = 1,
+  kSiteSplitFull = 2,
+  kSiteMmaAccEmpty = 3,
+  kSiteMmaOperands = 4,
+  kSiteEpilogueAccFull = 5,
+};
+
+struct Ctl {
+  uint64_t full[MAX_STAGES];   // operands of a stage are in shared memory
+  uint64_t split[MAX_STAGES];  // the split / transform step of a stage is done
+  uint64_t empty[MAX_STAGES];  // the MMAs reading a stage are done
+  uint64_t accf[2];            // accumulator buffer holds a finished tile
+  uint64_t acce[2];            // epilogue has drained an accumulator buffer
+  uint64_t drain;              // all MMAs of this CTA are done
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Waits for the phase with the given parity; gives up after kWaitLimitNs
+// (recording `site` in *watchdog and raising the CTA's abort flag) or when
+// another role has raised the abort flag.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                         int site, int* watchdog) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 127u) == 0) {
+      if (*abort) return false;
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        atomicCAS(watchdog, 0, site);
+        return false;
+      }
+    }
+  }
+}
+
+// Teardown wait: ignores the abort flag, gives up after kDrainLimitNs.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kDrainLimitNs) break;
+  }
+}
+
+__device__ __forceinline__ void init_barriers(Ctl* ctl, int stages, uint32_t full_count,
+                                              uint32_t split_count) {
+  for (int s = 0; s < stages; ++s) {
+    ptx::mbar_init(&ctl->full[s], full_count);
+    ptx::mbar_init(&ctl->split[s], split_count);
+    ptx::mbar_init(&ctl->empty[s], 1);
+  }
+  for (int b = 0; b < 2; ++b) {
+    ptx::mbar_init(&ctl->accf[b], 1);
+    ptx::mbar_init(&ctl->acce[b], 128);
+  }
+  ptx::mbar_init(&ctl->drain, 1);
+  ctl->abort = 0;
+  ptx::fence_mbar_init();
+}
+
+// The tensor core reads an fp32 operand as TF32 by dropping its 13 low
+// mantissa bits (measured on GB300: round toward zero), so hi = v with those
+// bits cleared is what it sees of v, and lo = v - hi is exact in fp32.
+__device__ __forceinline__ float tf32_hi(float v) {
+  return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+}
+__device__ __forceinline__ float tf32_lo(float v) {
+  return isfinite(v) ? v - tf32_hi(v) : 0.0f;
+}
+__device__ __forceinline__ float4 tf32_lo4(float4 v) {
+  return make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
+}
+__device__ __forceinline__ float4 tf32_hi4(float4 v) {
+  return make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+}
+
+// K-major tile with 64-byte rows (16 fp32 of K) and the 64-byte swizzle:
+// 8-row groups of 512 B; inside a row the 16-byte unit u sits at u ^ ((row/2) % 4).
+// This is the layout a TMA box {16, rows} with CU_TENSOR_MAP_SWIZZLE_64B writes.
+__device__ __forceinline__ int sw64_row_base(int row) { return (row >> 3) * 512 + (row & 7) * 64; }
+__device__ __forceinline__ int sw64_unit(int row, int u) { return ((u ^ ((row >> 1) & 3))) << 4; }
+
+// UMMA shared-memory descriptor of a K-major SW64 tile; k-step `ks` (8 fp32)
+// is 32 B into the 64-byte row.
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t tile_addr, int ks) {
+  return ptx::smem_desc(tile_addr + ks * 32, 16, 512, ptx::kSwizzle64B);
+}
+
+// Grouped raster: `group` M-tiles share each N-tile before moving on, so the
+// CTAs resident at one time reuse the same operand panels from L2.
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group, int& mt,
+                                            int& nt) {
+  const int per = group * num_n;
+  const int gi = t / per;
+  const int m_first = gi * group;
+  const int rows = min(group, num_m - m_first);
+  const int r = t - gi * per;
+  mt = m_first + r % rows;
+  nt = r / rows;
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Reads `ncols` (a multiple of 32) accumulator columns of the 32 rows this
+// warp owns (TMEM lanes 32q .. 32q+31, starting at column `col`), transposes
+// each 32x32 block through the warp's staging area and hands 16-byte row
+// segments to the store functor: first store.load(row, col) for all eight
+// segments a lane handles in the block (so their global reads are in flight
+// together), then store(row, col, acc, loaded) for each.
+template <class StoreFn>
+__device__ __forceinline__ void drain_accumulator(uint32_t tmem, int q, uint32_t col, int ncols,
+                                                  float* stage, const StoreFn& store) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + col;
+#pragma unroll 1
+  for (int c = 0; c < ncols; c += 32) {
+    uint32_t r[32];
+    ptx::tmem_ld32(tbase + (uint32_t)c, r);
+    ptx::tmem_ld_wait();
+    float4* dst = reinterpret_cast<float4*>(stage + lane * EPI_PITCH);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                           __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+    __syncwarp();
+    float4 pre[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pre[i] = store.load(q * 32 + i * 4 + (lane >> 3), c + (lane & 7) * 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = i * 4 + (lane >> 3), cc = (lane & 7) * 4;
+      store(q * 32 + rr, c + cc, *reinterpret_cast<const float4*>(stage + rr * EPI_PITCH + cc),
+            pre[i]);
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace tc
+}  // namespace imc

@@ -366,7 +366,7 @@ def _cached(key, fn):
 def cpu_baseline(target_seconds=1.0):
     import oracle
     cores = oracle.default_threads()
-    rows, chans = 64, 64
+    rows, chans = 256, 128
     flops, dt = oracle_sample_step(cores, rows, chans)
     return {"value": round(flops / dt / 1e9, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{rows} seeded rows of the 8192x4096x4096 addmm + {chans} output channels "

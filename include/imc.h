@@ -5,9 +5,14 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All tensor pointers are DEVICE pointers to contiguous row-major fp32
- *    data owned by the caller.  The library never allocates, frees or keeps a
- *    pointer to them beyond the call; it may cache CUDA function attributes
- *    per device.
+ *    data owned by the caller.  The library never frees or keeps a pointer to
+ *    them beyond the call; it may cache CUDA function attributes per device.
+ *  - Device memory: the tensor-core kernels need scratch -- addmm a copy of
+ *    mat2 transposed and split into TF32 hi / lo parts, conv2d the weight
+ *    split the same way in zero-padded rows.  The *_ws entry points take it
+ *    from the caller and allocate nothing; the others take it from the
+ *    device's stream-ordered memory pool (cudaMallocAsync / cudaFreeAsync on
+ *    `stream`).  The scratch is dead once the call's work completes.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *    enqueued asynchronously on it; no entry point synchronises the host.
  *  - Every argument is checked before anything is launched.  A call that
@@ -25,6 +30,7 @@
 #ifndef IMC_H
 #define IMC_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -83,9 +89,9 @@ extern "C" {
  *   beta, alpha  finite scalars (the pages default both to 1.0, which the
  *           Python binding supplies); used in fp32.
  *   stream  cudaStream_t or NULL.
- * Kernel choice: the tcgen05 path needs K % 4 == 0, N % 4 == 0 and 16-byte
- * aligned mat1 / mat2 (TMA row strides); other shapes, and tiny problems,
- * take the SIMT kernel.  imc_last_kernel() reports which ran.
+ * Kernel choice: the tcgen05 path needs K % 4 == 0 and a 16-byte aligned
+ * mat1 (its rows are TMA-loaded); other shapes, and tiny problems, take the
+ * SIMT kernel.  imc_last_kernel() reports which ran.
  */
 int gemm_addmm_f32(const float* self, int self_2d, const float* mat1, const float* mat2,
                    float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
@@ -96,6 +102,24 @@ int gemm_addmm_f32(const float* self, int self_2d, const float* mat1, const floa
 int gemm_addmm_f32_ex(const float* self, int self_2d, const float* mat1, const float* mat2,
                       float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
                       int mode, void* stream);
+
+/* Bytes of device scratch gemm_addmm_f32_ws needs for these sizes and mode:
+ * 2*N*K*4 when the 3xTF32 tensor-core kernel would run, N*K*4 for the 1xTF32
+ * one, 0 when the SIMT or epilogue-only kernel would (assuming alpha != 0 and
+ * an aligned mat1; a call that then takes SIMT simply leaves it unused).
+ * Returns 0 for invalid sizes or mode. */
+size_t gemm_addmm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode);
+
+/* gemm_addmm_f32_ex with caller-provided scratch: `workspace` is a device
+ * buffer of `workspace_bytes` (>= gemm_addmm_f32_workspace_bytes(M, N, K,
+ * mode), 16-byte aligned, not overlapping any argument; may be NULL when that
+ * size is 0).  Nothing is allocated.  The buffer is dead once the work
+ * enqueued on `stream` completes; work using the same buffer concurrently on
+ * another stream races.  Too small, NULL or unaligned: IMC_ERR_ARG;
+ * overlapping: IMC_ERR_ALIAS. */
+int gemm_addmm_f32_ws(const float* self, int self_2d, const float* mat1, const float* mat2,
+                      float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                      int mode, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * conv2d_gemm_f32 -- groups==1, non-transposed NCHW convolution lowered to
@@ -120,7 +144,7 @@ int gemm_addmm_f32_ex(const float* self, int self_2d, const float* mat1, const f
  *   both axes; OH, OW must come out >= 1 (else IMC_ERR_SHAPE).  Every
  *   tensor must hold fewer than 2^31 elements.
  * Kernel choice: the tcgen05 path gathers the im2col operand itself and has
- * no alignment rule on x; tiny problems take the SIMT kernel.
+ * no alignment rule on x or w; tiny problems take the SIMT kernel.
  */
 int conv2d_gemm_f32(const float* x, const float* w, const float* bias, float* out, int64_t B,
                     int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
@@ -138,6 +162,21 @@ int conv2d_gemm_f32_nd(const float* x, const float* w, const float* bias, float*
                        int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
                        int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW,
                        int mode, void* stream);
+
+/* Bytes of device scratch conv2d_gemm_f32_ws needs for these arguments:
+ * 2*OC*Kp*4 for the 3xTF32 tensor-core kernel, OC*Kp*4 for the 1xTF32 one
+ * (Kp = IC*KH*KW rounded up to a multiple of 4), 0 otherwise or when the
+ * arguments are invalid. */
+size_t conv2d_gemm_f32_workspace_bytes(int64_t B, int64_t IC, int64_t H, int64_t W, int64_t OC,
+                                       int64_t KH, int64_t KW, int64_t sH, int64_t sW,
+                                       int64_t pH, int64_t pW, int64_t dH, int64_t dW, int mode);
+
+/* conv2d_gemm_f32_nd with caller-provided scratch (same rules as
+ * gemm_addmm_f32_ws); nothing is allocated. */
+int conv2d_gemm_f32_ws(const float* x, const float* w, const float* bias, float* out, int64_t B,
+                       int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
+                       int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW,
+                       int mode, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* imc_status_string(int status);

@@ -107,6 +107,34 @@ def test_empty_problems_are_noops(lib):
     assert binding.last_kernel() == "none"
 
 
+def test_workspace_size_query(lib):
+    q = binding.gemm_addmm_f32_workspace_bytes
+    assert q(1024, 3072, 768, 0) == 2 * 3072 * 768 * 4  # 3xTF32: hi and lo of mat2^T
+    assert q(1024, 3072, 768, 1) == 3072 * 768 * 4      # 1xTF32: mat2^T only
+    assert q(1024, 3072, 768, 2) == 0                   # SIMT needs none
+    assert q(64, 80, 96, 0) == 0                        # tiny: SIMT
+    assert q(64, 80, 96, 3) == 2 * 80 * 96 * 4          # forced tensor-core kernel
+    assert q(1024, 3072, 770, 0) == 0                   # K % 4 != 0: SIMT
+    assert q(0, 8, 8, 0) == 0 and q(8, 8, -1, 0) == 0 and q(8, 8, 8, 9) == 0
+
+
+def gws(ws, nbytes, M=256, N=256, K=256, mode=0, out=P4):
+    return binding.gemm_addmm_f32_ws(P1, 0, P2, P3, out, M, N, K, 1.0, 1.0, mode, ws, nbytes,
+                                     None)
+
+
+def test_workspace_argument_errors(lib):
+    need = binding.gemm_addmm_f32_workspace_bytes(256, 256, 256, 0)
+    W = 0x50000000
+    assert gws(W, need - 4) == binding.IMC_ERR_ARG       # too small
+    assert gws(None, need) == binding.IMC_ERR_ARG        # missing
+    assert gws(W + 4, need) == binding.IMC_ERR_ARG       # not 16-byte aligned
+    assert gws(P4 - 16, need) == binding.IMC_ERR_ALIAS   # overlaps out
+    assert gws(P2, need) == binding.IMC_ERR_ALIAS        # overlaps mat1
+    assert gws(W, need) == binding.IMC_ERR_DEVICE        # valid: needs a GPU
+    assert gws(None, 0, mode=2) == binding.IMC_ERR_DEVICE  # SIMT needs no workspace
+
+
 def c(x=P1, w=P2, bias=P3, out=P4, B=2, IC=3, H=8, W=8, OC=4, KH=3, KW=3, sH=1, sW=1, pH=1, pW=1,
       dH=1, dW=1, mode=0):
     return binding.conv2d_gemm_f32_nd(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH,
@@ -136,6 +164,30 @@ def test_conv_argument_errors(lib):
                                    None) == binding.IMC_ERR_SHAPE
     assert binding.conv2d_gemm_f32_ex(P1, P2, P3, P4, 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 5,
                                       None) == binding.IMC_ERR_ARG
+
+
+def test_conv_workspace_size_query(lib):
+    q = binding.conv2d_gemm_f32_workspace_bytes
+    body = (8, 256, 56, 56, 256, 3, 3, 1, 1, 1, 1, 1, 1)
+    assert q(*body, 0) == 2 * 256 * 2304 * 4   # hi and lo weight planes
+    assert q(*body, 1) == 256 * 2304 * 4
+    assert q(*body, 2) == 0
+    stem = (1, 3, 768, 768, 128, 7, 7, 4, 4, 3, 3, 1, 1)
+    assert q(*stem, 0) == 2 * 128 * 148 * 4    # K = 147 padded to 148
+    assert q(2, 3, 9, 9, 4, 3, 3, 1, 1, 1, 1, 1, 1, 0) == 0  # tiny: SIMT
+    assert q(2, 3, 2, 2, 4, 5, 5, 1, 1, 0, 0, 1, 1, 0) == 0  # empty output: invalid
+
+
+def test_conv_workspace_argument_errors(lib):
+    args = (P1, P2, P3, P4, 8, 256, 56, 56, 256, 3, 3, 1, 1, 1, 1, 1, 1, 0)
+    need = binding.conv2d_gemm_f32_workspace_bytes(*args[4:])
+    W = 0x50000000
+    f = binding.conv2d_gemm_f32_ws
+    assert f(*args, W, need - 1, None) == binding.IMC_ERR_ARG
+    assert f(*args, None, need, None) == binding.IMC_ERR_ARG
+    assert f(*args, W + 8, need, None) == binding.IMC_ERR_ARG
+    assert f(*args, P2 + 64, need, None) == binding.IMC_ERR_ALIAS  # overlaps w
+    assert f(*args, W, need, None) == binding.IMC_ERR_DEVICE
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")

@@ -89,14 +89,49 @@ def test_addmm_integer_inputs_are_bit_exact(mode, mnk):
     assert np.array_equal(got.astype(np.float64), ref), f"max diff {np.abs(got - ref).max()}"
 
 
-def test_addmm_unaligned_shapes_take_simt():
-    for M, N, K in [(70, 33, 40), (70, 40, 33), (5, 7, 3)]:
+def test_addmm_k_not_multiple_of_4_takes_simt():
+    for M, N, K in [(70, 40, 33), (5, 7, 3), (300, 260, 130)]:
         s, a, b = synth.addmm_inputs(M, N, K, self_2d=False, workload=5)
         got, ref, S, kern = run_addmm(s, a, b, 1.0, 1.0, "default")
         assert kern == "simt"
         within(got, ref, S, 1e-5, f"{M}x{N}x{K}")
         with pytest.raises(binding.ImcError):
             binding.addmm(dev(s), dev(a), dev(b), mode="force_tc3")
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1"])
+def test_addmm_odd_n_on_tensor_cores(mode):
+    # mat2 is transposed by the pre-pass, so N needs no alignment
+    for M, N, K, self_2d in [(70, 33, 40, False), (300, 257, 132, True), (129, 1, 64, True)]:
+        s, a, b = synth.addmm_inputs(M, N, K, self_2d=self_2d, workload=6)
+        got, ref, S, kern = run_addmm(s, a, b, 0.5, 1.5, mode)
+        assert kern == EXPECT[mode]
+        within(got, ref, S, TOL[mode], f"{mode} {M}x{N}x{K}")
+
+
+def test_addmm_workspace_paths_agree():
+    """The pool-backed entry point and the caller-workspace entry point run the
+    same kernels: identical bits."""
+    M, N, K = 600, 520, 388
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=True, workload=8)
+    S, A, B = dev(s), dev(a), dev(b)
+    stream = torch.cuda.current_stream().cuda_stream
+    for mode in (0, 1, 3):
+        o1 = torch.empty((M, N), device="cuda")
+        o2 = torch.empty((M, N), device="cuda")
+        rc = binding.gemm_addmm_f32_ex(S.data_ptr(), 1, A.data_ptr(), B.data_ptr(), o1.data_ptr(),
+                                       M, N, K, 0.25, 1.5, mode, stream)
+        assert rc == 0
+        nbytes = binding.gemm_addmm_f32_workspace_bytes(M, N, K, mode)
+        assert nbytes > 0
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        rc = binding.gemm_addmm_f32_ws(S.data_ptr(), 1, A.data_ptr(), B.data_ptr(), o2.data_ptr(),
+                                       M, N, K, 0.25, 1.5, mode, ws.data_ptr(), nbytes, stream)
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2)
+        ref, Sref = oracle.addmm(s, a, b, beta=0.25, alpha=1.5)
+        within(o1.cpu().numpy(), ref, Sref, 1e-5 if mode != 1 else 2e-3, f"mode {mode}")
 
 
 @pytest.mark.parametrize("mode", ["default", "simt", "force_tc3"])
@@ -250,8 +285,8 @@ def test_conv_workloads(name):
 def test_launch_counter_and_watchdog():
     n0 = binding.launch_count()
     s, a, b = synth.addmm_inputs(256, 256, 64, self_2d=False, workload=3)
-    binding.addmm(dev(s), dev(a), dev(b), mode="force_tc3")
+    binding.addmm(dev(s), dev(a), dev(b), mode="force_tc3")  # mat2 pre-pass + main kernel
     binding.addmm(dev(s), dev(a), dev(b), mode="simt")
     torch.cuda.synchronize()
-    assert binding.launch_count() == n0 + 2
+    assert binding.launch_count() == n0 + 3
     assert binding.check_device_error(None) == binding.IMC_OK
