@@ -24,6 +24,8 @@ IMC_ERR_ALIAS = -4
 IMC_ERR_CUDA = -5
 IMC_ERR_TIMEOUT = -6
 IMC_ERR_DEVICE = -7
+IMC_ERR_SCRATCH = -8
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 MODES = {"default": 0, "tf32": 1, "simt": 2, "force_tc3": 3, "force_tc1": 4}
 KERNELS = {0: "none", 1: "tc3", 2: "tc1", 3: "simt", 4: "fill"}
@@ -43,6 +45,8 @@ SIGNATURES = {
     "conv2d_gemm_f32_ws": (_int, [_vp, _vp, _vp, _vp] + [_i64] * 13 + [_int, _vp, ctypes.c_size_t,
                                                                       _vp]),
     "conv2d_gemm_f32_workspace_bytes": (ctypes.c_size_t, [_i64] * 13 + [_int]),
+    "gemm_addmm_f32_noalloc": (_int, [_vp, _int, _vp, _vp, _vp, _i64, _i64, _i64, _dbl, _dbl,
+                                      _int, _vp]),
     "imc_status_string": (ctypes.c_char_p, [_int]),
     "imc_last_kernel": (_int, []),
     "imc_launch_count": (ctypes.c_uint64, []),
@@ -94,6 +98,13 @@ def gemm_addmm_f32_ws(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode
                       workspace_bytes, stream) -> int:
     return load().gemm_addmm_f32_ws(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode,
                                     workspace, workspace_bytes, stream)
+
+
+def gemm_addmm_f32_noalloc(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode,
+                           stream) -> int:
+    """The addmm entry point that allocates nothing (fixed library buffer)."""
+    return load().gemm_addmm_f32_noalloc(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha,
+                                         mode, stream)
 
 
 def gemm_addmm_f32_workspace_bytes(M, N, K, mode) -> int:

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libimc.so")
-SOURCES = ["imc_api.cu", "k_simt.cu", "k_tc_gemm.cu", "k_tc_conv.cu"]
+SOURCES = ["imc_api.cu", "k_simt.cu", "k_tc_gemm.cu", "k_tc_conv.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

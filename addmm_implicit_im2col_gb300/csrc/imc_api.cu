@@ -388,6 +388,9 @@ const char* imc_status_string(int status) {
     case IMC_ERR_CUDA: return "IMC_ERR_CUDA: a CUDA call or kernel launch failed";
     case IMC_ERR_TIMEOUT: return "IMC_ERR_TIMEOUT: a kernel gave up waiting on a barrier";
     case IMC_ERR_DEVICE: return "IMC_ERR_DEVICE: no usable compute capability 10.3 device";
+    case IMC_ERR_SCRATCH:
+      return "IMC_ERR_SCRATCH: the problem needs more scratch than the no-allocation "
+             "entry point's fixed buffer holds";
     default: return "IMC_ERR_UNKNOWN";
   }
 }
@@ -409,3 +412,27 @@ int imc_check_device_error(void* stream) {
 int imc_version(void) { return 101; }
 
 }  // extern "C"
+
+// Hooks for the fixed-scratch addmm entry point (noalloc.cu).
+namespace imc {
+
+size_t gemm_scratch_needed(const float* mat1, int64_t M, int64_t N, int64_t K, double alpha,
+                           int mode) {
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
+  if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return 0;
+  const bool tc_ok = alpha != 0.0 && K % 4 == 0 && aligned16(mat1);
+  const int kernel = plan_gemm(M, N, K, alpha, mode, tc_ok);
+  if (kernel != IMC_KERNEL_TC3 && kernel != IMC_KERNEL_TC1) return 0;
+  return tc_gemm_workspace_bytes(N, K, kernel == IMC_KERNEL_TC3);
+}
+
+int gemm_with_scratch(const float* self, int self_2d, const float* mat1, const float* mat2,
+                      float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                      int mode, void* scratch, size_t scratch_bytes, void* stream) {
+  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, scratch,
+                   scratch_bytes, true, stream);
+}
+
+int require_device() { return check_device(); }
+
+}  // namespace imc

@@ -62,6 +62,16 @@ cudaError_t launch_tc_conv(const ConvArgs& a, bool three_pass, void* workspace, 
 cudaError_t gemm_take_watchdog(int* value);
 cudaError_t conv_take_watchdog(int* value);
 
+// Used by the fixed-scratch addmm entry point: the scratch bytes the call
+// with these arguments would use (0 when no tensor-core kernel runs), the
+// addmm itself on a caller-held scratch buffer, and the device check.
+size_t gemm_scratch_needed(const float* mat1, int64_t M, int64_t N, int64_t K, double alpha,
+                           int mode);
+int gemm_with_scratch(const float* self, int self_2d, const float* mat1, const float* mat2,
+                      float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                      int mode, void* scratch, size_t scratch_bytes, void* stream);
+int require_device();
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

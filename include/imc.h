@@ -46,6 +46,7 @@ extern "C" {
 #define IMC_ERR_CUDA (-5)    /* a CUDA runtime call or kernel launch failed       */
 #define IMC_ERR_TIMEOUT (-6) /* a kernel gave up waiting on one of its barriers   */
 #define IMC_ERR_DEVICE (-7)  /* no usable device of compute capability 10.3       */
+#define IMC_ERR_SCRATCH (-8) /* needs more than gemm_addmm_f32_noalloc's buffer  */
 
 /* ------------------------------------------------------------------- modes */
 #define IMC_MODE_DEFAULT 0 /* fp32-accurate: 3xTF32 tensor cores, SIMT when needed */
@@ -162,6 +163,38 @@ int conv2d_gemm_f32_nd(const float* x, const float* w, const float* bias, float*
                        int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
                        int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW,
                        int mode, void* stream);
+
+/*
+ * gemm_addmm_f32_noalloc -- gemm_addmm_f32_ex for callers that cannot
+ * allocate device memory while they run.  (The pages have no counterpart:
+ * this is a deployment option of this library.)
+ *
+ * Meant for programs whose device memory is fixed when they start, such as a
+ * real-time or embedded runtime with a set memory budget, or an operator in a
+ * host framework that forbids allocation inside its compute callback: for
+ * them an allocation on the call path can block behind other device work or
+ * fail under memory pressure mid-run.  Inputs and output are still the
+ * caller's.  The tensor-core path's scratch (mat2 transposed, split into hi /
+ * lo parts) lives in a fixed device buffer of IMC_NOALLOC_SCRATCH_BYTES
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits; no call allocates or frees anything.
+ *
+ * Limit: a problem whose scratch (gemm_addmm_f32_workspace_bytes) would
+ * exceed IMC_NOALLOC_SCRATCH_BYTES -- N*K above 4 Mi elements in the default
+ * mode, 8 Mi in IMC_MODE_TF32 -- returns IMC_ERR_SCRATCH before any CUDA
+ * call.  Problems that take the SIMT kernel need no scratch.
+ * Set-up: the first call on a device looks up the buffer's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before capturing any stream.
+ * Sharing: every call uses the same buffer.  Nothing in it needs to start at
+ * zero (each call writes all it reads), but calls whose work overlaps on the
+ * GPU -- on different streams, or from different host threads -- race on it.
+ * Other arguments, status codes and results are those of gemm_addmm_f32_ex.
+ */
+#define IMC_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int gemm_addmm_f32_noalloc(const float* self, int self_2d, const float* mat1, const float* mat2,
+                           float* out, int64_t M, int64_t N, int64_t K, double beta,
+                           double alpha, int mode, void* stream);
 
 /* Bytes of device scratch conv2d_gemm_f32_ws needs for these arguments:
  * 2*OC*Kp*4 for the 3xTF32 tensor-core kernel, OC*Kp*4 for the 1xTF32 one
