@@ -5,9 +5,11 @@ reject bad arguments with the documented status before touching CUDA.  On a
 machine without a GPU a well-formed call must fail loudly (IMC_ERR_DEVICE),
 never fall back to host code.
 """
-import ctypes
+import json
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 import torch
@@ -22,6 +24,26 @@ HEADER = os.path.join(ROOT, "include", "imc.h")
 def lib():
     build.build()
     return binding.load()
+
+
+# Calls whose arguments are valid up to the device check use fake addresses;
+# they run in a child process that sees no GPU (CUDA_VISIBLE_DEVICES=""), so
+# they can never launch anything, whatever machine runs the suite.
+_CHILD = r"""
+import json, sys
+sys.path.insert(0, sys.argv[1])
+from addmm_implicit_im2col_gb300 import binding
+calls = json.loads(sys.argv[2])
+print(json.dumps([getattr(binding, fn)(*args) for fn, args in calls]))
+"""
+
+
+def without_gpu(calls):
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", _CHILD, ROOT, json.dumps(calls)], env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def declared_functions():
@@ -91,14 +113,18 @@ def test_addmm_argument_errors(lib):
     assert g(self_2d=1, out=P1 + 4) == binding.IMC_ERR_ALIAS
 
 
+def gargs(self=P1, self_2d=0, mat1=P2, mat2=P3, out=P4, M=8, N=8, K=8, beta=1.0, alpha=1.0,
+          mode=0):
+    return ["gemm_addmm_f32_ex", [self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, None]]
+
+
 def test_addmm_unread_operands_may_be_null(lib):
-    # beta == 0: self is not read; alpha == 0 or K == 0: operands are not read.
-    # These pass validation and then need a device.
-    assert g(self=None, beta=0.0) == binding.IMC_ERR_DEVICE
-    assert g(mat1=None, mat2=None, alpha=0.0) == binding.IMC_ERR_DEVICE
-    assert g(mat1=None, mat2=None, K=0) == binding.IMC_ERR_DEVICE
-    # out may equal self for an in-place [M,N] addmm
-    assert g(self_2d=1, self=P4) == binding.IMC_ERR_DEVICE
+    # beta == 0: self is not read; alpha == 0 or K == 0: operands are not read;
+    # out may equal self for an in-place [M,N] addmm.  These pass validation
+    # and then need a device.
+    got = without_gpu([gargs(self=None, beta=0.0), gargs(mat1=None, mat2=None, alpha=0.0),
+                       gargs(mat1=None, mat2=None, K=0), gargs(self_2d=1, self=P4)])
+    assert got == [binding.IMC_ERR_DEVICE] * 4
 
 
 def test_empty_problems_are_noops(lib):
@@ -131,8 +157,9 @@ def test_workspace_argument_errors(lib):
     assert gws(W + 4, need) == binding.IMC_ERR_ARG       # not 16-byte aligned
     assert gws(P4 - 16, need) == binding.IMC_ERR_ALIAS   # overlaps out
     assert gws(P2, need) == binding.IMC_ERR_ALIAS        # overlaps mat1
-    assert gws(W, need) == binding.IMC_ERR_DEVICE        # valid: needs a GPU
-    assert gws(None, 0, mode=2) == binding.IMC_ERR_DEVICE  # SIMT needs no workspace
+    valid = ["gemm_addmm_f32_ws", [P1, 0, P2, P3, P4, 256, 256, 256, 1.0, 1.0, 0, W, need, None]]
+    simt = ["gemm_addmm_f32_ws", [P1, 0, P2, P3, P4, 256, 256, 256, 1.0, 1.0, 2, None, 0, None]]
+    assert without_gpu([valid, simt]) == [binding.IMC_ERR_DEVICE] * 2  # needs a GPU
 
 
 def c(x=P1, w=P2, bias=P3, out=P4, B=2, IC=3, H=8, W=8, OC=4, KH=3, KW=3, sH=1, sW=1, pH=1, pW=1,
@@ -156,7 +183,9 @@ def test_conv_argument_errors(lib):
     assert c(w=None) == binding.IMC_ERR_NULL
     assert c(out=P1) == binding.IMC_ERR_ALIAS
     assert c(out=P3 - 8) == binding.IMC_ERR_ALIAS
-    assert c(bias=None) == binding.IMC_ERR_DEVICE  # bias is optional
+    no_bias = ["conv2d_gemm_f32_nd", [P1, P2, None, P4, 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 1, 0,
+                                      None]]
+    assert without_gpu([no_bias]) == [binding.IMC_ERR_DEVICE]  # bias is optional
     assert c(B=0) == binding.IMC_OK
     assert c(OC=0) == binding.IMC_OK
     # the symmetric entry point maps onto the per-axis one
@@ -187,14 +216,15 @@ def test_conv_workspace_argument_errors(lib):
     assert f(*args, None, need, None) == binding.IMC_ERR_ARG
     assert f(*args, W + 8, need, None) == binding.IMC_ERR_ARG
     assert f(*args, P2 + 64, need, None) == binding.IMC_ERR_ALIAS  # overlaps w
-    assert f(*args, W, need, None) == binding.IMC_ERR_DEVICE
+    assert without_gpu([["conv2d_gemm_f32_ws", list(args) + [W, need, None]]]) == [
+        binding.IMC_ERR_DEVICE]
 
 
-@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
 def test_no_gpu_fails_loudly(lib):
-    assert g() == binding.IMC_ERR_DEVICE
-    assert c() == binding.IMC_ERR_DEVICE
-    assert binding.check_device_error(None) == binding.IMC_ERR_DEVICE
+    # a well-formed call on a machine without a usable GPU: an error, no host fallback
+    conv = ["conv2d_gemm_f32_nd", [P1, P2, P3, P4, 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 1, 0, None]]
+    got = without_gpu([gargs(), conv, ["check_device_error", [None]]])
+    assert got == [binding.IMC_ERR_DEVICE] * 3
 
 
 def test_torch_wrappers_validate_before_calling(lib):
