@@ -324,13 +324,28 @@ def run_gpu(args):
 
 
 def load_profiled_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if any."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
-    try:
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when there is none or a source file it lists has changed since the capture."""
+    import glob
+    import hashlib
+    import re
+    pat = re.compile(r"^TRAFFIC kernel=(\S+) bytes_per_launch=(\d+) source_sha256_16=(\w+) "
+                     r"sources=(\S+)$")
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         with open(path) as f:
-            return json.load(f).get(kernel)
-    except (OSError, ValueError):
-        return None
+            for line in f:
+                m = pat.match(line.strip())
+                if not m or m.group(1) != kernel:
+                    continue
+                digest = hashlib.sha256()
+                try:
+                    for src in m.group(4).split(","):
+                        with open(os.path.join(ROOT, src), "rb") as g:
+                            digest.update(g.read())
+                except OSError:
+                    return None
+                return int(m.group(2)) if digest.hexdigest()[:16] == m.group(3) else None
+    return None
 
 
 # ------------------------------------------------------- CPU baseline arm
