@@ -10,6 +10,7 @@
 // pages state is a WebGPU dispatch limit and is not reproduced.
 #include <atomic>
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 #include <mutex>
 
@@ -153,9 +154,13 @@ int gemm_impl(const float* self, int self_2d, const float* mat1, const float* ma
   const int kernel = plan_gemm(M, N, K, alpha, mode, tc_ok);
   if (kernel < 0) return IMC_ERR_SHAPE;
   const bool tc = kernel == IMC_KERNEL_TC3 || kernel == IMC_KERNEL_TC1;
-  const size_t need = tc ? tc_gemm_workspace_bytes(N, K, kernel == IMC_KERNEL_TC3) : 0;
-  if (caller_ws && need > 0) {
-    if (!workspace || ws_bytes < need || !aligned16(workspace)) return IMC_ERR_ARG;
+  const bool three = kernel == IMC_KERNEL_TC3;
+  // minimum (no split-K) and the scratch the call will use
+  const size_t need_min = tc ? tc_gemm_workspace_bytes(M, N, K, three, 0) : 0;
+  const size_t need = tc ? tc_gemm_workspace_bytes(M, N, K, three, caller_ws ? ws_bytes : SIZE_MAX)
+                         : 0;
+  if (caller_ws && need_min > 0) {
+    if (!workspace || ws_bytes < need_min || !aligned16(workspace)) return IMC_ERR_ARG;
     if (overlaps(workspace, need, out, out_bytes) || overlaps(workspace, need, mat1, mat1_bytes) ||
         overlaps(workspace, need, mat2, mat2_bytes) ||
         (read_self && overlaps(workspace, need, self, self_bytes)))
@@ -172,7 +177,7 @@ int gemm_impl(const float* self, int self_2d, const float* mat1, const float* ma
   if (!caller_ws) {
     if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return IMC_ERR_CUDA;
   }
-  const cudaError_t e = launch_tc_gemm(a, kernel == IMC_KERNEL_TC3, ws, s);
+  const cudaError_t e = launch_tc_gemm(a, three, ws, need, s);
   if (!caller_ws) {
     const cudaError_t f = cudaFreeAsync(ws, s);
     if (e == cudaSuccess && f != cudaSuccess) return IMC_ERR_CUDA;
@@ -209,8 +214,8 @@ size_t gemm_addmm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode)
   if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
   if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return 0;
   const int kernel = plan_gemm(M, N, K, 1.0, mode, K % 4 == 0);
-  if (kernel == IMC_KERNEL_TC3) return tc_gemm_workspace_bytes(N, K, true);
-  if (kernel == IMC_KERNEL_TC1) return tc_gemm_workspace_bytes(N, K, false);
+  if (kernel == IMC_KERNEL_TC3) return tc_gemm_workspace_bytes(M, N, K, true, SIZE_MAX);
+  if (kernel == IMC_KERNEL_TC1) return tc_gemm_workspace_bytes(M, N, K, false, SIZE_MAX);
   return 0;
 }
 
@@ -423,7 +428,7 @@ size_t gemm_scratch_needed(const float* mat1, int64_t M, int64_t N, int64_t K, d
   const bool tc_ok = alpha != 0.0 && K % 4 == 0 && aligned16(mat1);
   const int kernel = plan_gemm(M, N, K, alpha, mode, tc_ok);
   if (kernel != IMC_KERNEL_TC3 && kernel != IMC_KERNEL_TC1) return 0;
-  return tc_gemm_workspace_bytes(N, K, kernel == IMC_KERNEL_TC3);
+  return tc_gemm_workspace_bytes(M, N, K, kernel == IMC_KERNEL_TC3, 0);
 }
 
 int gemm_with_scratch(const float* self, int self_2d, const float* mat1, const float* mat2,

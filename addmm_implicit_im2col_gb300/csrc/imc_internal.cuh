@@ -46,11 +46,16 @@ cudaError_t launch_fill_conv(const ConvArgs& a, cudaStream_t s);
 // tcgen05 tensor-core kernels.  three_pass selects 3xTF32 (fp32 accuracy)
 // over a single TF32 product.  Return cudaErrorNotSupported when the shape
 // does not meet the kernel's requirements (the caller falls back to SIMT).
-// The addmm kernel needs a workspace of tc_gemm_workspace_bytes() (16-byte
-// aligned) for the transposed mat2; it is dead once the launch completes.
+// The addmm kernel needs a 16-byte aligned workspace for the transposed mat2
+// and, for problems with few output tiles, split-K partial sums; it is dead
+// once the launch completes.  tc_gemm_workspace_bytes(.., limit) is the size
+// of the best plan whose scratch fits in `limit` bytes: SIZE_MAX gives the
+// preferred size, 0 the minimum (no split-K); launch_tc_gemm plans within the
+// workspace it is given.
 bool tc_gemm_supported(const GemmArgs& a);
-size_t tc_gemm_workspace_bytes(int64_t N, int64_t K, bool three_pass);
-cudaError_t launch_tc_gemm(const GemmArgs& a, bool three_pass, void* workspace, cudaStream_t s);
+size_t tc_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool three_pass, size_t limit);
+cudaError_t launch_tc_gemm(const GemmArgs& a, bool three_pass, void* workspace,
+                           size_t workspace_bytes, cudaStream_t s);
 // The conv kernel needs tc_conv_workspace_bytes() for the padded hi / lo
 // weight planes.
 bool tc_conv_supported(const ConvArgs& a);

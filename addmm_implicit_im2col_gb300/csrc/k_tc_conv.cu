@@ -105,30 +105,32 @@ struct Store {
   }
 };
 
-// The 16 im2col taps k0 .. k0+15 of one column: kk -> (ic, kh, kw).
+// One im2col column (output position n) and the running tap (ic, kh, kw)
+// of kk = k0, kept across k-blocks so no division is needed per k-block.
 struct Column {
   const float* xb;  // image b of x
   int ih0, iw0;     // oh*sH - pH, ow*sW - pW
   bool ok;
 };
+struct Tap {
+  int ic, kh, kw;
+};
 
+// The 16 taps kk = k0 .. k0+15 of one column (zero outside the image and for
+// kk >= K); advances `tap` by 16.
 __device__ __forceinline__ void gather(const ConvArgs& c, const Column& col, int k0, int K,
-                                       float (&v)[BK]) {
-  int kw = k0 % c.KW;
-  const int u = k0 / c.KW;
-  int kh = u % c.KH;
-  int ic = u / c.KH;
+                                       Tap& tap, float (&v)[BK]) {
 #pragma unroll
   for (int j = 0; j < BK; ++j) {
-    const int ih = col.ih0 + kh * c.dH, iw = col.iw0 + kw * c.dW;
+    const int ih = col.ih0 + tap.kh * c.dH, iw = col.iw0 + tap.kw * c.dW;
     const bool in = col.ok && (k0 + j < K) && (unsigned)ih < (unsigned)c.H &&
                     (unsigned)iw < (unsigned)c.W;
-    v[j] = in ? __ldg(col.xb + ((ic * c.H + ih) * c.W + iw)) : 0.0f;
-    if (++kw == c.KW) {
-      kw = 0;
-      if (++kh == c.KH) {
-        kh = 0;
-        ++ic;
+    v[j] = in ? __ldg(col.xb + ((tap.ic * c.H + ih) * c.W + iw)) : 0.0f;
+    if (++tap.kw == c.KW) {
+      tap.kw = 0;
+      if (++tap.kh == c.KH) {
+        tap.kh = 0;
+        ++tap.ic;
       }
     }
   }
@@ -182,14 +184,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         col.iw0 = ow * c.sW - c.pW;
         col.xb = c.x + (int64_t)b * c.IC * c.H * c.W;
       }
-      float v[BK], vn[BK];
-      gather(c, col, 0, K, v);
-      for (int kb = 0; kb < num_kb; ++kb) {
-        if (kb + 1 < num_kb) gather(c, col, (kb + 1) * BK, K, vn);
-        if (!wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) {
-          ok = false;
-          break;
-        }
+      // Three register buffers, rotated by unrolling (copying a buffer whose
+      // loads are in flight would wait for them): the taps of k-blocks kb+1
+      // and kb+2 are in flight while k-block kb is stored.
+      Tap tap{0, 0, 0};
+      float va[BK], vb[BK], vc[BK];
+      auto store = [&](const float (&v)[BK]) -> bool {
+        if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) return false;
         if (pt < bn) {
           uint8_t* row = smem + s * C::STAGE + C::B_HI + sw64_row_base(pt);
 #pragma unroll
@@ -210,8 +211,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           s = 0;
           ph ^= 1u;
         }
-#pragma unroll
-        for (int j = 0; j < BK; ++j) v[j] = vn[j];
+        return true;
+      };
+      gather(c, col, 0, K, tap, va);
+      if (num_kb > 1) gather(c, col, BK, K, tap, vb);
+      for (int kb = 0; kb < num_kb && ok; kb += 3) {
+        if (kb + 2 < num_kb) gather(c, col, (kb + 2) * BK, K, tap, vc);
+        if (!(ok = store(va)) || kb + 1 >= num_kb) break;
+        if (kb + 3 < num_kb) gather(c, col, (kb + 3) * BK, K, tap, va);
+        if (!(ok = store(vb)) || kb + 2 >= num_kb) break;
+        if (kb + 4 < num_kb) gather(c, col, (kb + 4) * BK, K, tap, vb);
+        ok = store(vc);
       }
     }
   } else if (warp == TMA_WARP) {
@@ -303,11 +313,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tl) {
       const int buf = tl % C::NBUF;
       const uint32_t use = (uint32_t)(tl / C::NBUF);
-      int ok = 1;
-      if (lane == 0)
-        ok = wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (!warp_wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd)) break;
       ptx::tc_fence_after();
       const int mt = t % num_m, nt = t / num_m;
 #pragma unroll 1

@@ -128,18 +128,74 @@ struct Store {
   }
 };
 
+// Split-K: a unit's raw partial tile goes to part[slice][M][N].
+struct PartStore {
+  float* p;
+  int64_t M, N, m0, n0;
+  __device__ __forceinline__ float4 load(int, int) const { return make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ void operator()(int r, int c, float4 v, float4) const {
+    const int64_t m = m0 + r, n = n0 + c;
+    if (m >= M || n >= N) return;
+    float* o = p + m * N + n;
+    if (N % 4 == 0) {
+      *reinterpret_cast<float4*>(o) = v;
+    } else {
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+      for (int j = 0; j < 4 && n + j < N; ++j) o[j] = vv[j];
+    }
+  }
+};
+
+// Split-K epilogue: out = beta*self + alpha * sum over slices 0, 1, ... of the
+// partial tiles, always in that order (deterministic).
+__global__ void __launch_bounds__(256) k_splitk_epilogue(const float* __restrict__ part,
+                                                         const int splits, const GemmArgs g) {
+  const int64_t MN = g.M * g.N;
+  if (g.vec_out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < MN / 4;
+         i += (int64_t)gridDim.x * blockDim.x) {
+      const int64_t e = 4 * i, n = e % g.N;
+      float4 acc = *reinterpret_cast<const float4*>(part + e);
+      for (int sl = 1; sl < splits; ++sl) {
+        const float4 v = *reinterpret_cast<const float4*>(part + sl * MN + e);
+        acc = make_float4(acc.x + v.x, acc.y + v.y, acc.z + v.z, acc.w + v.w);
+      }
+      float4 bs = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g.read_self) {
+        const float4 sv = *reinterpret_cast<const float4*>(g.self + (g.self_2d ? e : n));
+        bs = make_float4(g.beta * sv.x, g.beta * sv.y, g.beta * sv.z, g.beta * sv.w);
+      }
+      *reinterpret_cast<float4*>(g.out + e) =
+          make_float4(fmaf(g.alpha, acc.x, bs.x), fmaf(g.alpha, acc.y, bs.y),
+                      fmaf(g.alpha, acc.z, bs.z), fmaf(g.alpha, acc.w, bs.w));
+    }
+  } else {
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < MN;
+         e += (int64_t)gridDim.x * blockDim.x) {
+      float acc = part[e];
+      for (int sl = 1; sl < splits; ++sl) acc += part[sl * MN + e];
+      const float bs = g.read_self ? g.beta * g.self[g.self_2d ? e : e % g.N] : 0.0f;
+      g.out[e] = fmaf(g.alpha, acc, bs);
+    }
+  }
+}
+
 template <bool THREE>
 __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBh,
               const __grid_constant__ CUtensorMap tmBl, const GemmArgs g, const int num_m,
-              const int num_n, const int group, const int bn) {
+              const int num_n, const int group, const int bn, const int splits, const int kps,
+              float* __restrict__ part) {
   constexpr Layout L = THREE ? kL3 : kL1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   float* epi = reinterpret_cast<float*>(smem + L.stages * L.bytes);
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + L.stages * L.bytes + EPI_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Work unit u = (tile u % num_tiles, K-slice u / num_tiles); a slice covers
+  // k-blocks [slice*kps, min(num_kb, (slice+1)*kps)).  splits == 1: whole K.
   const int num_tiles = num_m * num_n;
+  const int num_units = num_tiles * splits;
   const int num_kb = (int)((g.K + BK - 1) / BK);
   int* wd = &g_watchdog_gemm;
 
@@ -165,10 +221,11 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
       const uint32_t tx = (uint32_t)(A_BYTES + (THREE ? 2 : 1) * bn * BK * 4);
       int s = 0, issued = 0;
       uint32_t ph = 0;
-      for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
+      for (int u = blockIdx.x; u < num_units && !*abort; u += gridDim.x) {
         int mt, nt;
-        tile_coords(t, num_m, num_n, group, mt, nt);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        tile_coords(u % num_tiles, num_m, num_n, group, mt, nt);
+        const int kb0 = (u / num_tiles) * kps, kb1 = min(num_kb, kb0 + kps);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) break;
           uint8_t* st = smem + s * L.bytes;
           ptx::mbar_arrive_expect_tx(&ctl->full[s], tx);
@@ -192,14 +249,15 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
       const uint32_t idesc = ptx::idesc_tf32(BM, (uint32_t)bn, false, false);
       int s = 0, tl = 0;
       uint32_t ph = 0;
-      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tl) {
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++tl) {
         const int buf = tl & 1;
         const uint32_t use = (uint32_t)(tl >> 1);
         if (!wait_bar(&ctl->acce[buf], (use & 1u) ^ 1u, abort, kSiteMmaAccEmpty, wd)) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)buf * ACC_STRIDE;
+        const int kb0 = (u / num_tiles) * kps, kb1 = min(num_kb, kb0 + kps);
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar(THREE ? &ctl->split[s] : &ctl->full[s], ph, abort, kSiteMmaOperands, wd)) {
             ok = false;
             break;
@@ -209,7 +267,7 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
 #pragma unroll
           for (int ks = 0; ks < KSTEPS; ++ks) {
             const uint64_t ah = sw64_desc(st + L.a, ks), bh = sw64_desc(st + L.b_hi, ks);
-            const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+            const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
             if (THREE) {
               const uint64_t al = sw64_desc(st + L.a_lo, ks), bl = sw64_desc(st + L.b_lo, ks);
               ptx::mma_tf32(d, al, bh, idesc, acc);  // small terms first
@@ -238,19 +296,20 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
     const int q = warp & 3;  // TMEM lane quadrant this warp may read
     float* stage = epi + (warp - 2) * 32 * EPI_PITCH;
     int tl = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tl) {
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++tl) {
       const int buf = tl & 1;
       const uint32_t use = (uint32_t)(tl >> 1);
-      int ok = 1;
-      if (lane == 0)
-        ok = wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (!warp_wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd)) break;
       ptx::tc_fence_after();
       int mt, nt;
-      tile_coords(t, num_m, num_n, group, mt, nt);
-      drain_accumulator(tmem, q, (uint32_t)buf * ACC_STRIDE, bn, stage,
-                        Store{g, (int64_t)mt * BM, (int64_t)nt * bn});
+      tile_coords(u % num_tiles, num_m, num_n, group, mt, nt);
+      if (splits == 1)
+        drain_accumulator(tmem, q, (uint32_t)buf * ACC_STRIDE, bn, stage,
+                          Store{g, (int64_t)mt * BM, (int64_t)nt * bn});
+      else
+        drain_accumulator(tmem, q, (uint32_t)buf * ACC_STRIDE, bn, stage,
+                          PartStore{part + (int64_t)(u / num_tiles) * g.M * g.N, g.M, g.N,
+                                    (int64_t)mt * BM, (int64_t)nt * bn});
       ptx::tc_fence_before();
       ptx::mbar_arrive(&ctl->acce[buf]);
     }
@@ -259,9 +318,11 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
     const int tid = threadIdx.x - 192;
     int s = 0;
     uint32_t ph = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       bool ok = true;
-      for (int kb = 0; kb < num_kb; ++kb) {
+      const int kb0 = (u / num_tiles) * kps, kb1 = min(num_kb, kb0 + kps);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        // every thread polls: measured faster here than one lane per warp
         if (!wait_bar(&ctl->full[s], ph, abort, kSiteSplitFull, wd)) {
           ok = false;
           break;
@@ -326,27 +387,80 @@ bool encode_k16(CUtensorMap* m, const float* base, uint64_t inner, uint64_t oute
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tile width: the BN (multiple of 32) whose number of waves times BN -- the
-// time of the last wave, in MMA columns -- is smallest; ties go to wider tiles.
-int pick_bn(int64_t M, int64_t N, int sms) {
-  const int64_t num_m = (M + BM - 1) / BM;
-  int best = BN_MAX;
-  int64_t best_cost = INT64_MAX;
-  for (int bn = BN_MAX; bn >= 32; bn -= 32) {
-    const int64_t tiles = num_m * ((N + bn - 1) / bn);
-    const int64_t cost = ((tiles + sms - 1) / sms) * (bn + 16);
+// Raster group (M-tiles sharing each N-tile): with `sms` tiles resident, a
+// group of G M-tiles keeps G mat1 panels and about sms/G mat2^T panels live.
+// Pick G to minimise the estimated panel re-reads from DRAM:
+// mat1_bytes * ceil(num_n / (sms / G)) + mat2t_bytes * ceil(num_m / G).
+int pick_group(int64_t num_m, int64_t num_n, int sms, double a_bytes, double b_bytes) {
+  int best = 1;
+  double best_cost = 1e300;
+  for (int g = 1; g <= num_m && g <= sms; ++g) {
+    const int64_t cols = sms / g > 0 ? sms / g : 1;
+    const double cost = a_bytes * (double)((num_n + cols - 1) / cols) +
+                        b_bytes * (double)((num_m + g - 1) / g);
     if (cost < best_cost) {
       best_cost = cost;
-      best = bn;
+      best = g;
     }
   }
   return best;
 }
 
+// Launch plan.  It depends on the problem only (not on the device), so the
+// scratch size can be queried before a device is chosen; kPlanSMs is the SM
+// count of the GB300 it is tuned for.
+constexpr int kPlanSMs = 152;
+
+struct Plan {
+  int bn, num_m, num_n, splits, kps;
+  int64_t part_offset;  // byte offset of the split-K partials in the scratch
+};
+
+// Picks the tile width BN (multiple of 32) and the number of K-slices by an
+// estimate of the last SM's time in MMA column-k-blocks: waves * kps * (BN +
+// 32), plus, when split, the slice-sum pass ((splits + 1) * M*N*4 bytes at
+// HBM speed, ~1.5 ns per unit).  Ties go to wider tiles and fewer slices.
+// Only plans whose scratch fits in `limit` bytes are considered (a single
+// slice is always allowed: its scratch is the mat2 copy alone).
+Plan make_plan(int64_t M, int64_t N, int64_t K, bool three, size_t limit) {
+  const int64_t num_kb = (K + BK - 1) / BK;
+  Plan best{BN_MAX, (int)((M + BM - 1) / BM), 0, 1, (int)num_kb, 0};
+  const int64_t bt = (three ? 2 : 1) * N * K * (int64_t)sizeof(float);
+  const int64_t part_offset = (bt + 255) / 256 * 256;
+  double best_cost = 1e300;
+  for (int bn = BN_MAX; bn >= 32; bn -= 32) {
+    const int64_t tiles = best.num_m * ((N + bn - 1) / bn);
+    for (int sp = 1; sp <= 16; ++sp) {
+      const int64_t kps = (num_kb + sp - 1) / sp;
+      const int64_t eff = (num_kb + kps - 1) / kps;  // non-empty slices
+      if (sp > 1 && (kps < 4 || eff != sp)) continue;
+      if (sp > 1 && (double)part_offset + (double)sp * M * N * 4.0 > (double)limit) continue;
+      const int64_t units = tiles * sp;
+      const double waves = (double)((units + kPlanSMs - 1) / kPlanSMs);
+      double cost = waves * (double)kps * (bn + 32);
+      if (sp > 1) cost += (double)(sp + 1) * (double)M * (double)N * 4.0 / 9750.0;
+      if (cost < best_cost * 0.999) {
+        best_cost = cost;
+        best.bn = bn;
+        best.splits = sp;
+        best.kps = (int)kps;
+      }
+    }
+  }
+  best.num_n = (int)((N + best.bn - 1) / best.bn);
+  best.part_offset = part_offset;
+  return best;
+}
+
+size_t plan_bytes(const Plan& p, int64_t M, int64_t N) {
+  return (size_t)p.part_offset + (p.splits > 1 ? (size_t)p.splits * M * N * sizeof(float) : 0);
+}
+
 constexpr int kMaxDev = 64;
 
 template <bool THREE>
-cudaError_t run(const GemmArgs& g, const float* bt_hi, const float* bt_lo, cudaStream_t s) {
+cudaError_t run(const GemmArgs& g, const Plan& p, const float* bt_hi, const float* bt_lo,
+                float* part, cudaStream_t s) {
   constexpr int smem = smem_bytes(THREE ? kL3 : kL1);
   static bool ready[kMaxDev];
   auto k = k_tc_gemm<THREE>;
@@ -359,17 +473,23 @@ cudaError_t run(const GemmArgs& g, const float* bt_hi, const float* bt_lo, cudaS
     if (dev < kMaxDev) ready[dev] = true;
   }
   const int sms = device_sm_count();
-  const int bn = pick_bn(g.M, g.N, sms);
   CUtensorMap ta, tbh, tbl;
   if (!encode_k16(&ta, g.mat1, (uint64_t)g.K, (uint64_t)g.M, BM) ||
-      !encode_k16(&tbh, bt_hi, (uint64_t)g.K, (uint64_t)g.N, (uint32_t)bn) ||
-      !encode_k16(&tbl, THREE ? bt_lo : bt_hi, (uint64_t)g.K, (uint64_t)g.N, (uint32_t)bn))
+      !encode_k16(&tbh, bt_hi, (uint64_t)g.K, (uint64_t)g.N, (uint32_t)p.bn) ||
+      !encode_k16(&tbl, THREE ? bt_lo : bt_hi, (uint64_t)g.K, (uint64_t)g.N, (uint32_t)p.bn))
     return cudaErrorInvalidValue;
-  const int num_m = (int)((g.M + BM - 1) / BM), num_n = (int)((g.N + bn - 1) / bn);
-  const int tiles = num_m * num_n;
-  const int grid = tiles < sms ? tiles : sms;
-  const int group = num_m < 8 ? num_m : 8;
-  k<<<grid, THREE ? 320 : 192, smem, s>>>(ta, tbh, tbl, g, num_m, num_n, group, bn);
+  const int units = p.num_m * p.num_n * p.splits;
+  const int grid = units < sms ? units : sms;
+  const int group = pick_group(p.num_m, p.num_n, kPlanSMs, (double)g.M * g.K * 4.0,
+                               (THREE ? 8.0 : 4.0) * (double)g.N * g.K);
+  k<<<grid, THREE ? 320 : 192, smem, s>>>(ta, tbh, tbl, g, p.num_m, p.num_n, group, p.bn,
+                                          p.splits, p.kps, part);
+  note_launch();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.splits == 1) return e;
+  const int64_t items = g.vec_out ? g.M * g.N / 4 : g.M * g.N;
+  const int64_t cap = (int64_t)sms * 8, blocks = (items + 255) / 256;
+  k_splitk_epilogue<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(part, p.splits, g);
   note_launch();
   return cudaGetLastError();
 }
@@ -382,14 +502,18 @@ bool tc_gemm_supported(const GemmArgs& a) {
   return a.K % 4 == 0 && aligned && tiles < 2147483647.0 && encode_fn() != nullptr;
 }
 
-size_t tc_gemm_workspace_bytes(int64_t N, int64_t K, bool three_pass) {
-  return (three_pass ? 2u : 1u) * (size_t)N * (size_t)K * sizeof(float);
+size_t tc_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool three_pass, size_t limit) {
+  return plan_bytes(make_plan(M, N, K, three_pass, limit), M, N);
 }
 
-cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace, cudaStream_t s) {
+cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
+                           size_t workspace_bytes, cudaStream_t s) {
   if (!tc_gemm_supported(g) || !workspace) return cudaErrorNotSupported;
+  const Plan p = make_plan(g.M, g.N, g.K, three_pass, workspace_bytes);
+  if (plan_bytes(p, g.M, g.N) > workspace_bytes) return cudaErrorInvalidValue;
   float* bt_hi = static_cast<float*>(workspace);
   float* bt_lo = three_pass ? bt_hi + g.N * g.K : nullptr;
+  float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.part_offset);
   const int64_t tiles = ((g.N + 31) / 32) * ((g.K + 31) / 32);
   const int64_t cap = (int64_t)device_sm_count() * 8;
   k_prep_b<<<(unsigned)(tiles < cap ? tiles : cap), dim3(32, 8), 0, s>>>(g.mat2, g.K, g.N, bt_hi,
@@ -397,7 +521,8 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace, 
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return three_pass ? run<true>(g, bt_hi, bt_lo, s) : run<false>(g, bt_hi, nullptr, s);
+  return three_pass ? run<true>(g, p, bt_hi, bt_lo, part, s)
+                    : run<false>(g, p, bt_hi, nullptr, part, s);
 }
 
 cudaError_t gemm_take_watchdog(int* value) {

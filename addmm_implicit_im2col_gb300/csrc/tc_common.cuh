@@ -59,6 +59,16 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
+// wait_bar for a whole warp: lane 0 polls, the result is broadcast, and the
+// warp leaves converged (32 lanes spinning on one barrier only add shared-
+// memory traffic and issue slots).
+__device__ __forceinline__ bool warp_wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              int site, int* watchdog) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort, site, watchdog) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // Teardown wait: ignores the abort flag, gives up after kDrainLimitNs.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer_ns();

@@ -104,20 +104,23 @@ int gemm_addmm_f32_ex(const float* self, int self_2d, const float* mat1, const f
                       float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
                       int mode, void* stream);
 
-/* Bytes of device scratch gemm_addmm_f32_ws needs for these sizes and mode:
- * 2*N*K*4 when the 3xTF32 tensor-core kernel would run, N*K*4 for the 1xTF32
- * one, 0 when the SIMT or epilogue-only kernel would (assuming alpha != 0 and
- * an aligned mat1; a call that then takes SIMT simply leaves it unused).
- * Returns 0 for invalid sizes or mode. */
+/* Bytes of device scratch the addmm prefers for these sizes and mode: the
+ * copy of mat2 transposed and split (2*N*K*4 bytes when the 3xTF32
+ * tensor-core kernel would run, N*K*4 for 1xTF32), plus split-K partial sums
+ * (slices*M*N*4) for problems with too few output tiles to fill the GPU; 0
+ * when the SIMT or epilogue-only kernel would run (assuming alpha != 0 and an
+ * aligned mat1).  Returns 0 for invalid sizes or mode. */
 size_t gemm_addmm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode);
 
 /* gemm_addmm_f32_ex with caller-provided scratch: `workspace` is a device
- * buffer of `workspace_bytes` (>= gemm_addmm_f32_workspace_bytes(M, N, K,
- * mode), 16-byte aligned, not overlapping any argument; may be NULL when that
- * size is 0).  Nothing is allocated.  The buffer is dead once the work
- * enqueued on `stream` completes; work using the same buffer concurrently on
- * another stream races.  Too small, NULL or unaligned: IMC_ERR_ARG;
- * overlapping: IMC_ERR_ALIAS. */
+ * buffer of `workspace_bytes`, 16-byte aligned, not overlapping any argument
+ * (may be NULL when no scratch is needed).  It must hold at least the mat2
+ * copy (2*N*K*4 or N*K*4 bytes); the kernel plans within the buffer given, so
+ * gemm_addmm_f32_workspace_bytes() bytes give the fastest plan and fewer
+ * bytes a plan with fewer (or no) split-K slices.  Nothing is allocated.
+ * The buffer is dead once the work enqueued on `stream` completes; work using
+ * it concurrently on another stream races.  Too small, NULL or unaligned:
+ * IMC_ERR_ARG; overlapping: IMC_ERR_ALIAS. */
 int gemm_addmm_f32_ws(const float* self, int self_2d, const float* mat1, const float* mat2,
                       float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
                       int mode, void* workspace, size_t workspace_bytes, void* stream);
@@ -179,10 +182,11 @@ int conv2d_gemm_f32_nd(const float* x, const float* w, const float* bias, float*
  * inside the library, which every GPU that loads the library holds until the
  * process exits; no call allocates or frees anything.
  *
- * Limit: a problem whose scratch (gemm_addmm_f32_workspace_bytes) would
- * exceed IMC_NOALLOC_SCRATCH_BYTES -- N*K above 4 Mi elements in the default
- * mode, 8 Mi in IMC_MODE_TF32 -- returns IMC_ERR_SCRATCH before any CUDA
- * call.  Problems that take the SIMT kernel need no scratch.
+ * Limit: a problem whose mat2 copy alone would exceed
+ * IMC_NOALLOC_SCRATCH_BYTES -- N*K above 4 Mi elements in the default mode,
+ * 8 Mi in IMC_MODE_TF32 -- returns IMC_ERR_SCRATCH before any CUDA call; the
+ * kernel plans its split-K partial sums within what is left of the buffer.
+ * Problems that take the SIMT kernel need no scratch.
  * Set-up: the first call on a device looks up the buffer's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
  * before capturing any stream.

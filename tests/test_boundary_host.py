@@ -137,6 +137,8 @@ def test_workspace_size_query(lib):
     q = binding.gemm_addmm_f32_workspace_bytes
     assert q(1024, 3072, 768, 0) == 2 * 3072 * 768 * 4  # 3xTF32: hi and lo of mat2^T
     assert q(1024, 3072, 768, 1) == 3072 * 768 * 4      # 1xTF32: mat2^T only
+    # few output tiles and a long K: the preferred plan adds split-K partial sums
+    assert q(1024, 768, 3072, 0) > 2 * 768 * 3072 * 4
     assert q(1024, 3072, 768, 2) == 0                   # SIMT needs none
     assert q(64, 80, 96, 0) == 0                        # tiny: SIMT
     assert q(64, 80, 96, 3) == 2 * 80 * 96 * 4          # forced tensor-core kernel
@@ -151,15 +153,19 @@ def gws(ws, nbytes, M=256, N=256, K=256, mode=0, out=P4):
 
 def test_workspace_argument_errors(lib):
     need = binding.gemm_addmm_f32_workspace_bytes(256, 256, 256, 0)
+    minimum = 2 * 256 * 256 * 4  # the mat2 copy alone; more lets the plan split K
+    assert need >= minimum
     W = 0x50000000
-    assert gws(W, need - 4) == binding.IMC_ERR_ARG       # too small
+    assert gws(W, minimum - 4) == binding.IMC_ERR_ARG    # too small
     assert gws(None, need) == binding.IMC_ERR_ARG        # missing
     assert gws(W + 4, need) == binding.IMC_ERR_ARG       # not 16-byte aligned
     assert gws(P4 - 16, need) == binding.IMC_ERR_ALIAS   # overlaps out
     assert gws(P2, need) == binding.IMC_ERR_ALIAS        # overlaps mat1
     valid = ["gemm_addmm_f32_ws", [P1, 0, P2, P3, P4, 256, 256, 256, 1.0, 1.0, 0, W, need, None]]
     simt = ["gemm_addmm_f32_ws", [P1, 0, P2, P3, P4, 256, 256, 256, 1.0, 1.0, 2, None, 0, None]]
-    assert without_gpu([valid, simt]) == [binding.IMC_ERR_DEVICE] * 2  # needs a GPU
+    at_min = ["gemm_addmm_f32_ws", [P1, 0, P2, P3, P4, 256, 256, 256, 1.0, 1.0, 0, W, minimum,
+                                    None]]
+    assert without_gpu([valid, simt, at_min]) == [binding.IMC_ERR_DEVICE] * 3  # needs a GPU
 
 
 def c(x=P1, w=P2, bias=P3, out=P4, B=2, IC=3, H=8, W=8, OC=4, KH=3, KW=3, sH=1, sW=1, pH=1, pW=1,
