@@ -8,7 +8,7 @@ __all__ = ["binding", "synth"]
 
 
 def __getattr__(name):
-    if name in ("addmm", "conv2d", "gemm_addmm_f32", "conv2d_gemm_f32"):
+    if name in ("addmm", "conv2d", "linear", "gemm_addmm_f32", "conv2d_gemm_f32", "linear_f32"):
         from . import binding
         return getattr(binding, name)
     raise AttributeError(name)

@@ -27,8 +27,9 @@ IMC_ERR_DEVICE = -7
 IMC_ERR_SCRATCH = -8
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
-MODES = {"default": 0, "tf32": 1, "simt": 2, "force_tc3": 3, "force_tc1": 4}
-KERNELS = {0: "none", 1: "tc3", 2: "tc1", 3: "simt", 4: "fill"}
+MODES = {"default": 0, "tf32": 1, "simt": 2, "force_tc3": 3, "force_tc1": 4, "direct": 5}
+ACT_RELU = 0x100
+KERNELS = {0: "none", 1: "tc3", 2: "tc1", 3: "simt", 4: "fill", 5: "direct"}
 
 # Every symbol the header declares, with (restype, argtypes).
 _i64, _dbl, _vp, _int = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
@@ -47,6 +48,9 @@ SIGNATURES = {
     "conv2d_gemm_f32_workspace_bytes": (ctypes.c_size_t, [_i64] * 13 + [_int]),
     "gemm_addmm_f32_noalloc": (_int, [_vp, _int, _vp, _vp, _vp, _i64, _i64, _i64, _dbl, _dbl,
                                       _int, _vp]),
+    "linear_f32": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]),
+    "linear_f32_ws": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, ctypes.c_size_t, _vp]),
+    "linear_f32_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64, _int]),
     "imc_status_string": (ctypes.c_char_p, [_int]),
     "imc_last_kernel": (_int, []),
     "imc_launch_count": (ctypes.c_uint64, []),
@@ -141,6 +145,18 @@ def conv2d_gemm_f32_workspace_bytes(B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH,
                                                       dH, dW, mode))
 
 
+def linear_f32(x, w, bias, out, M, N, K, mode, stream) -> int:
+    return load().linear_f32(x, w, bias, out, M, N, K, mode, stream)
+
+
+def linear_f32_ws(x, w, bias, out, M, N, K, mode, workspace, workspace_bytes, stream) -> int:
+    return load().linear_f32_ws(x, w, bias, out, M, N, K, mode, workspace, workspace_bytes, stream)
+
+
+def linear_f32_workspace_bytes(M, N, K, mode) -> int:
+    return int(load().linear_f32_workspace_bytes(M, N, K, mode))
+
+
 def status_string(status: int) -> str:
     return load().imc_status_string(status).decode()
 
@@ -179,11 +195,16 @@ def _check_tensor(t, name, ndim=None):
         raise ValueError(f"{name} must have {ndim} dimensions")
 
 
-def addmm(self, mat1, mat2, *, beta=1.0, alpha=1.0, mode="default", out=None):
+def _mode(mode, relu):
+    return MODES[mode] | (ACT_RELU if relu else 0)
+
+
+def addmm(self, mat1, mat2, *, beta=1.0, alpha=1.0, mode="default", relu=False, out=None):
     """out = beta*self + alpha*(mat1 @ mat2) on the GPU (aten.addmm semantics).
 
     self is [N] or [M, N]; alpha and beta default to 1.0.  ``mode`` is one of
-    ``MODES``.  Returns ``out`` (allocated with torch when not given).
+    ``MODES``; ``relu`` fuses max(v, 0) into the epilogue.  Returns ``out``
+    (allocated with torch when not given).
     """
     import torch
     _check_tensor(mat1, "mat1", (2,))
@@ -209,10 +230,38 @@ def addmm(self, mat1, mat2, *, beta=1.0, alpha=1.0, mode="default", out=None):
     nbytes = gemm_addmm_f32_workspace_bytes(M, N, K, MODES[mode])
     ws = torch.empty(nbytes, dtype=torch.uint8, device=mat1.device) if nbytes else None
     rc = gemm_addmm_f32_ws(_ptr(self), self_2d, _ptr(mat1), _ptr(mat2), _ptr(out), M, N, K,
-                           float(beta), float(alpha), MODES[mode], _ptr(ws), nbytes,
+                           float(beta), float(alpha), _mode(mode, relu), _ptr(ws), nbytes,
                            _stream_ptr(mat1.device))
     if rc != IMC_OK:
         raise ImcError(rc, "gemm_addmm_f32")
+    return out
+
+
+def linear(x, w, bias=None, *, mode="default", relu=False, out=None):
+    """out = x @ w^T (+ bias) on the GPU (aten.linear semantics).
+
+    x is [M, K], w is [N, K] (the transposed weight), bias [N] or None.
+    """
+    import torch
+    _check_tensor(x, "x", (2,))
+    _check_tensor(w, "w", (2,))
+    _check_tensor(bias, "bias", (1,))
+    M, K = x.shape
+    N, K2 = w.shape
+    if K2 != K:
+        raise ValueError(f"w must be [N, K] = [N, {K}], got {list(w.shape)}")
+    if bias is not None and bias.shape[0] != N:
+        raise ValueError("bias must be [N]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    else:
+        _check_tensor(out, "out", (2,))
+    nbytes = linear_f32_workspace_bytes(M, N, K, MODES[mode])
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=x.device) if nbytes else None
+    rc = linear_f32_ws(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), M, N, K, _mode(mode, relu),
+                       _ptr(ws), nbytes, _stream_ptr(x.device))
+    if rc != IMC_OK:
+        raise ImcError(rc, "linear_f32")
     return out
 
 
@@ -225,7 +274,8 @@ def _pair(v):
     return (int(v[0]), int(v[1])) if isinstance(v, (tuple, list)) else (int(v), int(v))
 
 
-def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, *, mode="default", out=None):
+def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, *, mode="default", relu=False,
+           out=None):
     """groups==1 NCHW conv2d via the implicit-im2col GEMM.
 
     x [B, IC, H, W], w [OC, IC, KH, KW], bias [OC] or None; stride, padding and
@@ -256,7 +306,7 @@ def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, *, mode="default", 
                                              MODES[mode])
     ws = torch.empty(nbytes, dtype=torch.uint8, device=x.device) if nbytes else None
     rc = conv2d_gemm_f32_ws(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), B, IC, H, W, OC, KH, KW,
-                            sH, sW, pH, pW, dH, dW, MODES[mode], _ptr(ws), nbytes,
+                            sH, sW, pH, pW, dH, dW, _mode(mode, relu), _ptr(ws), nbytes,
                             _stream_ptr(x.device))
     if rc != IMC_OK:
         raise ImcError(rc, "conv2d_gemm_f32")

@@ -93,6 +93,16 @@ using namespace imc;
 
 namespace {
 
+// Splits a mode argument into the kernel mode and the ReLU flag.  False for
+// unknown bits or a kernel mode the operation does not have (IMC_MODE_DIRECT
+// is conv-only).
+bool parse_mode(int mode, bool conv, int* base, int* relu) {
+  if (mode & ~(0xFF | IMC_ACT_RELU)) return false;
+  *base = mode & 0xFF;
+  *relu = (mode & IMC_ACT_RELU) ? 1 : 0;
+  return *base >= IMC_MODE_DEFAULT && *base <= (conv ? IMC_MODE_DIRECT : IMC_MODE_FORCE_TC1);
+}
+
 // Which kernel a well-formed addmm takes.  `tc_ok` is whether the tcgen05
 // path can take the operands (K % 4 == 0, aligned mat1).
 int plan_gemm(int64_t M, int64_t N, int64_t K, double alpha, int mode, bool tc_ok) {
@@ -109,11 +119,13 @@ int plan_gemm(int64_t M, int64_t N, int64_t K, double alpha, int mode, bool tc_o
 // from the device's stream-ordered pool (cudaMallocAsync / cudaFreeAsync on
 // `stream`).  caller_ws: the caller's buffer of ws_bytes is used, nothing is
 // allocated.
+// b_kmajor: mat2 is given transposed as [N,K] (linear).
 int gemm_impl(const float* self, int self_2d, const float* mat1, const float* mat2, float* out,
-              int64_t M, int64_t N, int64_t K, double beta, double alpha, int mode,
-              void* workspace, size_t ws_bytes, bool caller_ws, void* stream) {
+              int64_t M, int64_t N, int64_t K, double beta, double alpha, int mode_arg,
+              bool b_kmajor, void* workspace, size_t ws_bytes, bool caller_ws, void* stream) {
   if (self_2d != 0 && self_2d != 1) return IMC_ERR_ARG;
-  if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return IMC_ERR_ARG;
+  int mode = 0, relu = 0;
+  if (!parse_mode(mode_arg, false, &mode, &relu)) return IMC_ERR_ARG;
   if (!std::isfinite(beta) || !std::isfinite(alpha)) return IMC_ERR_ARG;
   if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return IMC_ERR_SHAPE;
   if (M == 0 || N == 0) {
@@ -150,15 +162,18 @@ int gemm_impl(const float* self, int self_2d, const float* mat1, const float* ma
   a.self_2d = self_2d;
   a.read_self = read_self ? 1 : 0;
   a.vec_out = (N % 4 == 0) && aligned16(out) && (!read_self || aligned16(self)) ? 1 : 0;
-  const bool tc_ok = read_ops && K % 4 == 0 && aligned16(mat1);
+  a.relu = relu;
+  a.b_kmajor = b_kmajor ? 1 : 0;
+  const bool tc_ok =
+      read_ops && K % 4 == 0 && aligned16(mat1) && (!b_kmajor || aligned16(mat2));
   const int kernel = plan_gemm(M, N, K, alpha, mode, tc_ok);
   if (kernel < 0) return IMC_ERR_SHAPE;
   const bool tc = kernel == IMC_KERNEL_TC3 || kernel == IMC_KERNEL_TC1;
   const bool three = kernel == IMC_KERNEL_TC3;
   // minimum (no split-K) and the scratch the call will use
-  const size_t need_min = tc ? tc_gemm_workspace_bytes(M, N, K, three, 0) : 0;
-  const size_t need = tc ? tc_gemm_workspace_bytes(M, N, K, three, caller_ws ? ws_bytes : SIZE_MAX)
-                         : 0;
+  const size_t need_min = tc ? tc_gemm_workspace_bytes(M, N, K, three, b_kmajor, 0) : 0;
+  const size_t need =
+      tc ? tc_gemm_workspace_bytes(M, N, K, three, b_kmajor, caller_ws ? ws_bytes : SIZE_MAX) : 0;
   if (caller_ws && need_min > 0) {
     if (!workspace || ws_bytes < need_min || !aligned16(workspace)) return IMC_ERR_ARG;
     if (overlaps(workspace, need, out, out_bytes) || overlaps(workspace, need, mat1, mat1_bytes) ||
@@ -174,11 +189,10 @@ int gemm_impl(const float* self, int self_2d, const float* mat1, const float* ma
   if (kernel == IMC_KERNEL_SIMT) return finish(launch_simt_gemm(a, s), kernel);
   if (!tc_gemm_supported(a)) return IMC_ERR_DEVICE;  // driver without tensor-map support
   void* ws = workspace;
-  if (!caller_ws) {
-    if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return IMC_ERR_CUDA;
-  }
+  const bool pool = !caller_ws && need > 0;
+  if (pool && cudaMallocAsync(&ws, need, s) != cudaSuccess) return IMC_ERR_CUDA;
   const cudaError_t e = launch_tc_gemm(a, three, ws, need, s);
-  if (!caller_ws) {
+  if (pool) {
     const cudaError_t f = cudaFreeAsync(ws, s);
     if (e == cudaSuccess && f != cudaSuccess) return IMC_ERR_CUDA;
   }
@@ -192,31 +206,60 @@ extern "C" {
 int gemm_addmm_f32_ex(const float* self, int self_2d, const float* mat1, const float* mat2,
                       float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
                       int mode, void* stream) {
-  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, nullptr, 0, false,
-                   stream);
+  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, false, nullptr, 0,
+                   false, stream);
 }
 
 int gemm_addmm_f32(const float* self, int self_2d, const float* mat1, const float* mat2,
                    float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
                    void* stream) {
-  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, IMC_MODE_DEFAULT,
+  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, IMC_MODE_DEFAULT, false,
                    nullptr, 0, false, stream);
 }
 
 int gemm_addmm_f32_ws(const float* self, int self_2d, const float* mat1, const float* mat2,
                       float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
                       int mode, void* workspace, size_t workspace_bytes, void* stream) {
-  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, workspace,
+  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, false, workspace,
                    workspace_bytes, true, stream);
 }
 
-size_t gemm_addmm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode) {
+}  // extern "C"
+
+namespace {
+size_t gemm_query(int64_t M, int64_t N, int64_t K, int mode_arg, bool b_kmajor) {
   if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
-  if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return 0;
+  int mode = 0, relu = 0;
+  if (!parse_mode(mode_arg, false, &mode, &relu)) return 0;
   const int kernel = plan_gemm(M, N, K, 1.0, mode, K % 4 == 0);
-  if (kernel == IMC_KERNEL_TC3) return tc_gemm_workspace_bytes(M, N, K, true, SIZE_MAX);
-  if (kernel == IMC_KERNEL_TC1) return tc_gemm_workspace_bytes(M, N, K, false, SIZE_MAX);
+  if (kernel == IMC_KERNEL_TC3) return tc_gemm_workspace_bytes(M, N, K, true, b_kmajor, SIZE_MAX);
+  if (kernel == IMC_KERNEL_TC1) return tc_gemm_workspace_bytes(M, N, K, false, b_kmajor, SIZE_MAX);
   return 0;
+}
+}  // namespace
+
+extern "C" {
+
+size_t gemm_addmm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode) {
+  return gemm_query(M, N, K, mode, false);
+}
+
+// aten.linear on the addmm path with mat2 = w given as [N,K], self = bias [N].
+int linear_f32(const float* x, const float* w, const float* bias, float* out, int64_t M,
+               int64_t N, int64_t K, int mode, void* stream) {
+  return gemm_impl(bias, 0, x, w, out, M, N, K, bias ? 1.0 : 0.0, 1.0, mode, true, nullptr, 0,
+                   false, stream);
+}
+
+size_t linear_f32_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode) {
+  return gemm_query(M, N, K, mode, true);
+}
+
+int linear_f32_ws(const float* x, const float* w, const float* bias, float* out, int64_t M,
+                  int64_t N, int64_t K, int mode, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  return gemm_impl(bias, 0, x, w, out, M, N, K, bias ? 1.0 : 0.0, 1.0, mode, true, workspace,
+                   workspace_bytes, true, stream);
 }
 
 }  // extern "C"
@@ -256,6 +299,7 @@ int conv_shape(int64_t B, int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t 
 int plan_conv(int64_t M, int64_t N, int64_t K, int mode) {
   if (M == 0 || N == 0) return IMC_KERNEL_NONE;
   if (K == 0) return IMC_KERNEL_FILL;
+  if (mode == IMC_MODE_DIRECT) return IMC_KERNEL_DIRECT;
   if (mode == IMC_MODE_FORCE_TC3) return IMC_KERNEL_TC3;
   if (mode == IMC_MODE_FORCE_TC1) return IMC_KERNEL_TC1;
   if (mode == IMC_MODE_SIMT || (double)M * N * K < (double)kTinyMacs) return IMC_KERNEL_SIMT;
@@ -264,9 +308,10 @@ int plan_conv(int64_t M, int64_t N, int64_t K, int mode) {
 
 int conv_impl(const float* x, const float* w, const float* bias, float* out, int64_t B,
               int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW, int64_t sH,
-              int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW, int mode,
+              int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW, int mode_arg,
               void* workspace, size_t ws_bytes, bool caller_ws, void* stream) {
-  if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return IMC_ERR_ARG;
+  int mode = 0, relu = 0;
+  if (!parse_mode(mode_arg, true, &mode, &relu)) return IMC_ERR_ARG;
   ConvShape cs;
   const int sh = conv_shape(B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, &cs);
   if (sh != IMC_OK) return sh;
@@ -319,9 +364,11 @@ int conv_impl(const float* x, const float* w, const float* bias, float* out, int
   c.N = B * OH * OW;
   c.K = K;
   c.vec_out = ((OH * OW) % 4 == 0) && aligned16(out) ? 1 : 0;
+  c.relu = relu;
   cudaStream_t s = (cudaStream_t)stream;
 
   if (kernel == IMC_KERNEL_FILL) return finish(launch_fill_conv(c, s), kernel);
+  if (kernel == IMC_KERNEL_DIRECT) return finish(launch_direct_conv(c, s), kernel);
   if (kernel == IMC_KERNEL_SIMT) return finish(launch_simt_conv(c, s), kernel);
   if (!tc_conv_supported(c)) return IMC_ERR_DEVICE;
   void* ws = workspace;
@@ -359,8 +406,9 @@ int conv2d_gemm_f32_ws(const float* x, const float* w, const float* bias, float*
 size_t conv2d_gemm_f32_workspace_bytes(int64_t B, int64_t IC, int64_t H, int64_t W, int64_t OC,
                                        int64_t KH, int64_t KW, int64_t sH, int64_t sW,
                                        int64_t pH, int64_t pW, int64_t dH, int64_t dW,
-                                       int mode) {
-  if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return 0;
+                                       int mode_arg) {
+  int mode = 0, relu = 0;
+  if (!parse_mode(mode_arg, true, &mode, &relu)) return 0;
   ConvShape cs;
   if (conv_shape(B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, &cs) != IMC_OK) return 0;
   const int kernel = plan_conv(OC, B * cs.OH * cs.OW, cs.K, mode);
@@ -422,19 +470,20 @@ int imc_version(void) { return 101; }
 namespace imc {
 
 size_t gemm_scratch_needed(const float* mat1, int64_t M, int64_t N, int64_t K, double alpha,
-                           int mode) {
+                           int mode_arg) {
   if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
-  if (mode < IMC_MODE_DEFAULT || mode > IMC_MODE_FORCE_TC1) return 0;
+  int mode = 0, relu = 0;
+  if (!parse_mode(mode_arg, false, &mode, &relu)) return 0;
   const bool tc_ok = alpha != 0.0 && K % 4 == 0 && aligned16(mat1);
   const int kernel = plan_gemm(M, N, K, alpha, mode, tc_ok);
   if (kernel != IMC_KERNEL_TC3 && kernel != IMC_KERNEL_TC1) return 0;
-  return tc_gemm_workspace_bytes(M, N, K, kernel == IMC_KERNEL_TC3, 0);
+  return tc_gemm_workspace_bytes(M, N, K, kernel == IMC_KERNEL_TC3, false, 0);
 }
 
 int gemm_with_scratch(const float* self, int self_2d, const float* mat1, const float* mat2,
                       float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
                       int mode, void* scratch, size_t scratch_bytes, void* stream) {
-  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, scratch,
+  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, false, scratch,
                    scratch_bytes, true, stream);
 }
 

@@ -18,6 +18,8 @@ struct GemmArgs {
   int self_2d;        // 1: self is [M,N]
   int read_self;      // beta != 0
   int vec_out;        // out (and self) allow 16-byte vector access: N % 4 == 0, aligned
+  int relu;           // apply max(v, 0) to every output
+  int b_kmajor;       // mat2 is given transposed, [N,K] (aten.linear weight)
 };
 
 // One conv2d problem after validation, already viewed as the GEMM
@@ -32,6 +34,7 @@ struct ConvArgs {
   int OH, OW;
   int64_t M, N, K;
   int vec_out;        // OH*OW % 4 == 0 and out 16-byte aligned
+  int relu;           // apply max(v, 0) to every output
 };
 
 // SIMT fp32 FFMA kernels (any shape, any alignment).
@@ -43,6 +46,10 @@ cudaError_t launch_simt_conv(const ConvArgs& a, cudaStream_t s);
 cudaError_t launch_fill_gemm(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_fill_conv(const ConvArgs& a, cudaStream_t s);
 
+// Direct conv2d: one thread per output element, receptive field read from
+// global memory for every output (the design the implicit GEMM replaces).
+cudaError_t launch_direct_conv(const ConvArgs& a, cudaStream_t s);
+
 // tcgen05 tensor-core kernels.  three_pass selects 3xTF32 (fp32 accuracy)
 // over a single TF32 product.  Return cudaErrorNotSupported when the shape
 // does not meet the kernel's requirements (the caller falls back to SIMT).
@@ -53,7 +60,8 @@ cudaError_t launch_fill_conv(const ConvArgs& a, cudaStream_t s);
 // preferred size, 0 the minimum (no split-K); launch_tc_gemm plans within the
 // workspace it is given.
 bool tc_gemm_supported(const GemmArgs& a);
-size_t tc_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool three_pass, size_t limit);
+size_t tc_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool three_pass, bool b_kmajor,
+                               size_t limit);
 cudaError_t launch_tc_gemm(const GemmArgs& a, bool three_pass, void* workspace,
                            size_t workspace_bytes, cudaStream_t s);
 // The conv kernel needs tc_conv_workspace_bytes() for the padded hi / lo

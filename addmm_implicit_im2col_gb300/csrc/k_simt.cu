@@ -22,7 +22,7 @@ struct GemmOperands {
     return a.mat1[m * a.K + k];
   }
   __device__ __forceinline__ float load_b(int64_t k, int64_t n) const {
-    return a.mat2[k * a.N + n];
+    return a.b_kmajor ? a.mat2[n * a.K + k] : a.mat2[k * a.N + n];  // linear: w[n, k]
   }
   __device__ __forceinline__ void store_row4(int64_t m, int64_t n0, const float* acc) const {
     float* o = a.out + m * a.N;
@@ -34,13 +34,15 @@ struct GemmOperands {
       r.y = a.read_self ? fmaf(a.alpha, acc[1], a.beta * sv.y) : a.alpha * acc[1];
       r.z = a.read_self ? fmaf(a.alpha, acc[2], a.beta * sv.z) : a.alpha * acc[2];
       r.w = a.read_self ? fmaf(a.alpha, acc[3], a.beta * sv.w) : a.alpha * acc[3];
+      if (a.relu) r = make_float4(fmaxf(r.x, 0.f), fmaxf(r.y, 0.f), fmaxf(r.z, 0.f), fmaxf(r.w, 0.f));
       *reinterpret_cast<float4*>(o + n0) = r;
       return;
     }
     for (int j = 0; j < 4; ++j) {
       int64_t n = n0 + j;
       if (n >= a.N) break;
-      o[n] = a.read_self ? fmaf(a.alpha, acc[j], a.beta * sp[n]) : a.alpha * acc[j];
+      const float v = a.read_self ? fmaf(a.alpha, acc[j], a.beta * sp[n]) : a.alpha * acc[j];
+      o[n] = a.relu ? fmaxf(v, 0.f) : v;
     }
   }
   __device__ __forceinline__ int64_t M() const { return a.M; }
@@ -75,7 +77,8 @@ struct ConvOperands {
       int64_t n = n0 + j;
       if (n >= c.N) break;
       const int64_t b = n / P, p = n - b * P;
-      c.out[(b * c.OC + m) * P + p] = acc[j] + bv;
+      const float v = acc[j] + bv;
+      c.out[(b * c.OC + m) * P + p] = c.relu ? fmaxf(v, 0.f) : v;
     }
   }
   __device__ __forceinline__ int64_t M() const { return c.M; }
@@ -141,7 +144,7 @@ __global__ void k_fill_gemm(const GemmArgs a) {
     const int64_t n = e % a.N;
     float v = 0.0f;
     if (a.read_self) v = a.beta * (a.self_2d ? a.self[e] : a.self[n]);
-    a.out[e] = v;
+    a.out[e] = a.relu ? fmaxf(v, 0.f) : v;
   }
 }
 
@@ -151,7 +154,42 @@ __global__ void k_fill_conv(const ConvArgs c) {
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t oc = (e / P) % c.OC;
-    c.out[e] = c.bias ? c.bias[oc] : 0.0f;
+    const float v = c.bias ? c.bias[oc] : 0.0f;
+    c.out[e] = c.relu ? fmaxf(v, 0.f) : v;
+  }
+}
+
+// Direct convolution (the conv page's Problem paragraph: one thread per output
+// element re-reading its receptive field from global memory, no reuse across
+// threads).  Consecutive threads take consecutive ow, so output stores and
+// input loads along a row are coalesced.  fp32 FMA in (ic, kh, kw) order.
+__global__ void __launch_bounds__(256) k_direct_conv(const ConvArgs c) {
+  const int64_t P = (int64_t)c.OH * c.OW;
+  const int64_t total = (int64_t)c.B * c.OC * P;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int ow = (int)(e % c.OW);
+    const int64_t t = e / c.OW;
+    const int oh = (int)(t % c.OH);
+    const int64_t u = t / c.OH;
+    const int oc = (int)(u % c.OC);
+    const int b = (int)(u / c.OC);
+    const float* xb = c.x + (int64_t)b * c.IC * c.H * c.W;
+    const float* wr = c.w + (int64_t)oc * c.K;
+    float acc = 0.0f;
+    for (int ic = 0; ic < c.IC; ++ic)
+      for (int kh = 0; kh < c.KH; ++kh) {
+        const int ih = oh * c.sH - c.pH + kh * c.dH;
+        if (ih < 0 || ih >= c.H) continue;
+        for (int kw = 0; kw < c.KW; ++kw) {
+          const int iw = ow * c.sW - c.pW + kw * c.dW;
+          if (iw < 0 || iw >= c.W) continue;
+          acc = fmaf(__ldg(wr + (ic * c.KH + kh) * c.KW + kw),
+                     __ldg(xb + ((int64_t)ic * c.H + ih) * c.W + iw), acc);
+        }
+      }
+    const float v = acc + (c.bias ? __ldg(c.bias + oc) : 0.0f);
+    c.out[e] = c.relu ? fmaxf(v, 0.f) : v;
   }
 }
 
@@ -189,6 +227,14 @@ cudaError_t launch_simt_conv(const ConvArgs& c, cudaStream_t s) {
 
 cudaError_t launch_fill_gemm(const GemmArgs& a, cudaStream_t s) {
   k_fill_gemm<<<fill_blocks(a.M * a.N), 256, 0, s>>>(a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_direct_conv(const ConvArgs& c, cudaStream_t s) {
+  const int64_t total = (int64_t)c.B * c.OC * c.OH * c.OW;
+  const int64_t cap = (int64_t)device_sm_count() * 16, blocks = (total + 255) / 256;
+  k_direct_conv<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(c);
   note_launch();
   return cudaGetLastError();
 }

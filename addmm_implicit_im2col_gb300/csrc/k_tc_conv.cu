@@ -91,15 +91,16 @@ struct Store {
     if (col >= bn || m >= c.M || n >= c.N) return;
     const float bv = b4.x;
     const int64_t P = (int64_t)c.OH * c.OW;
+    float4 o4 = make_float4(v.x + bv, v.y + bv, v.z + bv, v.w + bv);
+    if (c.relu) o4 = make_float4(fmaxf(o4.x, 0.f), fmaxf(o4.y, 0.f), fmaxf(o4.z, 0.f), fmaxf(o4.w, 0.f));
     if (c.vec_out && col + 3 < bn) {  // P % 4 == 0: n .. n+3 lie in one image
       const int64_t b = n / P, p = n - b * P;
-      *reinterpret_cast<float4*>(c.out + (b * c.OC + m) * P + p) =
-          make_float4(v.x + bv, v.y + bv, v.z + bv, v.w + bv);
+      *reinterpret_cast<float4*>(c.out + (b * c.OC + m) * P + p) = o4;
     } else {
-      const float vv[4] = {v.x, v.y, v.z, v.w};
+      const float vv[4] = {o4.x, o4.y, o4.z, o4.w};
       for (int j = 0; j < 4 && n + j < c.N && col + j < bn; ++j) {
         const int64_t nn = n + j, b = nn / P, p = nn - b * P;
-        c.out[(b * c.OC + m) * P + p] = vv[j] + bv;
+        c.out[(b * c.OC + m) * P + p] = vv[j];
       }
     }
   }
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // loads are in flight would wait for them): the taps of k-blocks kb+1
       // and kb+2 are in flight while k-block kb is stored.
       Tap tap{0, 0, 0};
+      auto next = [&](int kb, float (&v)[BK]) { gather(c, col, kb * BK, K, tap, v); };
       float va[BK], vb[BK], vc[BK];
       auto store = [&](const float (&v)[BK]) -> bool {
         if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) return false;
@@ -213,14 +215,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         return true;
       };
-      gather(c, col, 0, K, tap, va);
-      if (num_kb > 1) gather(c, col, BK, K, tap, vb);
+      next(0, va);
+      if (num_kb > 1) next(1, vb);
       for (int kb = 0; kb < num_kb && ok; kb += 3) {
-        if (kb + 2 < num_kb) gather(c, col, (kb + 2) * BK, K, tap, vc);
+        if (kb + 2 < num_kb) next(kb + 2, vc);
         if (!(ok = store(va)) || kb + 1 >= num_kb) break;
-        if (kb + 3 < num_kb) gather(c, col, (kb + 3) * BK, K, tap, va);
+        if (kb + 3 < num_kb) next(kb + 3, va);
         if (!(ok = store(vb)) || kb + 2 >= num_kb) break;
-        if (kb + 4 < num_kb) gather(c, col, (kb + 4) * BK, K, tap, vb);
+        if (kb + 4 < num_kb) next(kb + 4, vb);
         ok = store(vc);
       }
     }

@@ -91,6 +91,15 @@ __global__ void __launch_bounds__(256) k_prep_b(const float* __restrict__ mat2, 
   }
 }
 
+// linear: the weight w[N,K] is already K-major and serves as B_hi as it is
+// (the tensor core truncates to TF32); 3xTF32 needs only w_lo = w - tf32(w).
+__global__ void __launch_bounds__(256) k_prep_blo(const float* __restrict__ w, int64_t total,
+                                                  float* __restrict__ w_lo) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x)
+    w_lo[i] = tf32_lo(__ldg(w + i));
+}
+
 // ------------------------------------------------------------ main kernel
 struct Store {
   const GemmArgs& g;
@@ -117,8 +126,9 @@ struct Store {
     const int64_t m = m0 + r, n = n0 + c;
     if (m >= g.M || n >= g.N) return;
     float* o = g.out + m * g.N + n;
-    const float4 o4 = make_float4(fmaf(g.alpha, v.x, bs.x), fmaf(g.alpha, v.y, bs.y),
-                                  fmaf(g.alpha, v.z, bs.z), fmaf(g.alpha, v.w, bs.w));
+    float4 o4 = make_float4(fmaf(g.alpha, v.x, bs.x), fmaf(g.alpha, v.y, bs.y),
+                            fmaf(g.alpha, v.z, bs.z), fmaf(g.alpha, v.w, bs.w));
+    if (g.relu) o4 = make_float4(fmaxf(o4.x, 0.f), fmaxf(o4.y, 0.f), fmaxf(o4.z, 0.f), fmaxf(o4.w, 0.f));
     if (g.vec_out) {  // N % 4 == 0 and 16-byte aligned rows: n .. n+3 are in range
       *reinterpret_cast<float4*>(o) = o4;
     } else {
@@ -165,9 +175,11 @@ __global__ void __launch_bounds__(256) k_splitk_epilogue(const float* __restrict
         const float4 sv = *reinterpret_cast<const float4*>(g.self + (g.self_2d ? e : n));
         bs = make_float4(g.beta * sv.x, g.beta * sv.y, g.beta * sv.z, g.beta * sv.w);
       }
-      *reinterpret_cast<float4*>(g.out + e) =
-          make_float4(fmaf(g.alpha, acc.x, bs.x), fmaf(g.alpha, acc.y, bs.y),
-                      fmaf(g.alpha, acc.z, bs.z), fmaf(g.alpha, acc.w, bs.w));
+      float4 o4 = make_float4(fmaf(g.alpha, acc.x, bs.x), fmaf(g.alpha, acc.y, bs.y),
+                              fmaf(g.alpha, acc.z, bs.z), fmaf(g.alpha, acc.w, bs.w));
+      if (g.relu)
+        o4 = make_float4(fmaxf(o4.x, 0.f), fmaxf(o4.y, 0.f), fmaxf(o4.z, 0.f), fmaxf(o4.w, 0.f));
+      *reinterpret_cast<float4*>(g.out + e) = o4;
     }
   } else {
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < MN;
@@ -175,7 +187,8 @@ __global__ void __launch_bounds__(256) k_splitk_epilogue(const float* __restrict
       float acc = part[e];
       for (int sl = 1; sl < splits; ++sl) acc += part[sl * MN + e];
       const float bs = g.read_self ? g.beta * g.self[g.self_2d ? e : e % g.N] : 0.0f;
-      g.out[e] = fmaf(g.alpha, acc, bs);
+      const float v = fmaf(g.alpha, acc, bs);
+      g.out[e] = g.relu ? fmaxf(v, 0.f) : v;
     }
   }
 }
@@ -394,7 +407,8 @@ bool encode_k16(CUtensorMap* m, const float* base, uint64_t inner, uint64_t oute
 int pick_group(int64_t num_m, int64_t num_n, int sms, double a_bytes, double b_bytes) {
   int best = 1;
   double best_cost = 1e300;
-  for (int g = 1; g <= num_m && g <= sms; ++g) {
+  // groups above 16 measured slower on the 32768x1024x1024 workload
+  for (int g = 1; g <= num_m && g <= sms && g <= 16; ++g) {
     const int64_t cols = sms / g > 0 ? sms / g : 1;
     const double cost = a_bytes * (double)((num_n + cols - 1) / cols) +
                         b_bytes * (double)((num_m + g - 1) / g);
@@ -422,10 +436,12 @@ struct Plan {
 // HBM speed, ~1.5 ns per unit).  Ties go to wider tiles and fewer slices.
 // Only plans whose scratch fits in `limit` bytes are considered (a single
 // slice is always allowed: its scratch is the mat2 copy alone).
-Plan make_plan(int64_t M, int64_t N, int64_t K, bool three, size_t limit) {
+Plan make_plan(int64_t M, int64_t N, int64_t K, bool three, bool b_kmajor, size_t limit) {
   const int64_t num_kb = (K + BK - 1) / BK;
   Plan best{BN_MAX, (int)((M + BM - 1) / BM), 0, 1, (int)num_kb, 0};
-  const int64_t bt = (three ? 2 : 1) * N * K * (int64_t)sizeof(float);
+  // mat2 copy: transposed hi (+ lo); a K-major B needs only its lo part
+  const int64_t copies = b_kmajor ? (three ? 1 : 0) : (three ? 2 : 1);
+  const int64_t bt = copies * N * K * (int64_t)sizeof(float);
   const int64_t part_offset = (bt + 255) / 256 * 256;
   double best_cost = 1e300;
   for (int bn = BN_MAX; bn >= 32; bn -= 32) {
@@ -497,32 +513,46 @@ cudaError_t run(const GemmArgs& g, const Plan& p, const float* bt_hi, const floa
 }  // namespace
 
 bool tc_gemm_supported(const GemmArgs& a) {
-  const bool aligned = (reinterpret_cast<uintptr_t>(a.mat1) & 15u) == 0;
+  const bool aligned = (reinterpret_cast<uintptr_t>(a.mat1) & 15u) == 0 &&
+                       (!a.b_kmajor || (reinterpret_cast<uintptr_t>(a.mat2) & 15u) == 0);
   const double tiles = (double)((a.M + BM - 1) / BM) * (double)((a.N + 31) / 32);
   return a.K % 4 == 0 && aligned && tiles < 2147483647.0 && encode_fn() != nullptr;
 }
 
-size_t tc_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool three_pass, size_t limit) {
-  return plan_bytes(make_plan(M, N, K, three_pass, limit), M, N);
+size_t tc_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool three_pass, bool b_kmajor,
+                               size_t limit) {
+  return plan_bytes(make_plan(M, N, K, three_pass, b_kmajor, limit), M, N);
 }
 
 cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
                            size_t workspace_bytes, cudaStream_t s) {
-  if (!tc_gemm_supported(g) || !workspace) return cudaErrorNotSupported;
-  const Plan p = make_plan(g.M, g.N, g.K, three_pass, workspace_bytes);
-  if (plan_bytes(p, g.M, g.N) > workspace_bytes) return cudaErrorInvalidValue;
-  float* bt_hi = static_cast<float*>(workspace);
-  float* bt_lo = three_pass ? bt_hi + g.N * g.K : nullptr;
+  if (!tc_gemm_supported(g)) return cudaErrorNotSupported;
+  const Plan p = make_plan(g.M, g.N, g.K, three_pass, g.b_kmajor != 0, workspace_bytes);
+  if (plan_bytes(p, g.M, g.N) > workspace_bytes || (plan_bytes(p, g.M, g.N) > 0 && !workspace))
+    return cudaErrorInvalidValue;
+  float* ws = static_cast<float*>(workspace);
   float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.part_offset);
-  const int64_t tiles = ((g.N + 31) / 32) * ((g.K + 31) / 32);
+  const float *b_hi, *b_lo;
   const int64_t cap = (int64_t)device_sm_count() * 8;
-  k_prep_b<<<(unsigned)(tiles < cap ? tiles : cap), dim3(32, 8), 0, s>>>(g.mat2, g.K, g.N, bt_hi,
-                                                                         bt_lo);
-  note_launch();
+  if (g.b_kmajor) {  // w[N,K] is B_hi; 3xTF32 adds w_lo in the scratch
+    b_hi = g.mat2;
+    b_lo = three_pass ? ws : nullptr;
+    if (three_pass) {
+      const int64_t total = g.N * g.K, blocks = (total + 255) / 256;
+      k_prep_blo<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(g.mat2, total, ws);
+      note_launch();
+    }
+  } else {  // transpose mat2[K,N] into Bt_hi[N,K] (+ Bt_lo)
+    b_hi = ws;
+    b_lo = three_pass ? ws + g.N * g.K : nullptr;
+    const int64_t tiles = ((g.N + 31) / 32) * ((g.K + 31) / 32);
+    k_prep_b<<<(unsigned)(tiles < cap ? tiles : cap), dim3(32, 8), 0, s>>>(
+        g.mat2, g.K, g.N, ws, three_pass ? ws + g.N * g.K : nullptr);
+    note_launch();
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return three_pass ? run<true>(g, p, bt_hi, bt_lo, part, s)
-                    : run<false>(g, p, bt_hi, nullptr, part, s);
+  return three_pass ? run<true>(g, p, b_hi, b_lo, part, s) : run<false>(g, p, b_hi, nullptr, part, s);
 }
 
 cudaError_t gemm_take_watchdog(int* value) {

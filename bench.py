@@ -272,6 +272,25 @@ def run_gpu(args):
     barrier(dist_mod, device)
     e2e_ms = max_over_ranks(sum(e_ms) / len(e_ms), dist_mod, device)
     e2e_value = whole_job_rate(flops_step, ws, e2e_ms)
+    # The pages' one published figure is the implicit-im2col GEMM's speed-up
+    # over their direct conv kernel; time the same ratio here (outside the
+    # timed region, after it).
+    direct = None
+    if rank == 0 and not args.no_direct_baseline:
+        d_ms = []
+        for _ in range(3):
+            flush.fill_(0.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            binding.conv2d(X, Wt, Bias, cc["stride"], cc["pad"], cc["dilation"], mode="direct",
+                           out=out_c)
+            e1.record(stream)
+            e1.synchronize()
+            d_ms.append(e0.elapsed_time(e1))
+        dm = statistics.median(d_ms)
+        direct = {"workload": "the step's conv2d", "direct_ms": round(dm, 4),
+                  "gemm_ms": round(sum(ms_conv) / len(ms_conv), 4),
+                  "speedup": round(dm / (sum(ms_conv) / len(ms_conv)), 2)}
     status = binding.check_device_error(None)
 
     if rank != 0:
@@ -313,6 +332,7 @@ def run_gpu(args):
                 "path": "pinned host -> device copies, addmm + conv2d through the C ABI, "
                         "device -> pinned host copies, one stream"},
         "gpu_launches": launches,
+        "conv_gemm_vs_direct": direct,
         "clocks": clocks,
         "watchdog": status,
     }
@@ -428,6 +448,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["imc", "reference"], default="imc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-direct-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=1.0)
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # the timing rules want at least 3 warm-up steps

@@ -55,6 +55,13 @@ extern "C" {
 #define IMC_MODE_FORCE_TC3 3 /* force the tcgen05 3xTF32 kernel (IMC_ERR_SHAPE if the
                                 shape cannot take it); for tests and measurement    */
 #define IMC_MODE_FORCE_TC1 4 /* force the tcgen05 1xTF32 kernel, likewise          */
+#define IMC_MODE_DIRECT 5    /* conv2d only: the direct kernel (one thread per output
+                                element, no operand reuse) -- the pre-GEMM design the
+                                conv page replaces, kept as a measured baseline       */
+/* Flag OR-ed into any mode: apply max(v, 0) to every output element in the
+ * fused epilogue (the ReLU of a Linear / Conv + ReLU block, ExecuTorch WebGPU
+ * "Add relu op" pull request referenced from the addmm page). */
+#define IMC_ACT_RELU 0x100
 
 /* ---------------------------------------- kernel ids (imc_last_kernel()) */
 #define IMC_KERNEL_NONE 0 /* nothing launched (empty problem)              */
@@ -62,6 +69,7 @@ extern "C" {
 #define IMC_KERNEL_TC1 2  /* tcgen05 1xTF32 kernel                         */
 #define IMC_KERNEL_SIMT 3 /* fp32 FFMA SIMT kernel                         */
 #define IMC_KERNEL_FILL 4 /* epilogue only: K == 0 or alpha == 0           */
+#define IMC_KERNEL_DIRECT 5 /* direct conv2d kernel (IMC_MODE_DIRECT)      */
 
 /*
  * gemm_addmm_f32 -- aten.addmm semantics.
@@ -98,8 +106,9 @@ int gemm_addmm_f32(const float* self, int self_2d, const float* mat1, const floa
                    float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
                    void* stream);
 
-/* gemm_addmm_f32 with an explicit mode (IMC_MODE_*); mode IMC_MODE_DEFAULT
- * is exactly gemm_addmm_f32.  Any other mode value is IMC_ERR_ARG. */
+/* gemm_addmm_f32 with an explicit mode (IMC_MODE_* other than
+ * IMC_MODE_DIRECT, optionally | IMC_ACT_RELU); mode IMC_MODE_DEFAULT is
+ * exactly gemm_addmm_f32.  Any other mode value is IMC_ERR_ARG. */
 int gemm_addmm_f32_ex(const float* self, int self_2d, const float* mat1, const float* mat2,
                       float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
                       int mode, void* stream);
@@ -154,7 +163,8 @@ int conv2d_gemm_f32(const float* x, const float* w, const float* bias, float* ou
                     int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
                     int64_t stride, int64_t pad, int64_t dilation, void* stream);
 
-/* conv2d_gemm_f32 with an explicit mode (IMC_MODE_*). */
+/* conv2d_gemm_f32 with an explicit mode (IMC_MODE_*, optionally
+ * | IMC_ACT_RELU). */
 int conv2d_gemm_f32_ex(const float* x, const float* w, const float* bias, float* out, int64_t B,
                        int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
                        int64_t stride, int64_t pad, int64_t dilation, int mode, void* stream);
@@ -214,6 +224,33 @@ int conv2d_gemm_f32_ws(const float* x, const float* w, const float* bias, float*
                        int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
                        int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW,
                        int mode, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * linear_f32 -- aten.linear: out[M,N] = x[M,K] @ w[N,K]^T (+ bias[N]).
+ *
+ * Source: the same tiled GEMM as addmm with the B operand read from the
+ * transposed [N, K] weight -- ExecuTorch WebGPU "Add optimized addmm op",
+ * Implementation paragraph (addmm re-derives its B read for mat2's [K,N]
+ * layout, "unlike linear's transposed [N,K] weight"), and the conv page's
+ * Implementation paragraph (conv2d_gemm forks linear_fp32_tiled).
+ *
+ *   out[m,n] = bias[n] + sum_k x[m*K + k] * w[n*K + k]     (bias may be NULL)
+ *
+ * x [M,K], w [N,K], bias [N] or NULL, out [M,N]: contiguous row-major fp32
+ * device pointers; out may not overlap x, w or bias.  M, N, K in [0, 2^31).
+ * mode: IMC_MODE_* (not IMC_MODE_DIRECT), optionally | IMC_ACT_RELU.  The
+ * weight is already K-major, so the tensor-core path needs scratch only for
+ * its TF32 lo part (N*K*4 bytes, 3xTF32) and any split-K partial sums;
+ * linear_f32 takes it from the stream-ordered pool, linear_f32_ws from the
+ * caller (rules as gemm_addmm_f32_ws).  Tensor-core path: K % 4 == 0 and
+ * 16-byte aligned x and w; otherwise SIMT.
+ */
+int linear_f32(const float* x, const float* w, const float* bias, float* out, int64_t M,
+               int64_t N, int64_t K, int mode, void* stream);
+size_t linear_f32_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode);
+int linear_f32_ws(const float* x, const float* w, const float* bias, float* out, int64_t M,
+                  int64_t N, int64_t K, int mode, void* workspace, size_t workspace_bytes,
+                  void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* imc_status_string(int status);

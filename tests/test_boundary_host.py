@@ -96,6 +96,9 @@ def test_addmm_argument_errors(lib):
     assert g(self_2d=2) == binding.IMC_ERR_ARG
     assert g(mode=7) == binding.IMC_ERR_ARG
     assert g(mode=-1) == binding.IMC_ERR_ARG
+    assert g(mode=5) == binding.IMC_ERR_ARG             # the direct kernel is conv-only
+    assert g(mode=0x200) == binding.IMC_ERR_ARG         # unknown flag bit
+    assert g(mode=0x100 | 7) == binding.IMC_ERR_ARG     # ReLU flag on a bad mode
     assert g(alpha=float("nan")) == binding.IMC_ERR_ARG
     assert g(beta=float("inf")) == binding.IMC_ERR_ARG
     assert g(M=-1) == binding.IMC_ERR_SHAPE
@@ -197,7 +200,7 @@ def test_conv_argument_errors(lib):
     # the symmetric entry point maps onto the per-axis one
     assert binding.conv2d_gemm_f32(P1, P2, P3, P4, 2, 3, 8, 8, 4, 3, 3, 0, 1, 1,
                                    None) == binding.IMC_ERR_SHAPE
-    assert binding.conv2d_gemm_f32_ex(P1, P2, P3, P4, 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 5,
+    assert binding.conv2d_gemm_f32_ex(P1, P2, P3, P4, 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 6,
                                       None) == binding.IMC_ERR_ARG
 
 
@@ -224,6 +227,27 @@ def test_conv_workspace_argument_errors(lib):
     assert f(*args, P2 + 64, need, None) == binding.IMC_ERR_ALIAS  # overlaps w
     assert without_gpu([["conv2d_gemm_f32_ws", list(args) + [W, need, None]]]) == [
         binding.IMC_ERR_DEVICE]
+
+
+def test_mode_flags_and_linear_validation(lib):
+    # ReLU flag and the conv-only direct mode pass validation (then need a device)
+    relu = gargs(mode=binding.ACT_RELU | 3)
+    direct = ["conv2d_gemm_f32_nd", [P1, P2, P3, P4, 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 1,
+                                     5 | binding.ACT_RELU, None]]
+    lin = ["linear_f32", [P1, P2, P3, P4, 8, 8, 8, 0, None]]
+    lin_nobias = ["linear_f32", [P1, P2, None, P4, 8, 8, 8, 1, None]]
+    assert without_gpu([relu, direct, lin, lin_nobias]) == [binding.IMC_ERR_DEVICE] * 4
+    L = binding.linear_f32
+    assert L(P1, P2, P3, None, 8, 8, 8, 0, None) == binding.IMC_ERR_NULL
+    assert L(None, P2, P3, P4, 8, 8, 8, 0, None) == binding.IMC_ERR_NULL
+    assert L(P1, P2, P3, P1, 8, 8, 8, 0, None) == binding.IMC_ERR_ALIAS
+    assert L(P1, P2, P3, P4, -1, 8, 8, 0, None) == binding.IMC_ERR_SHAPE
+    assert L(P1, P2, P3, P4, 8, 8, 8, 5, None) == binding.IMC_ERR_ARG
+    assert L(P1, P2, P3, P4, 0, 8, 8, 0, None) == binding.IMC_OK
+    q = binding.linear_f32_workspace_bytes
+    assert q(1024, 3072, 768, 0) == 3072 * 768 * 4  # only the weight's lo part
+    assert q(1024, 3072, 768, 1) == 0               # 1xTF32 reads the weight as it is
+    assert q(64, 80, 96, 0) == 0
 
 
 def test_no_gpu_fails_loudly(lib):
