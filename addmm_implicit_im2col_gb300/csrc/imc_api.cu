@@ -296,14 +296,51 @@ int conv_shape(int64_t B, int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t 
   return IMC_OK;
 }
 
-int plan_conv(int64_t M, int64_t N, int64_t K, int mode) {
+// Which kernel a well-formed conv takes.  `tc_ok`: the tcgen05 kernel takes
+// the sizes (tc_conv_shape_ok); forced tensor-core modes fail otherwise.
+int plan_conv(int64_t M, int64_t N, int64_t K, int mode, bool tc_ok) {
   if (M == 0 || N == 0) return IMC_KERNEL_NONE;
   if (K == 0) return IMC_KERNEL_FILL;
   if (mode == IMC_MODE_DIRECT) return IMC_KERNEL_DIRECT;
-  if (mode == IMC_MODE_FORCE_TC3) return IMC_KERNEL_TC3;
-  if (mode == IMC_MODE_FORCE_TC1) return IMC_KERNEL_TC1;
-  if (mode == IMC_MODE_SIMT || (double)M * N * K < (double)kTinyMacs) return IMC_KERNEL_SIMT;
+  if (mode == IMC_MODE_FORCE_TC3 || mode == IMC_MODE_FORCE_TC1)
+    return tc_ok ? (mode == IMC_MODE_FORCE_TC3 ? IMC_KERNEL_TC3 : IMC_KERNEL_TC1) : -1;
+  if (mode == IMC_MODE_SIMT || !tc_ok || (double)M * N * K < (double)kTinyMacs)
+    return IMC_KERNEL_SIMT;
   return mode == IMC_MODE_DEFAULT ? IMC_KERNEL_TC3 : IMC_KERNEL_TC1;
+}
+
+// The validated problem as kernel arguments (pointers may be null for a
+// size query).
+ConvArgs conv_args(const float* x, const float* w, const float* bias, float* out, int64_t B,
+                   int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
+                   int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW,
+                   const ConvShape& cs, int relu) {
+  ConvArgs c;
+  c.x = x;
+  c.w = w;
+  c.bias = bias;
+  c.out = out;
+  c.B = (int)B;
+  c.IC = (int)IC;
+  c.H = (int)H;
+  c.W = (int)W;
+  c.OC = (int)OC;
+  c.KH = (int)KH;
+  c.KW = (int)KW;
+  c.sH = (int)sH;
+  c.sW = (int)sW;
+  c.pH = (int)pH;
+  c.pW = (int)pW;
+  c.dH = (int)dH;
+  c.dW = (int)dW;
+  c.OH = (int)cs.OH;
+  c.OW = (int)cs.OW;
+  c.M = OC;
+  c.N = B * cs.OH * cs.OW;
+  c.K = cs.K;
+  c.vec_out = ((cs.OH * cs.OW) % 4 == 0) && aligned16(out) ? 1 : 0;
+  c.relu = relu;
+  return c;
 }
 
 int conv_impl(const float* x, const float* w, const float* bias, float* out, int64_t B,
@@ -327,11 +364,18 @@ int conv_impl(const float* x, const float* w, const float* bias, float* out, int
   if ((K > 0 && (overlaps(out, out_bytes, x, x_bytes) || overlaps(out, out_bytes, w, w_bytes))) ||
       overlaps(out, out_bytes, bias, (uint64_t)OC * 4u))
     return IMC_ERR_ALIAS;
-  const int kernel = plan_conv(OC, B * OH * OW, K, mode);
+  const ConvArgs c = conv_args(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW,
+                               cs, relu);
+  const int kernel = plan_conv(OC, B * OH * OW, K, mode, tc_conv_shape_ok(c));
+  if (kernel < 0) return IMC_ERR_SHAPE;
   const bool tc = kernel == IMC_KERNEL_TC3 || kernel == IMC_KERNEL_TC1;
-  const size_t need = tc ? tc_conv_workspace_bytes(OC, K, kernel == IMC_KERNEL_TC3) : 0;
-  if (caller_ws && need > 0) {
-    if (!workspace || ws_bytes < need || !aligned16(workspace)) return IMC_ERR_ARG;
+  const bool three = kernel == IMC_KERNEL_TC3;
+  // minimum (no K-slices) and the scratch the call will use
+  const size_t need_min = tc ? tc_conv_workspace_bytes(c, three, 0) : 0;
+  const size_t need =
+      tc ? tc_conv_workspace_bytes(c, three, caller_ws ? ws_bytes : SIZE_MAX) : 0;
+  if (caller_ws && need_min > 0) {
+    if (!workspace || ws_bytes < need_min || !aligned16(workspace)) return IMC_ERR_ARG;
     if (overlaps(workspace, need, out, out_bytes) || overlaps(workspace, need, x, x_bytes) ||
         overlaps(workspace, need, w, w_bytes) ||
         overlaps(workspace, need, bias, (uint64_t)OC * 4u))
@@ -339,43 +383,17 @@ int conv_impl(const float* x, const float* w, const float* bias, float* out, int
   }
   const int dev = check_device();
   if (dev != IMC_OK) return dev;
-
-  ConvArgs c;
-  c.x = x;
-  c.w = w;
-  c.bias = bias;
-  c.out = out;
-  c.B = (int)B;
-  c.IC = (int)IC;
-  c.H = (int)H;
-  c.W = (int)W;
-  c.OC = (int)OC;
-  c.KH = (int)KH;
-  c.KW = (int)KW;
-  c.sH = (int)sH;
-  c.sW = (int)sW;
-  c.pH = (int)pH;
-  c.pW = (int)pW;
-  c.dH = (int)dH;
-  c.dW = (int)dW;
-  c.OH = (int)OH;
-  c.OW = (int)OW;
-  c.M = OC;
-  c.N = B * OH * OW;
-  c.K = K;
-  c.vec_out = ((OH * OW) % 4 == 0) && aligned16(out) ? 1 : 0;
-  c.relu = relu;
   cudaStream_t s = (cudaStream_t)stream;
 
   if (kernel == IMC_KERNEL_FILL) return finish(launch_fill_conv(c, s), kernel);
   if (kernel == IMC_KERNEL_DIRECT) return finish(launch_direct_conv(c, s), kernel);
   if (kernel == IMC_KERNEL_SIMT) return finish(launch_simt_conv(c, s), kernel);
-  if (!tc_conv_supported(c)) return IMC_ERR_DEVICE;
+  if (!tc_conv_supported(c)) return IMC_ERR_DEVICE;  // driver without tensor-map support
   void* ws = workspace;
   if (!caller_ws) {
     if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return IMC_ERR_CUDA;
   }
-  const cudaError_t e = launch_tc_conv(c, kernel == IMC_KERNEL_TC3, ws, s);
+  const cudaError_t e = launch_tc_conv(c, three, ws, need, s);
   if (!caller_ws) {
     const cudaError_t f = cudaFreeAsync(ws, s);
     if (e == cudaSuccess && f != cudaSuccess) return IMC_ERR_CUDA;
@@ -411,9 +429,11 @@ size_t conv2d_gemm_f32_workspace_bytes(int64_t B, int64_t IC, int64_t H, int64_t
   if (!parse_mode(mode_arg, true, &mode, &relu)) return 0;
   ConvShape cs;
   if (conv_shape(B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, &cs) != IMC_OK) return 0;
-  const int kernel = plan_conv(OC, B * cs.OH * cs.OW, cs.K, mode);
-  if (kernel == IMC_KERNEL_TC3) return tc_conv_workspace_bytes(OC, cs.K, true);
-  if (kernel == IMC_KERNEL_TC1) return tc_conv_workspace_bytes(OC, cs.K, false);
+  const ConvArgs c = conv_args(nullptr, nullptr, nullptr, nullptr, B, IC, H, W, OC, KH, KW, sH,
+                               sW, pH, pW, dH, dW, cs, relu);
+  const int kernel = plan_conv(OC, B * cs.OH * cs.OW, cs.K, mode, tc_conv_shape_ok(c));
+  if (kernel == IMC_KERNEL_TC3) return tc_conv_workspace_bytes(c, true, SIZE_MAX);
+  if (kernel == IMC_KERNEL_TC1) return tc_conv_workspace_bytes(c, false, SIZE_MAX);
   return 0;
 }
 

@@ -64,11 +64,17 @@ size_t tc_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool three_pass,
                                size_t limit);
 cudaError_t launch_tc_gemm(const GemmArgs& a, bool three_pass, void* workspace,
                            size_t workspace_bytes, cudaStream_t s);
-// The conv kernel needs tc_conv_workspace_bytes() for the padded hi / lo
-// weight planes.
+// The conv kernel needs a 16-byte aligned workspace for the padded hi / lo
+// weight planes and, when the last wave of tiles is cut into K-slices, their
+// partial sums; tc_conv_workspace_bytes(.., limit) follows the same rule as
+// the addmm one (SIZE_MAX: preferred size, 0: minimum, no slices).
+// tc_conv_shape_ok: the sizes the kernel's 32-bit indexing and tap table
+// take (pointers may be null); tc_conv_supported adds the driver check.
+bool tc_conv_shape_ok(const ConvArgs& a);
 bool tc_conv_supported(const ConvArgs& a);
-size_t tc_conv_workspace_bytes(int64_t OC, int64_t K, bool three_pass);
-cudaError_t launch_tc_conv(const ConvArgs& a, bool three_pass, void* workspace, cudaStream_t s);
+size_t tc_conv_workspace_bytes(const ConvArgs& a, bool three_pass, size_t limit);
+cudaError_t launch_tc_conv(const ConvArgs& a, bool three_pass, void* workspace,
+                           size_t workspace_bytes, cudaStream_t s);
 
 // Read and clear the watchdog word of the addmm / conv tensor-core kernels on
 // the current device (the caller synchronises first).

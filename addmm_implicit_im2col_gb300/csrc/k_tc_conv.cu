@@ -2,28 +2,48 @@
 //
 // Semantics: ExecuTorch WebGPU "et_vk conv2d: route standard (groups==1) conv
 // through an im2col tiled GEMM", Solution and Implementation paragraphs:
-// M = OC, N = B*OH*OW, K = IC*KH*KW; the weight is the [OC, K] operand; the
-// input is im2col-sampled on the fly (n -> (b, oh, ow), kk -> (ic, kh, kw),
+// GEMM M = OC, N = B*OH*OW, K = IC*KH*KW; the weight is the [OC, K] operand;
+// the input is im2col-sampled on the fly (n -> (b, oh, ow), kk -> (ic, kh, kw),
 // ih = oh*sH - pH + kh*dH, likewise iw, out-of-range taps read 0); bias per
 // output channel; NCHW output.
 //
-// Layout for sm_103a:
-//   pre-pass    the weight is written once per call as zero-padded rows of Kp
-//               (K rounded up to 4) fp32 -- hi part and, for 3xTF32, lo part --
-//               so that its tiles can be TMA-loaded whatever K is
-//   warp 8      TMA producer of the weight tiles (MH x 128 rows x 16, 64B swizzle)
-//   warps 0-7   im2col producers: thread t owns column n = n0 + t of the tile;
-//               per k-block of 16 it gathers its 16 taps (loads for the next
-//               k-block are issued before the current one is stored), splits
-//               them into TF32 hi / lo and writes them as one K-major row of
-//               the B tiles
-//   warp 9      TMEM owner + MMA issuer: MH 128-row halves share every B tile;
-//               3 MMAs per k-step (A_lo*B_hi + A_hi*B_lo + A_hi*B_hi) or 1
-//   warps 10-13 epilogue: tcgen05.ld, 32x32 transpose through shared memory,
-//               acc + bias[oc] to NCHW rows
-// One persistent CTA per SM; the tile width BN (multiple of 16, up to
-// BN_MAX) is chosen per problem so the tiles fill the SMs in few waves.
+// Layout for sm_103a.  The kernel forms the transposed product
+// D[p, oc] = sum_k im2col[p, k] * w[oc, k], so that the operand built on the
+// fly is the MMA's A operand and lives in tensor memory (the tensor core then
+// reads only the weight tile from shared memory, and the gather never writes
+// shared memory):
+//   tile        128 output positions p (TMEM lanes) x BN output channels
+//               (BN a multiple of 16, at most 256)
+//   K order     with IC >= 8, k runs over (kh, kw, ic) inside the kernel --
+//               input channel fastest -- instead of the pages' (ic, kh, kw):
+//               a sum does not depend on the order of its terms up to
+//               rounding, and this way the 8 k a thread gathers per k-block
+//               usually share one spatial tap (one bounds check, then reads
+//               at a fixed channel-plane stride).  Few channels keep the pages'
+//               order, where consecutive k reuse the same input rows.
+//   pre-pass    the weight is written once per call, in the kernel's K order,
+//               as zero-padded rows of Kp (K rounded up to 4) fp32 -- hi part
+//               and, for 3xTF32, lo part -- so that its tiles can be
+//               TMA-loaded whatever K is
+//   warps 0-7   im2col gather: warp w fills TMEM lanes 32*(w%4) .. +31 (32
+//               positions) with k = 8*(w/4) .. +7 of every k-block of 16; the
+//               values of the next two k-blocks are in flight while one is
+//               split into TF32 hi / lo and written to its stage (tcgen05.st)
+//   warp 8      TMA producer of the weight tiles (BN x 16 fp32, 64B swizzle)
+//   warp 9      TMEM owner + MMA issuer, A from TMEM and B from shared memory:
+//               A_lo*B_hi + A_hi*B_lo + A_hi*B_hi per k-step of 8, or A*B
+//   warps 10-13 epilogue: tcgen05.ld (one position per lane), transposed
+//               through shared memory, + bias, written to NCHW as 512-byte
+//               runs of positions per channel
+// TMEM columns 0-255 hold the accumulator (two of 128 when BN <= 128, so the
+// epilogue of one tile overlaps the next), columns 256-511 the A stages (32
+// columns each: hi 0-15, lo 16-31).
+// Scheduling: persistent CTAs take whole tiles first.  When the last wave
+// would leave SMs idle, its tiles are cut into S K-slices; a slice writes its
+// partial sums to scratch and k_conv_tail adds them in slice order (the result
+// does not depend on which CTA ran which slice).
 // Every barrier wait is bounded (see tc_common.cuh).
+#include <algorithm>
 #include <mutex>
 
 #include "imc.h"
@@ -37,37 +57,71 @@ using namespace tc;
 
 constexpr int BK = 16;           // fp32 per k-block: one 64-byte swizzle row
 constexpr int KSTEPS = BK / UK;  // 2
-constexpr int HALF_BYTES = BM * BK * 4;  // one 128-row A tile: 8 KB
-constexpr int PRODUCERS = 256;           // im2col producer threads (warps 0-7)
-constexpr int TMA_WARP = 8, MMA_WARP = 9, EPI_WARP0 = 10, THREADS = 14 * 32;
+constexpr int BN_MAX = 256;
+constexpr int GATHER_WARPS = 8;
+constexpr int TMA_WARP = 8, MMA_WARP = 9, THREADS = 14 * 32;
+constexpr uint32_t A_COL0 = 256, A_STAGE_COLS = 32;
+constexpr int MAX_TAPS = 1024;  // KH*KW entries of the per-CTA tap table
+constexpr int EPI_STAGE_BYTES = 32 * BM * 4;  // one 32-channel chunk of a tile
+constexpr int SMEM_LIMIT = 232448;
+constexpr int kPlanSMs = 152;            // SM count the K-slice plan is made for
+constexpr double kSliceLaunchKb = 8.0;   // fix-up launch, in k-block times
+constexpr double kHbmBytesPerClkSm = 24.0;  // one SM's share of HBM bandwidth
 
 __device__ int g_watchdog_conv;
 
-template <int MH, bool THREE>
-struct Cfg {
-  static constexpr int BN_MAX = MH == 2 ? 192 : 256;
-  static constexpr int B_BYTES = BN_MAX * BK * 4;
-  static constexpr int A_HI = 0;
-  static constexpr int A_LO = MH * HALF_BYTES;
-  static constexpr int B_HI = (THREE ? 2 : 1) * MH * HALF_BYTES;
-  static constexpr int B_LO = B_HI + B_BYTES;
-  static constexpr int STAGE = B_HI + (THREE ? 2 : 1) * B_BYTES;
-  static constexpr int STAGES = (196608 / STAGE) < MAX_STAGES ? (196608 / STAGE) : MAX_STAGES;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + EPI_BYTES + (int)sizeof(Ctl);
-  static constexpr int NBUF = MH == 2 ? 1 : 2;  // accumulator buffers in TMEM
-  static_assert(STAGES >= 3, "pipeline depth");
-  static_assert(SMEM <= 232448, "shared memory");
+// Work split and shared-memory layout, the same for every CTA of a launch.
+struct Sched {
+  int bn, n_oc, kb;         // channel-tile width, channel tiles, k-blocks of a whole tile
+  int full, slices, units;  // whole-tile units, K-slices per tail tile, all units
+  int stages, nacc;         // pipeline stages, accumulator buffers
+  int w_bytes;              // weight tiles of a stage (hi [+ lo])
+  int tab_bytes;            // tap table
+  float* part;              // tail partial sums [units - full][bn][128]
 };
 
+struct Unit {
+  int pt, ot;    // position tile, channel tile
+  int kb0, kb1;  // k-block range
+  int slot;      // partial-sum slot, -1 for a whole tile
+};
+
+__device__ __forceinline__ Unit decode(const Sched& q, int u) {
+  Unit r;
+  int t;
+  if (u < q.full) {
+    t = u;
+    r.kb0 = 0;
+    r.kb1 = q.kb;
+    r.slot = -1;
+  } else {
+    const int v = u - q.full, tt = v / q.slices, sl = v - tt * q.slices;
+    t = q.full + tt;
+    r.kb0 = (int)((int64_t)sl * q.kb / q.slices);
+    r.kb1 = (int)((int64_t)(sl + 1) * q.kb / q.slices);
+    r.slot = v;
+  }
+  r.pt = t / q.n_oc;
+  r.ot = t - r.pt * q.n_oc;
+  return r;
+}
+
 // ------------------------------------------------------- weight pre-pass
-// w_hi[oc*Kp + k] = tf32 part of w[oc*K + k] (0 for k >= K), w_lo the rest.
-__global__ void k_prep_w(const float* __restrict__ w, int64_t OC, int64_t K, int64_t Kp,
-                         float* __restrict__ w_hi, float* __restrict__ w_lo) {
+// Column k of row oc takes w[oc, ic, kh, kw]: k = ic*taps + tap (the pages'
+// order) or, with icf, k = tap*IC + ic (tap = kh*KW + kw).  w_hi gets its TF32
+// part (0 for k >= K), w_lo the rest.
+__global__ void k_prep_w(const float* __restrict__ w, int64_t OC, int64_t K, int64_t Kp, int IC,
+                         int taps, int icf, float* __restrict__ w_hi, float* __restrict__ w_lo) {
   const int64_t total = OC * Kp;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t oc = e / Kp, k = e - oc * Kp;
-    const float v = k < K ? __ldg(w + oc * K + k) : 0.0f;
+    int64_t src = k;
+    if (icf) {
+      const int64_t tap = k / IC;
+      src = (k - tap * IC) * taps + tap;
+    }
+    const float v = k < K ? __ldg(w + oc * K + src) : 0.0f;
     if (w_lo) {
       w_hi[e] = tf32_hi(v);
       w_lo[e] = tf32_lo(v);
@@ -77,82 +131,66 @@ __global__ void k_prep_w(const float* __restrict__ w, int64_t OC, int64_t K, int
   }
 }
 
-struct Store {
-  const ConvArgs& c;
-  int64_t m0, n0;
-  int bn;
-  __device__ __forceinline__ float4 load(int r, int) const {
-    const int64_t m = m0 + r;
-    const float bv = (c.bias && m < c.M) ? __ldg(c.bias + m) : 0.0f;
-    return make_float4(bv, bv, bv, bv);
+// Three register buffers of gathered values, rotated by unrolling (copying a
+// buffer whose loads are in flight would wait for them): the values of k-blocks
+// i+1 and i+2 are in flight while k-block i is stored.
+template <class Gather, class Store>
+__device__ __forceinline__ bool rotate3(int nkb, Gather& gather, Store& store) {
+  float va[8], vb[8], vc[8];
+  gather(va);
+  if (nkb > 1) gather(vb);
+  for (int i = 0; i < nkb; i += 3) {
+    if (i + 2 < nkb) gather(vc);
+    if (!store(va)) return false;
+    if (i + 1 >= nkb) break;
+    if (i + 3 < nkb) gather(va);
+    if (!store(vb)) return false;
+    if (i + 2 >= nkb) break;
+    if (i + 4 < nkb) gather(vb);
+    if (!store(vc)) return false;
   }
-  __device__ __forceinline__ void operator()(int r, int col, float4 v, float4 b4) const {
-    const int64_t m = m0 + r, n = n0 + col;
-    if (col >= bn || m >= c.M || n >= c.N) return;
-    const float bv = b4.x;
-    const int64_t P = (int64_t)c.OH * c.OW;
-    float4 o4 = make_float4(v.x + bv, v.y + bv, v.z + bv, v.w + bv);
-    if (c.relu) o4 = make_float4(fmaxf(o4.x, 0.f), fmaxf(o4.y, 0.f), fmaxf(o4.z, 0.f), fmaxf(o4.w, 0.f));
-    if (c.vec_out && col + 3 < bn) {  // P % 4 == 0: n .. n+3 lie in one image
-      const int64_t b = n / P, p = n - b * P;
-      *reinterpret_cast<float4*>(c.out + (b * c.OC + m) * P + p) = o4;
-    } else {
-      const float vv[4] = {o4.x, o4.y, o4.z, o4.w};
-      for (int j = 0; j < 4 && n + j < c.N && col + j < bn; ++j) {
-        const int64_t nn = n + j, b = nn / P, p = nn - b * P;
-        c.out[(b * c.OC + m) * P + p] = vv[j];
-      }
-    }
-  }
-};
-
-// One im2col column (output position n) and the running tap (ic, kh, kw)
-// of kk = k0, kept across k-blocks so no division is needed per k-block.
-struct Column {
-  const float* xb;  // image b of x
-  int ih0, iw0;     // oh*sH - pH, ow*sW - pW
-  bool ok;
-};
-struct Tap {
-  int ic, kh, kw;
-};
-
-// The 16 taps kk = k0 .. k0+15 of one column (zero outside the image and for
-// kk >= K); advances `tap` by 16.
-__device__ __forceinline__ void gather(const ConvArgs& c, const Column& col, int k0, int K,
-                                       Tap& tap, float (&v)[BK]) {
-#pragma unroll
-  for (int j = 0; j < BK; ++j) {
-    const int ih = col.ih0 + tap.kh * c.dH, iw = col.iw0 + tap.kw * c.dW;
-    const bool in = col.ok && (k0 + j < K) && (unsigned)ih < (unsigned)c.H &&
-                    (unsigned)iw < (unsigned)c.W;
-    v[j] = in ? __ldg(col.xb + ((tap.ic * c.H + ih) * c.W + iw)) : 0.0f;
-    if (++tap.kw == c.KW) {
-      tap.kw = 0;
-      if (++tap.kh == c.KH) {
-        tap.kh = 0;
-        ++tap.ic;
-      }
-    }
-  }
+  return true;
 }
 
-template <int MH, bool THREE>
+// Named barrier 1 over the four epilogue warps; epi_any also ORs a flag
+// across them (so that they leave their loop together).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+// ------------------------------------------------------------ main kernel
+template <bool THREE, bool ICF>
 __global__ void __launch_bounds__(THREADS, 1)
     k_tc_conv(const __grid_constant__ CUtensorMap tmWh, const __grid_constant__ CUtensorMap tmWl,
-              const ConvArgs c, const int num_m, const int num_n, const int bn) {
-  using C = Cfg<MH, THREE>;
+              const ConvArgs c, const Sched q) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  float* epi = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE);
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::STAGES * C::STAGE + EPI_BYTES);
+  const int b_tile = q.bn * BK * 4;  // one weight tile (hi or lo)
+  // [weight stages][tap table][epilogue staging][barriers]
+  int2* tab = reinterpret_cast<int2*>(smem + q.stages * q.w_bytes);
+  float* epi_stage = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tab) + q.tab_bytes);
+  Ctl* ctl = reinterpret_cast<Ctl*>(reinterpret_cast<uint8_t*>(epi_stage) + EPI_STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_tiles = num_m * num_n;
-  const int K = (int)c.K;
-  const int num_kb = (K + BK - 1) / BK;
+  const int taps = c.KH * c.KW;
   int* wd = &g_watchdog_conv;
 
-  if (threadIdx.x == 0) init_barriers(ctl, C::STAGES, PRODUCERS + 1, 1);
+  // tap table: r = kh*KW + kw -> (kh*dH, kw*dW)
+  for (int r = threadIdx.x; r < taps; r += blockDim.x) {
+    const int kh = r / c.KW, kw = r - kh * c.KW;
+    tab[r] = make_int2(kh * c.dH, kw * c.dW);
+  }
+  // full: the 8 gather warps + the weight TMA
+  if (threadIdx.x == 0) init_barriers(ctl, q.stages, GATHER_WARPS + 1, 1);
   if (warp == TMA_WARP && lane == 0) {
     ptx::tma_prefetch_desc(&tmWh);
     if (THREE) ptx::tma_prefetch_desc(&tmWl);
@@ -167,135 +205,189 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort = &ctl->abort;
 
-  if (warp < 8) {
-    // ----------------------------------------------------- im2col producers
-    const int pt = threadIdx.x;
-    const int P = c.OH * c.OW;
+  if (warp < GATHER_WARPS) {
+    // ------------------------------------------------------ im2col gather
+    const int quarter = warp & 3, half = warp >> 2;
+    const int HW = c.H * c.W, ICHW = c.IC * HW, P = c.OH * c.OW;
+    const uint32_t trow =
+        tmem + ((uint32_t)(quarter * 32) << 16) + A_COL0 + (uint32_t)(half * 8);
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      const int nt = t / num_m;  // tiles of one column block are adjacent
-      const int64_t n = (int64_t)nt * bn + pt;
-      Column col{c.x, 0, 0, pt < bn && n < c.N};
-      if (col.ok) {
-        const int b = (int)(n / P), p = (int)(n - (int64_t)b * P);
-        const int oh = p / c.OW, ow = p - oh * c.OW;
-        col.ih0 = oh * c.sH - c.pH;
-        col.iw0 = ow * c.sW - c.pW;
-        col.xb = c.x + (int64_t)b * c.IC * c.H * c.W;
-      }
-      // Three register buffers, rotated by unrolling (copying a buffer whose
-      // loads are in flight would wait for them): the taps of k-blocks kb+1
-      // and kb+2 are in flight while k-block kb is stored.
-      Tap tap{0, 0, 0};
-      auto next = [&](int kb, float (&v)[BK]) { gather(c, col, kb * BK, K, tap, v); };
-      float va[BK], vb[BK], vc[BK];
-      auto store = [&](const float (&v)[BK]) -> bool {
-        if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) return false;
-        if (pt < bn) {
-          uint8_t* row = smem + s * C::STAGE + C::B_HI + sw64_row_base(pt);
+    // Splits the 8 values of a k-block into TF32 hi / lo and writes them to
+    // the stage's TMEM columns; then arrives on the stage's full barrier.
+    auto put = [&](const float (&v)[8]) {
+      const uint32_t ta = trow + (uint32_t)s * A_STAGE_COLS;
+      if (THREE) {
+        float hi[8], lo[8];
 #pragma unroll
-          for (int j = 0; j < BK / 4; ++j) {
-            const float4 q = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-            const int off = sw64_unit(pt, j);
-            if (THREE) {
-              *reinterpret_cast<float4*>(row + off) = tf32_hi4(q);
-              *reinterpret_cast<float4*>(row + (C::B_LO - C::B_HI) + off) = tf32_lo4(q);
-            } else {
-              *reinterpret_cast<float4*>(row + off) = q;
-            }
-          }
+        for (int j = 0; j < 8; ++j) {
+          hi[j] = tf32_hi(v[j]);
+          lo[j] = tf32_lo(v[j]);
         }
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(&ctl->full[s]);
-        if (++s == C::STAGES) {
-          s = 0;
-          ph ^= 1u;
-        }
+        ptx::tmem_st8(ta, hi);
+        ptx::tmem_st8(ta + 16, lo);
+      } else {
+        ptx::tmem_st8(ta, v);  // the tensor core reads it as TF32
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ctl->full[s]);
+      if (++s == q.stages) {
+        s = 0;
+        ph ^= 1u;
+      }
+    };
+    for (int u = blockIdx.x; u < q.units && ok; u += gridDim.x) {
+      const Unit un = decode(q, u);
+      const int64_t p = (int64_t)un.pt * BM + quarter * 32 + lane;
+      const bool pok = p < c.N;
+      int b = 0, ih0 = 0, iw0 = 0;
+      if (pok) {
+        b = (int)(p / P);
+        const int pix = (int)(p - (int64_t)b * P);
+        const int oh = pix / c.OW, ow = pix - oh * c.OW;
+        ih0 = oh * c.sH - c.pH;
+        iw0 = ow * c.sW - c.pW;
+      }
+      const float* xb = c.x + (int64_t)b * ICHW;
+      const int k0 = un.kb0 * BK + half * 8;
+      const int nkb = un.kb1 - un.kb0;
+      auto store = [&](const float (&v)[8]) -> bool {
+        if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) return false;
+        ptx::tc_fence_after();
+        put(v);
         return true;
       };
-      next(0, va);
-      if (num_kb > 1) next(1, vb);
-      for (int kb = 0; kb < num_kb && ok; kb += 3) {
-        if (kb + 2 < num_kb) next(kb + 2, vc);
-        if (!(ok = store(va)) || kb + 1 >= num_kb) break;
-        if (kb + 3 < num_kb) next(kb + 3, va);
-        if (!(ok = store(vb)) || kb + 2 >= num_kb) break;
-        if (kb + 4 < num_kb) next(kb + 4, vb);
-        ok = store(vc);
+      if constexpr (ICF) {
+        // running position of this warp's next k = tap*IC + ic: the tap's
+        // validity and in-plane offset, and the channel plane offset ic*H*W
+        int tap = k0 / c.IC, ic = k0 - tap * c.IC, ic_hw = ic * HW;
+        bool tap_in = false;
+        int tap_off = 0;
+        auto set_tap = [&]() {
+          tap_in = false;
+          if (pok && tap < taps) {
+            const int2 d = tab[tap];
+            const int ih = ih0 + d.x, iw = iw0 + d.y;
+            tap_in = (unsigned)ih < (unsigned)c.H && (unsigned)iw < (unsigned)c.W;
+            tap_off = ih * c.W + iw;
+          }
+        };
+        set_tap();
+        // The 8 values of one k-block (0 past K, outside the image, or past
+        // the last position), then skip the other half's 8.
+        auto gather = [&](float (&v)[8]) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            v[j] = tap_in ? __ldg(xb + (ic_hw + tap_off)) : 0.0f;
+            ic_hw += HW;
+            if (++ic == c.IC) {
+              ic = 0;
+              ic_hw = 0;
+              ++tap;
+              set_tap();
+            }
+          }
+          ic += 8;
+          ic_hw += 8 * HW;
+          if (ic >= c.IC) {
+            while (ic >= c.IC) {
+              ic -= c.IC;
+              ++tap;
+            }
+            ic_hw = ic * HW;
+            set_tap();
+          }
+        };
+        ok = rotate3(nkb, gather, store);
+      } else {
+        // running (ic, r) of this warp's next k = ic*taps + r
+        int ic_hw = (k0 / taps) * HW, r = k0 - (k0 / taps) * taps;
+        auto gather = [&](float (&v)[8]) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int2 d = tab[r];
+            const int ih = ih0 + d.x, iw = iw0 + d.y;
+            const bool in = pok && ic_hw < ICHW && (unsigned)ih < (unsigned)c.H &&
+                            (unsigned)iw < (unsigned)c.W;
+            v[j] = in ? __ldg(xb + (ic_hw + ih * c.W + iw)) : 0.0f;
+            if (++r == taps) {
+              r = 0;
+              ic_hw += HW;
+            }
+          }
+          r += 8;
+          while (r >= taps) {
+            r -= taps;
+            ic_hw += HW;
+          }
+        };
+        ok = rotate3(nkb, gather, store);
       }
     }
   } else if (warp == TMA_WARP) {
     // ------------------------------------------------ weight TMA producer
     if (lane == 0) {
-      const uint32_t tx = (uint32_t)((THREE ? 2 : 1) * MH * HALF_BYTES);
       int s = 0, issued = 0;
       uint32_t ph = 0;
-      for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
-        const int mt = t % num_m;
-        for (int kb = 0; kb < num_kb; ++kb) {
+      for (int u = blockIdx.x; u < q.units && !*abort; u += gridDim.x) {
+        const Unit un = decode(q, u);
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) break;
-          uint8_t* st = smem + s * C::STAGE;
-          ptx::mbar_arrive_expect_tx(&ctl->full[s], tx);
-#pragma unroll
-          for (int h = 0; h < MH; ++h) {
-            ptx::tma_load_2d(st + C::A_HI + h * HALF_BYTES, &tmWh, &ctl->full[s], kb * BK,
-                             mt * MH * BM + h * BM);
-            if (THREE)
-              ptx::tma_load_2d(st + C::A_LO + h * HALF_BYTES, &tmWl, &ctl->full[s], kb * BK,
-                               mt * MH * BM + h * BM);
-          }
+          uint8_t* st = smem + s * q.w_bytes;
+          ptx::mbar_arrive_expect_tx(&ctl->full[s], (uint32_t)q.w_bytes);
+          ptx::tma_load_2d(st, &tmWh, &ctl->full[s], kb * BK, un.ot * q.bn);
+          if (THREE) ptx::tma_load_2d(st + b_tile, &tmWl, &ctl->full[s], kb * BK, un.ot * q.bn);
           ++issued;
-          if (++s == C::STAGES) {
+          if (++s == q.stages) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
-      for (int j = (issued > C::STAGES ? issued - C::STAGES : 0); j < issued; ++j)
-        drain_wait(&ctl->full[j % C::STAGES], (uint32_t)((j / C::STAGES) & 1));
+      for (int j = (issued > q.stages ? issued - q.stages : 0); j < issued; ++j)
+        drain_wait(&ctl->full[j % q.stages], (uint32_t)((j / q.stages) & 1));
     }
   } else if (warp == MMA_WARP) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = ptx::idesc_tf32(BM, (uint32_t)bn, false, false);
-      int s = 0, tl = 0;
+      const uint32_t idesc = ptx::idesc_tf32(BM, (uint32_t)q.bn, false, false);
+      int s = 0, ul = 0;
       uint32_t ph = 0;
-      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tl) {
-        const int buf = tl % C::NBUF;
-        const uint32_t use = (uint32_t)(tl / C::NBUF);
+      for (int u = blockIdx.x; u < q.units; u += gridDim.x, ++ul) {
+        const Unit un = decode(q, u);
+        const int buf = ul % q.nacc;
+        const uint32_t use = (uint32_t)(ul / q.nacc);
         if (!wait_bar(&ctl->acce[buf], (use & 1u) ^ 1u, abort, kSiteMmaAccEmpty, wd)) break;
         ptx::tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)buf * 128u;
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!wait_bar(&ctl->full[s], ph, abort, kSiteMmaOperands, wd)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t st = ptx::smem_addr(smem + s * C::STAGE);
+          const uint32_t bst = ptx::smem_addr(smem + s * q.w_bytes);
+          const uint32_t a = tmem + A_COL0 + (uint32_t)s * A_STAGE_COLS;
 #pragma unroll
-          for (int h = 0; h < MH; ++h) {
-            const uint32_t d = tmem + (uint32_t)(buf + h) * 256u;
-#pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-              const uint64_t ah = sw64_desc(st + C::A_HI + h * HALF_BYTES, ks);
-              const uint64_t bh = sw64_desc(st + C::B_HI, ks);
-              const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-              if (THREE) {
-                const uint64_t al = sw64_desc(st + C::A_LO + h * HALF_BYTES, ks);
-                const uint64_t bl = sw64_desc(st + C::B_LO, ks);
-                ptx::mma_tf32(d, al, bh, idesc, acc);
-                ptx::mma_tf32(d, ah, bl, idesc, 1u);
-                ptx::mma_tf32(d, ah, bh, idesc, 1u);
-              } else {
-                ptx::mma_tf32(d, ah, bh, idesc, acc);
-              }
+          for (int ks = 0; ks < KSTEPS; ++ks) {
+            const uint32_t ah = a + (uint32_t)(ks * UK);
+            const uint64_t bh = sw64_desc(bst, ks);
+            const uint32_t acc = (kb > un.kb0 || ks > 0) ? 1u : 0u;
+            if (THREE) {
+              const uint64_t bl = sw64_desc(bst + (uint32_t)b_tile, ks);
+              ptx::mma_tf32_ts(d, ah + 16u, bh, idesc, acc);  // A_lo * B_hi
+              ptx::mma_tf32_ts(d, ah, bl, idesc, 1u);         // A_hi * B_lo
+              ptx::mma_tf32_ts(d, ah, bh, idesc, 1u);         // A_hi * B_hi
+            } else {
+              ptx::mma_tf32_ts(d, ah, bh, idesc, acc);
             }
           }
           ptx::mma_commit(&ctl->empty[s]);
-          if (++s == C::STAGES) {
+          if (++s == q.stages) {
             s = 0;
             ph ^= 1u;
           }
@@ -309,21 +401,79 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else {
     // ----------------------------------------------------------- epilogue
-    const int q = warp & 3;
-    float* stage = epi + (warp - EPI_WARP0) * 32 * EPI_PITCH;
-    int tl = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tl) {
-      const int buf = tl % C::NBUF;
-      const uint32_t use = (uint32_t)(tl / C::NBUF);
-      if (!warp_wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd)) break;
+    // Per 32-channel chunk: TMEM -> registers -> a [32 channels][128
+    // positions] staging block in shared memory; then warp q writes channels
+    // 8q .. 8q+7 of the chunk, each as one 512-byte run of positions (lane l
+    // stores positions 4l .. 4l+3 with one 16-byte store).  The accumulator is
+    // released as soon as its last chunk is in registers.
+    const int quarter = warp & 3;
+    const int64_t P = (int64_t)c.OH * c.OW;
+    int ul = 0;
+    for (int u = blockIdx.x; u < q.units; u += gridDim.x, ++ul) {
+      const Unit un = decode(q, u);
+      const int buf = ul % q.nacc;
+      const uint32_t use = (uint32_t)(ul / q.nacc);
+      const bool ok = warp_wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd);
+      if (epi_any(!ok)) break;
       ptx::tc_fence_after();
-      const int mt = t % num_m, nt = t / num_m;
+      // this lane's four positions in the store phase
+      const int64_t pq = (int64_t)un.pt * BM + 4 * lane;
+      const int nvalid = pq >= c.N ? 0 : (int)(c.N - pq < 4 ? c.N - pq : 4);
+      int64_t obase = 0;  // out offset of (b, oc = 0, position pq)
+      if (nvalid > 0) {
+        const int64_t b = pq / P;
+        obase = b * c.OC * P + (pq - b * P);
+      }
+      // P % 4 == 0 and a 16-byte aligned out: the four positions are in one
+      // image and form one aligned float4
+      const bool vec = nvalid == 4 && c.vec_out;
+      const int oc0 = un.ot * q.bn;
+      const uint32_t tacc = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)buf * 128u;
 #pragma unroll 1
-      for (int h = 0; h < MH; ++h)
-        drain_accumulator(tmem, q, (uint32_t)(buf + h) * 256u, (bn + 31) & ~31, stage,
-                          Store{c, (int64_t)mt * MH * BM + h * BM, (int64_t)nt * bn, bn});
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&ctl->acce[buf]);
+      for (int cc = 0; cc < q.bn; cc += 32) {
+        uint32_t r[32];
+        ptx::tmem_ld32(tacc + (uint32_t)cc, r);
+        ptx::tmem_ld_wait();
+        if (cc + 32 >= q.bn) {  // the whole accumulator is read: hand it back
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&ctl->acce[buf]);
+        }
+        epi_sync();  // the previous chunk's readers are done with the block
+#pragma unroll
+        for (int j = 0; j < 32; ++j) epi_stage[j * BM + quarter * 32 + lane] = __uint_as_float(r[j]);
+        epi_sync();
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {
+          const int jj = quarter * 8 + i, col = cc + jj;  // channel in chunk / in tile
+          if (col >= q.bn) break;
+          const float4 v = *reinterpret_cast<const float4*>(epi_stage + jj * BM + 4 * lane);
+          if (un.slot >= 0) {  // K-slice partial sums: [slot][col][128 positions]
+            *reinterpret_cast<float4*>(q.part + ((int64_t)un.slot * q.bn + col) * BM + 4 * lane) =
+                v;
+            continue;
+          }
+          const int oc = oc0 + col;
+          if (oc >= c.OC) break;
+          const float bv = c.bias ? __ldg(c.bias + oc) : 0.0f;
+          float o[4] = {v.x + bv, v.y + bv, v.z + bv, v.w + bv};
+          if (c.relu) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[k] = fmaxf(o[k], 0.0f);
+          }
+          if (vec) {
+            *reinterpret_cast<float4*>(c.out + obase + (int64_t)oc * P) =
+                make_float4(o[0], o[1], o[2], o[3]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              if (k < nvalid) {
+                const int64_t pk = pq + k, b = pk / P;
+                c.out[(b * c.OC + oc) * P + (pk - b * P)] = o[k];
+              }
+            }
+          }
+        }
+      }
     }
   }
 
@@ -332,6 +482,33 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == MMA_WARP) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// Adds the K-slice partial sums of the tail tiles in slice order, then bias
+// (and ReLU), and writes NCHW.  Block (tail tile tt, 4 channels), thread =
+// position row: every partial read and output write is a 128-float run.
+constexpr int TAIL_COLS = 4;
+__global__ void __launch_bounds__(BM) k_conv_tail(const ConvArgs c, const Sched q) {
+  const int groups = q.bn / TAIL_COLS;  // bn is a multiple of 16
+  const int tt = blockIdx.x / groups, col0 = (blockIdx.x - tt * groups) * TAIL_COLS;
+  const int row = threadIdx.x;
+  const int t = q.full + tt, pt = t / q.n_oc, ot = t - pt * q.n_oc;
+  const int64_t p = (int64_t)pt * BM + row;
+  if (p >= c.N) return;
+  const int P = c.OH * c.OW;
+  const int b = (int)(p / P), pix = (int)(p - (int64_t)b * P);
+  const int64_t per = (int64_t)q.bn * BM;
+  const float* src = q.part + ((int64_t)tt * q.slices * q.bn + col0) * BM + row;
+#pragma unroll
+  for (int j = 0; j < TAIL_COLS; ++j) {
+    const int oc = ot * q.bn + col0 + j;
+    if (oc >= c.OC) break;
+    float acc = src[j * BM];
+    for (int sl = 1; sl < q.slices; ++sl) acc += src[sl * per + j * BM];
+    if (c.bias) acc += __ldg(c.bias + oc);
+    if (c.relu) acc = fmaxf(acc, 0.0f);
+    c.out[((int64_t)b * c.OC + oc) * P + pix] = acc;
   }
 }
 
@@ -357,94 +534,166 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Padded weight plane [OC, Kp] -> tensor map, box {16, 128}, 64-byte swizzle.
-bool encode_w(CUtensorMap* m, const float* base, uint64_t Kp, uint64_t OC) {
+// Padded weight plane [OC, Kp] -> tensor map, box {16, bn}, 64-byte swizzle;
+// rows past OC read as zero.
+bool encode_w(CUtensorMap* m, const float* base, uint64_t Kp, uint64_t OC, int bn) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {Kp, OC};
   const cuuint64_t strides[1] = {Kp * 4};
-  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)bn};
   const cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tile width: multiple of 16 up to bn_max minimising waves * (bn + 16).
-int pick_bn(int64_t num_m, int64_t N, int bn_max, int sms) {
-  int best = bn_max;
-  int64_t best_cost = INT64_MAX;
-  for (int bn = bn_max; bn >= 32; bn -= 16) {
-    const int64_t tiles = num_m * ((N + bn - 1) / bn);
-    const int64_t cost = ((tiles + sms - 1) / sms) * (bn + 16);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = bn;
+int64_t padded_k(int64_t K) { return (K + 3) / 4 * 4; }
+
+struct Plan {
+  Sched q;
+  int tail;         // tiles cut into K-slices
+  size_t part_off;  // byte offset of the partial sums in the workspace
+  size_t bytes;     // workspace bytes
+  int smem;         // dynamic shared memory of the main kernel
+};
+
+// Channel tiles of at most 256 (as even as possible, multiples of 16);
+// 128-position tiles; K-slices for the tail tiles when they shorten the
+// longest CTA's work and the partial sums fit in `limit` bytes of workspace.
+// Cost in k-block times of one CTA: whole-tile waves, the sliced wave(s), the
+// fix-up launch, and the partial sums' write + read at HBM speed (one k-block
+// of MMAs takes (3 or 1) * 2 * 128 * BN * 8 / 2047 clocks at ~90 % of the
+// measured TF32 rate, at least 400: below that the gather sets the pace).
+Plan make_plan(int64_t OC, int64_t Npix, int64_t K, bool three, size_t limit) {
+  Plan pl{};
+  Sched& q = pl.q;
+  q.n_oc = (int)((OC + BN_MAX - 1) / BN_MAX);
+  q.bn = (int)(((OC + q.n_oc - 1) / q.n_oc + 15) / 16 * 16);
+  q.kb = (int)((K + BK - 1) / BK);
+  const int64_t tiles = (Npix + BM - 1) / BM * q.n_oc;
+  const size_t w_bytes = (three ? 2u : 1u) * (size_t)OC * (size_t)padded_k(K) * sizeof(float);
+  pl.part_off = (w_bytes + 255) / 256 * 256;
+  const int64_t waves = tiles / kPlanSMs, tail = tiles - waves * kPlanSMs;
+  const double kb_clk =
+      std::max(400.0, (three ? 6.0 : 2.0) * BM * q.bn * UK / (2047.0 * 0.9));
+  const double gpu_bytes_per_kb = kHbmBytesPerClkSm * kb_clk * kPlanSMs;
+  int best_s = 1;
+  double best = (double)((waves + (tail > 0 ? 1 : 0)) * q.kb);
+  for (int S = 2; S <= 16 && S <= q.kb / 4 && tail > 0; ++S) {
+    const size_t part = (size_t)tail * S * q.bn * BM * sizeof(float);
+    if (pl.part_off + part > limit) break;
+    const double cost = (double)(waves * q.kb +
+                                 (tail * S + kPlanSMs - 1) / kPlanSMs * ((q.kb + S - 1) / S)) +
+                        kSliceLaunchKb + 2.0 * (double)part / gpu_bytes_per_kb;
+    if (cost < best) {
+      best = cost;
+      best_s = S;
     }
   }
-  return best;
+  q.slices = best_s;
+  pl.tail = best_s > 1 ? (int)tail : 0;
+  q.full = (int)(tiles - pl.tail);
+  q.units = q.full + pl.tail * best_s;
+  pl.bytes = best_s > 1 ? pl.part_off + (size_t)pl.tail * best_s * q.bn * BM * sizeof(float)
+                        : w_bytes;
+  q.nacc = q.bn <= 128 ? 2 : 1;
+  return pl;
 }
+
+// Shared-memory layout: weight stages, the tap table, the epilogue's staging
+// block, the barriers.  False when fewer than three stages fit.
+bool layout(Plan& pl, const ConvArgs& c, bool three) {
+  Sched& q = pl.q;
+  q.w_bytes = (three ? 2 : 1) * q.bn * BK * 4;
+  q.tab_bytes = (c.KH * c.KW * 8 + 127) / 128 * 128;
+  const int avail = SMEM_LIMIT - 1024 - q.tab_bytes - EPI_STAGE_BYTES - (int)sizeof(Ctl);
+  q.stages = avail / q.w_bytes < MAX_STAGES ? avail / q.w_bytes : MAX_STAGES;
+  pl.smem = 1024 + q.stages * q.w_bytes + q.tab_bytes + EPI_STAGE_BYTES + (int)sizeof(Ctl);
+  return q.stages >= 3;
+}
+
+// Input channel fastest in the kernel's K order (see the file comment).
+bool ic_fastest(const ConvArgs& c) { return c.IC >= 8; }
 
 constexpr int kMaxDev = 64;
 
-template <int MH, bool THREE>
-cudaError_t run(const ConvArgs& c, const float* w_hi, const float* w_lo, int64_t Kp,
-                cudaStream_t s) {
-  using Cf = Cfg<MH, THREE>;
+template <bool THREE, bool ICF>
+cudaError_t launch_main(const ConvArgs& c, const Plan& pl, const CUtensorMap& th,
+                        const CUtensorMap& tl, int grid, cudaStream_t s) {
   static bool ready[kMaxDev];
-  auto k = k_tc_conv<MH, THREE>;
+  auto k = k_tc_conv<THREE, ICF>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= kMaxDev || !ready[dev]) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (e != cudaSuccess) return e;
     if (dev < kMaxDev) ready[dev] = true;
   }
+  k<<<grid, THREADS, pl.smem, s>>>(th, tl, c, pl.q);
+  return cudaGetLastError();
+}
+
+template <bool THREE>
+cudaError_t run(const ConvArgs& c, Plan pl, const float* w_hi, const float* w_lo, int64_t Kp,
+                float* part, cudaStream_t s) {
   CUtensorMap th, tl;
-  if (!encode_w(&th, w_hi, (uint64_t)Kp, (uint64_t)c.OC) ||
-      !encode_w(&tl, THREE ? w_lo : w_hi, (uint64_t)Kp, (uint64_t)c.OC))
+  if (!encode_w(&th, w_hi, (uint64_t)Kp, (uint64_t)c.OC, pl.q.bn) ||
+      !encode_w(&tl, THREE ? w_lo : w_hi, (uint64_t)Kp, (uint64_t)c.OC, pl.q.bn))
     return cudaErrorInvalidValue;
+  if (!layout(pl, c, THREE)) return cudaErrorInvalidValue;
+  pl.q.part = part;
   const int sms = device_sm_count();
-  const int num_m = (int)((c.M + MH * BM - 1) / (MH * BM));
-  const int bn = pick_bn(num_m, c.N, Cf::BN_MAX, sms);
-  const int num_n = (int)((c.N + bn - 1) / bn);
-  const int tiles = num_m * num_n;
-  const int grid = tiles < sms ? tiles : sms;
-  k<<<grid, THREADS, Cf::SMEM, s>>>(th, tl, c, num_m, num_n, bn);
+  const int grid = pl.q.units < sms ? pl.q.units : sms;
+  cudaError_t e = ic_fastest(c) ? launch_main<THREE, true>(c, pl, th, tl, grid, s)
+                                : launch_main<THREE, false>(c, pl, th, tl, grid, s);
+  note_launch();
+  if (e != cudaSuccess || pl.tail == 0) return e;
+  k_conv_tail<<<(unsigned)(pl.tail * (pl.q.bn / TAIL_COLS)), BM, 0, s>>>(c, pl.q);
   note_launch();
   return cudaGetLastError();
 }
 
-int64_t padded_k(int64_t K) { return (K + 3) / 4 * 4; }
-
 }  // namespace
 
-bool tc_conv_supported(const ConvArgs& c) {
-  const double tiles = (double)((c.M + BM - 1) / BM) * (double)((c.N + 31) / 32);
-  return tiles < 2147483647.0 && encode_fn() != nullptr;
+bool tc_conv_shape_ok(const ConvArgs& c) {
+  const int64_t lim30 = int64_t(1) << 30, lim31 = (int64_t(1) << 31) - 1;
+  if ((int64_t)c.KH * c.KW > MAX_TAPS) return false;
+  if ((int64_t)(c.KH - 1) * c.dH >= lim30 || (int64_t)(c.KW - 1) * c.dW >= lim30) return false;
+  if ((int64_t)c.H + 2 * (int64_t)c.pH >= lim30 || (int64_t)c.W + 2 * (int64_t)c.pW >= lim30)
+    return false;
+  // the running input-channel offset may pass IC by up to 17 planes
+  if (((int64_t)c.IC + 17) * c.H * c.W > lim31) return false;
+  const int64_t tiles = (c.N + BM - 1) / BM * ((c.M + BN_MAX - 1) / BN_MAX);
+  return tiles < lim31;
 }
 
-size_t tc_conv_workspace_bytes(int64_t OC, int64_t K, bool three_pass) {
-  return (three_pass ? 2u : 1u) * (size_t)OC * (size_t)padded_k(K) * sizeof(float);
+bool tc_conv_supported(const ConvArgs& c) { return tc_conv_shape_ok(c) && encode_fn() != nullptr; }
+
+size_t tc_conv_workspace_bytes(const ConvArgs& c, bool three_pass, size_t limit) {
+  return make_plan(c.M, c.N, c.K, three_pass, limit).bytes;
 }
 
-cudaError_t launch_tc_conv(const ConvArgs& c, bool three_pass, void* workspace, cudaStream_t s) {
+cudaError_t launch_tc_conv(const ConvArgs& c, bool three_pass, void* workspace,
+                           size_t workspace_bytes, cudaStream_t s) {
   if (!tc_conv_supported(c) || !workspace) return cudaErrorNotSupported;
+  const Plan pl = make_plan(c.M, c.N, c.K, three_pass, workspace_bytes);
+  if (pl.bytes > workspace_bytes) return cudaErrorInvalidValue;
   const int64_t Kp = padded_k(c.K);
   float* w_hi = static_cast<float*>(workspace);
   float* w_lo = three_pass ? w_hi + c.OC * Kp : nullptr;
+  float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.part_off);
   const int64_t total = c.OC * Kp;
   const int64_t cap = (int64_t)device_sm_count() * 8;
   const int64_t blocks = (total + 255) / 256;
-  k_prep_w<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(c.w, c.OC, c.K, Kp, w_hi,
-                                                                   w_lo);
+  k_prep_w<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(
+      c.w, c.OC, c.K, Kp, c.IC, c.KH * c.KW, ic_fastest(c) ? 1 : 0, w_hi, w_lo);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (c.M > BM)
-    return three_pass ? run<2, true>(c, w_hi, w_lo, Kp, s) : run<2, false>(c, w_hi, w_lo, Kp, s);
-  return three_pass ? run<1, true>(c, w_hi, w_lo, Kp, s) : run<1, false>(c, w_hi, w_lo, Kp, s);
+  return three_pass ? run<true>(c, pl, w_hi, w_lo, Kp, part, s)
+                    : run<false>(c, pl, w_hi, nullptr, Kp, part, s);
 }
 
 cudaError_t conv_take_watchdog(int* value) {

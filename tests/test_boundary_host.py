@@ -207,8 +207,12 @@ def test_conv_argument_errors(lib):
 def test_conv_workspace_size_query(lib):
     q = binding.conv2d_gemm_f32_workspace_bytes
     body = (8, 256, 56, 56, 256, 3, 3, 1, 1, 1, 1, 1, 1)
-    assert q(*body, 0) == 2 * 256 * 2304 * 4   # hi and lo weight planes
-    assert q(*body, 1) == 256 * 2304 * 4
+    # hi and lo weight planes, then the partial sums of the last wave's 44
+    # tiles (196 tiles of 128 positions on 152 SMs), each cut into 3 K-slices
+    # of a 128 x 256 fp32 tile
+    parts = 44 * 3 * 128 * 256 * 4
+    assert q(*body, 0) == 2 * 256 * 2304 * 4 + parts
+    assert q(*body, 1) == 256 * 2304 * 4 + parts
     assert q(*body, 2) == 0
     stem = (1, 3, 768, 768, 128, 7, 7, 4, 4, 3, 3, 1, 1)
     assert q(*stem, 0) == 2 * 128 * 148 * 4    # K = 147 padded to 148
@@ -219,14 +223,17 @@ def test_conv_workspace_size_query(lib):
 def test_conv_workspace_argument_errors(lib):
     args = (P1, P2, P3, P4, 8, 256, 56, 56, 256, 3, 3, 1, 1, 1, 1, 1, 1, 0)
     need = binding.conv2d_gemm_f32_workspace_bytes(*args[4:])
+    least = 2 * 256 * 2304 * 4  # the weight planes alone (no K-slices)
+    assert need > least
     W = 0x50000000
     f = binding.conv2d_gemm_f32_ws
-    assert f(*args, W, need - 1, None) == binding.IMC_ERR_ARG
+    assert f(*args, W, least - 1, None) == binding.IMC_ERR_ARG
     assert f(*args, None, need, None) == binding.IMC_ERR_ARG
     assert f(*args, W + 8, need, None) == binding.IMC_ERR_ARG
     assert f(*args, P2 + 64, need, None) == binding.IMC_ERR_ALIAS  # overlaps w
-    assert without_gpu([["conv2d_gemm_f32_ws", list(args) + [W, need, None]]]) == [
-        binding.IMC_ERR_DEVICE]
+    assert without_gpu([["conv2d_gemm_f32_ws", list(args) + [W, need, None]],
+                        ["conv2d_gemm_f32_ws", list(args) + [W, least, None]]]) == [
+        binding.IMC_ERR_DEVICE] * 2
 
 
 def test_mode_flags_and_linear_validation(lib):

@@ -246,6 +246,50 @@ def test_conv_integer_inputs_are_bit_exact(mode, idx):
     assert np.array_equal(got.astype(np.float64), ref)
 
 
+# Shapes that steer the tensor-core conv's work split (128-position x BN-channel
+# tiles on 152 SMs; the last wave's tiles cut into K-slices whose partial sums
+# a second kernel adds):
+SCHED_CONV = [  # B, IC, H, W, OC, KH, KW, stride, pad, dil, channels checked (None: all)
+    # 160 tiles: one whole wave, then 8 tiles in 9 K-slices (BN 256, one accumulator)
+    (5, 64, 64, 64, 256, 3, 3, 1, 1, 1, np.arange(0, 256, 9)),
+    # OC 320: two channel tiles of 160; 14 tiles, all K-sliced
+    (2, 32, 20, 20, 320, 3, 3, 1, 1, 1, None),
+    # 11x11 taps, stride 4
+    (1, 3, 67, 67, 64, 11, 11, 4, 2, 1, None),
+    # K = 9 < one k-block of 16; BN 16
+    (2, 1, 30, 30, 16, 3, 3, 1, 1, 1, None),
+    # dilation 4 with padding 4, 48 channels
+    (1, 4, 30, 30, 48, 3, 3, 1, 4, 4, None),
+    # 1x1, K = 520 (not a multiple of 16), 290 tiles: two waves, two accumulators
+    (2, 520, 136, 136, 96, 1, 1, 1, 0, 1, np.arange(0, 96, 5)),
+    # input rows staged in shared memory: 5x5 stride 2, tiles running into the next image
+    (3, 24, 40, 40, 96, 5, 5, 2, 2, 1, None),
+    # staged, dilation 2 with padding 2
+    (2, 16, 32, 32, 64, 3, 3, 1, 2, 2, None),
+]
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1", "default"])
+@pytest.mark.parametrize("idx", range(len(SCHED_CONV)))
+def test_conv_work_split(mode, idx):
+    t = SCHED_CONV[idx]
+    x, w, b, s, p, d = _conv_case(t[:10], 320 + idx)
+    got, ref, S, kern = run_conv(x, w, b, s, p, d, mode, channels=t[10])
+    if mode in EXPECT:
+        assert kern == EXPECT[mode]
+    within(got, ref, S, TOL[mode], f"{mode} sched conv #{idx}")
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1"])
+@pytest.mark.parametrize("idx", [0, 1, 5])
+def test_conv_work_split_integer_bit_exact(mode, idx):
+    t = SCHED_CONV[idx]
+    x, w, b, s, p, d = _conv_case(t[:10], 420 + idx, spec=("I", -2, 2))
+    got, ref, _, kern = run_conv(x, w, b, s, p, d, mode, channels=t[10])
+    assert kern == EXPECT[mode]
+    assert np.array_equal(got.astype(np.float64), ref)
+
+
 def test_conv_1x1_matches_addmm_path():
     B, IC, H, W, OC = 2, 64, 16, 16, 128
     x, w, b = synth.conv_inputs(B, IC, H, W, OC, 1, 1, workload=55)
