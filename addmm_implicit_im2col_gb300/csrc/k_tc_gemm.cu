@@ -13,12 +13,21 @@
 // (1xTF32).  The main kernel is then a plain pipeline:
 //
 //   warp 0      TMA producer: mat1 tile (128 x 16), Bt_hi / Bt_lo tiles (BN x 16),
-//               64-byte swizzle, into a 4-stage ring (8 stages for 1xTF32)
-//   warps 6-9   (3xTF32) A_lo = mat1 - tf32(mat1), elementwise into the stage
+//               64-byte swizzle, into a 4-stage ring (5 for the TS form, 8 for
+//               1xTF32)
+//   warps 6-9   (3xTF32) A_lo = mat1 - tf32(mat1); in the TS form each thread
+//               takes one row of the mat1 tile, splits it and writes A_hi and
+//               A_lo to the stage's TMEM columns, otherwise A_lo goes to a
+//               shared-memory tile elementwise
 //   warp 1      TMEM owner + MMA issuer: per 8-deep k-step
-//               A_lo*B_hi + A_hi*B_lo + A_hi*B_hi into an fp32 TMEM accumulator
-//               (A_hi is the raw mat1 tile: the tensor core drops the 13 low
-//               mantissa bits itself); double-buffered accumulator
+//               A_lo*B_hi + A_hi*B_lo + A_hi*B_hi into an fp32 TMEM accumulator;
+//               the TS form reads A from TMEM (measured: 94 % of the TF32 MMA
+//               rate at N = 256, against 80 % with both operands in shared
+//               memory) and has one accumulator, the other form reads the raw
+//               mat1 tile as A_hi (the tensor core drops the 13 low mantissa
+//               bits itself) and double-buffers the accumulator.  The TS form
+//               is used when a unit runs at least kTsMinKb k-blocks, where the
+//               faster MMAs outweigh the drain of the single accumulator
 //   warps 2-5   epilogue: tcgen05.ld, 32x32 transpose through shared memory,
 //               beta*self + alpha*acc, 16-byte row-segment stores
 //
@@ -48,11 +57,21 @@ struct Layout {
 };
 constexpr Layout kL3 = {0, A_BYTES, 2 * A_BYTES, 2 * A_BYTES + B_BYTES, 2 * (A_BYTES + B_BYTES), 4};
 constexpr Layout kL1 = {0, 0, A_BYTES, 0, A_BYTES + B_BYTES, 8};
+// 3xTF32 with A from TMEM: no A_lo tile in shared memory
+constexpr Layout kLts = {0, 0, A_BYTES, A_BYTES + B_BYTES, A_BYTES + 2 * B_BYTES, 5};
 constexpr int smem_bytes(const Layout& L) {
   return 1024 + L.stages * L.bytes + EPI_BYTES + (int)sizeof(Ctl);
 }
-static_assert(smem_bytes(kL3) <= 232448 && smem_bytes(kL1) <= 232448, "shared memory");
+static_assert(smem_bytes(kL3) <= 232448 && smem_bytes(kL1) <= 232448 &&
+                  smem_bytes(kLts) <= 232448, "shared memory");
 static_assert(kL1.stages <= MAX_STAGES, "stages");
+// A-from-TMEM form: one accumulator (columns 0-255), A stages of 32 columns
+// (hi 0-15, lo 16-31) from column 256.
+constexpr uint32_t TS_A_COL0 = 256, TS_A_STAGE_COLS = 32;
+static_assert(TS_A_COL0 + kLts.stages * TS_A_STAGE_COLS <= TMEM_COLS, "TMEM");
+// K-blocks per unit from which the A-from-TMEM form is used: it runs the MMAs
+// faster but holds the MMA while the single accumulator drains.
+constexpr int kTsMinKb = 96;
 
 __device__ int g_watchdog_gemm;
 
@@ -193,13 +212,15 @@ __global__ void __launch_bounds__(256) k_splitk_epilogue(const float* __restrict
   }
 }
 
-template <bool THREE>
+template <bool THREE, bool TS>
 __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBh,
               const __grid_constant__ CUtensorMap tmBl, const GemmArgs g, const int num_m,
               const int num_n, const int group, const int bn, const int splits, const int kps,
               float* __restrict__ part) {
-  constexpr Layout L = THREE ? kL3 : kL1;
+  static_assert(!TS || THREE, "the A-from-TMEM form is 3xTF32");
+  constexpr Layout L = TS ? kLts : (THREE ? kL3 : kL1);
+  constexpr int NACC = TS ? 1 : 2;  // accumulator buffers
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   float* epi = reinterpret_cast<float*>(smem + L.stages * L.bytes);
@@ -212,7 +233,7 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
   const int num_kb = (int)((g.K + BK - 1) / BK);
   int* wd = &g_watchdog_gemm;
 
-  if (threadIdx.x == 0) init_barriers(ctl, L.stages, 1, 128);
+  if (threadIdx.x == 0) init_barriers(ctl, L.stages, 1, TS ? 4 : 128);
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmBh);
@@ -263,8 +284,8 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
       int s = 0, tl = 0;
       uint32_t ph = 0;
       for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++tl) {
-        const int buf = tl & 1;
-        const uint32_t use = (uint32_t)(tl >> 1);
+        const int buf = tl % NACC;
+        const uint32_t use = (uint32_t)(tl / NACC);
         if (!wait_bar(&ctl->acce[buf], (use & 1u) ^ 1u, abort, kSiteMmaAccEmpty, wd)) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)buf * ACC_STRIDE;
@@ -281,7 +302,13 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
           for (int ks = 0; ks < KSTEPS; ++ks) {
             const uint64_t ah = sw64_desc(st + L.a, ks), bh = sw64_desc(st + L.b_hi, ks);
             const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
-            if (THREE) {
+            if (TS) {
+              const uint32_t th = tmem + TS_A_COL0 + (uint32_t)s * TS_A_STAGE_COLS + ks * UK;
+              const uint64_t bl = sw64_desc(st + L.b_lo, ks);
+              ptx::mma_tf32_ts(d, th + 16u, bh, idesc, acc);  // A_lo * B_hi
+              ptx::mma_tf32_ts(d, th, bl, idesc, 1u);         // A_hi * B_lo
+              ptx::mma_tf32_ts(d, th, bh, idesc, 1u);         // A_hi * B_hi
+            } else if (THREE) {
               const uint64_t al = sw64_desc(st + L.a_lo, ks), bl = sw64_desc(st + L.b_lo, ks);
               ptx::mma_tf32(d, al, bh, idesc, acc);  // small terms first
               ptx::mma_tf32(d, ah, bl, idesc, 1u);
@@ -310,21 +337,71 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
     float* stage = epi + (warp - 2) * 32 * EPI_PITCH;
     int tl = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++tl) {
-      const int buf = tl & 1;
-      const uint32_t use = (uint32_t)(tl >> 1);
+      const int buf = tl % NACC;
+      const uint32_t use = (uint32_t)(tl / NACC);
       if (!warp_wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd)) break;
       ptx::tc_fence_after();
       int mt, nt;
       tile_coords(u % num_tiles, num_m, num_n, group, mt, nt);
+      // the single accumulator is handed back as soon as it is read
+      uint64_t* early = TS ? &ctl->acce[buf] : nullptr;
       if (splits == 1)
         drain_accumulator(tmem, q, (uint32_t)buf * ACC_STRIDE, bn, stage,
-                          Store{g, (int64_t)mt * BM, (int64_t)nt * bn});
+                          Store{g, (int64_t)mt * BM, (int64_t)nt * bn}, early);
       else
         drain_accumulator(tmem, q, (uint32_t)buf * ACC_STRIDE, bn, stage,
                           PartStore{part + (int64_t)(u / num_tiles) * g.M * g.N, g.M, g.N,
-                                    (int64_t)mt * BM, (int64_t)nt * bn});
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&ctl->acce[buf]);
+                                    (int64_t)mt * BM, (int64_t)nt * bn},
+                          early);
+      if (!TS) {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&ctl->acce[buf]);
+      }
+    }
+  } else if (TS) {
+    // ------------------------------- split warps: A_hi / A_lo into TMEM
+    // Thread = row r of the A tile (TMEM lane r): its 16 values of a k-block
+    // are read from the swizzled tile, split, and written to the stage's
+    // TMEM columns; one arrival per warp on split[s].
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TS_A_COL0;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      bool ok = true;
+      const int kb0 = (u / num_tiles) * kps, kb1 = min(num_kb, kb0 + kps);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd) ||
+            !warp_wait_bar(&ctl->full[s], ph, abort, kSiteSplitFull, wd)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint8_t* row = smem + s * L.bytes + L.a + sw64_row_base(r);
+        float hi[16], lo[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 v = *reinterpret_cast<const float4*>(row + sw64_unit(r, j));
+          const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[4 * j + e] = tf32_hi(vv[e]);
+            lo[4 * j + e] = tf32_lo(vv[e]);
+          }
+        }
+        const uint32_t ta = trow + (uint32_t)s * TS_A_STAGE_COLS;
+        ptx::tmem_st16(ta, hi);
+        ptx::tmem_st16(ta + 16, lo);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ctl->split[s]);
+        if (++s == L.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
     }
   } else if (THREE) {
     // ------------------------------------------------ split warps: A_lo
@@ -474,12 +551,12 @@ size_t plan_bytes(const Plan& p, int64_t M, int64_t N) {
 
 constexpr int kMaxDev = 64;
 
-template <bool THREE>
+template <bool THREE, bool TS>
 cudaError_t run(const GemmArgs& g, const Plan& p, const float* bt_hi, const float* bt_lo,
                 float* part, cudaStream_t s) {
-  constexpr int smem = smem_bytes(THREE ? kL3 : kL1);
+  constexpr int smem = smem_bytes(TS ? kLts : (THREE ? kL3 : kL1));
   static bool ready[kMaxDev];
-  auto k = k_tc_gemm<THREE>;
+  auto k = k_tc_gemm<THREE, TS>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -552,7 +629,9 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return three_pass ? run<true>(g, p, b_hi, b_lo, part, s) : run<false>(g, p, b_hi, nullptr, part, s);
+  if (!three_pass) return run<false, false>(g, p, b_hi, nullptr, part, s);
+  return p.kps >= kTsMinKb ? run<true, true>(g, p, b_hi, b_lo, part, s)
+                           : run<true, false>(g, p, b_hi, b_lo, part, s);
 }
 
 cudaError_t gemm_take_watchdog(int* value) {

@@ -144,9 +144,13 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // segments to the store functor: first store.load(row, col) for all eight
 // segments a lane handles in the block (so their global reads are in flight
 // together), then store(row, col, acc, loaded) for each.
+// With `release` given, the thread arrives on it (after a tcgen05 fence) as
+// soon as its last columns are in registers, so the MMA can reuse the
+// accumulator while the stores finish; otherwise the caller arrives after.
 template <class StoreFn>
 __device__ __forceinline__ void drain_accumulator(uint32_t tmem, int q, uint32_t col, int ncols,
-                                                  float* stage, const StoreFn& store) {
+                                                  float* stage, const StoreFn& store,
+                                                  uint64_t* release = nullptr) {
   const int lane = threadIdx.x & 31;
   const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + col;
 #pragma unroll 1
@@ -154,6 +158,10 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tmem, int q, uint32_t
     uint32_t r[32];
     ptx::tmem_ld32(tbase + (uint32_t)c, r);
     ptx::tmem_ld_wait();
+    if (release && c + 32 >= ncols) {
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(release);
+    }
     float4* dst = reinterpret_cast<float4*>(stage + lane * EPI_PITCH);
 #pragma unroll
     for (int j = 0; j < 8; ++j)
