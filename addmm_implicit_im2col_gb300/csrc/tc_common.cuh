@@ -121,17 +121,22 @@ __device__ __forceinline__ uint64_t sw64_desc(uint32_t tile_addr, int ks) {
   return ptx::smem_desc(tile_addr + ks * 32, 16, 512, ptx::kSwizzle64B);
 }
 
-// Grouped raster: `group` M-tiles share each N-tile before moving on, so the
-// CTAs resident at one time reuse the same operand panels from L2.
+// Grouped raster.  group > 0: `group` M-tiles share each N-tile before moving
+// on to the next N-tile; group < 0: -group N-tiles share each M-tile.  Either
+// way the CTAs resident at one time reuse the same operand panels from L2.
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group, int& mt,
                                             int& nt) {
-  const int per = group * num_n;
+  const bool along_n = group < 0;
+  const int g = along_n ? -group : group;
+  const int major = along_n ? num_n : num_m, minor = along_n ? num_m : num_n;
+  const int per = g * minor;
   const int gi = t / per;
-  const int m_first = gi * group;
-  const int rows = min(group, num_m - m_first);
+  const int first = gi * g;
+  const int width = min(g, major - first);
   const int r = t - gi * per;
-  mt = m_first + r % rows;
-  nt = r / rows;
+  const int a = first + r % width, b = r / width;
+  mt = along_n ? b : a;
+  nt = along_n ? a : b;
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
