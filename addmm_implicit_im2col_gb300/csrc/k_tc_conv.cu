@@ -301,7 +301,26 @@ __global__ void __launch_bounds__(THREADS, 1)
             set_tap();
           }
         };
-        ok = rotate3(nkb, gather, store);
+        if (c.IC % BK == 0) {
+          // a k-block lies in one tap: one bounds check per k-block, then 8
+          // loads at the channel-plane stride (ic, tap: this warp's next k)
+          auto gather16 = [&](float (&v)[8]) {
+            const float* src = xb + (ic_hw + tap_off);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = tap_in ? __ldg(src + j * HW) : 0.0f;
+            ic += BK;
+            ic_hw += BK * HW;
+            if (ic >= c.IC) {  // next tap: ic comes back to 0 or 8 (this warp's half)
+              ic -= c.IC;
+              ic_hw = ic * HW;
+              ++tap;
+              set_tap();
+            }
+          };
+          ok = rotate3(nkb, gather16, store);
+        } else {
+          ok = rotate3(nkb, gather, store);
+        }
       } else {
         // running (ic, r) of this warp's next k = ic*taps + r
         int ic_hw = (k0 / taps) * HW, r = k0 - (k0 / taps) * taps;
