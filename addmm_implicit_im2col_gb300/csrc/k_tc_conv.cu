@@ -461,19 +461,24 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) epi_stage[j * BM + quarter * 32 + lane] = __uint_as_float(r[j]);
         epi_sync();
-#pragma unroll 1
+        // bias of chunk channel `lane`, handed to the rows below by shuffle
+        const int my_oc = oc0 + cc + lane;
+        const float my_bias =
+            (un.slot < 0 && c.bias && cc + lane < q.bn && my_oc < c.OC) ? __ldg(c.bias + my_oc)
+                                                                          : 0.0f;
+#pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int jj = quarter * 8 + i, col = cc + jj;  // channel in chunk / in tile
-          if (col >= q.bn) break;
+          const float bv = __shfl_sync(0xffffffffu, my_bias, jj);
           const float4 v = *reinterpret_cast<const float4*>(epi_stage + jj * BM + 4 * lane);
+          if (col >= q.bn) continue;
           if (un.slot >= 0) {  // K-slice partial sums: [slot][col][128 positions]
             *reinterpret_cast<float4*>(q.part + ((int64_t)un.slot * q.bn + col) * BM + 4 * lane) =
                 v;
             continue;
           }
           const int oc = oc0 + col;
-          if (oc >= c.OC) break;
-          const float bv = c.bias ? __ldg(c.bias + oc) : 0.0f;
+          if (oc >= c.OC) continue;
           float o[4] = {v.x + bv, v.y + bv, v.z + bv, v.w + bv};
           if (c.relu) {
 #pragma unroll
