@@ -40,8 +40,8 @@
 // columns each: hi 0-15, lo 16-31).
 // Scheduling: persistent CTAs take whole tiles first.  When the last wave
 // would leave SMs idle, its tiles are cut into S K-slices; a slice writes its
-// partial sums to scratch and k_conv_tail adds them in slice order (the result
-// does not depend on which CTA ran which slice).
+// partial sums to scratch and k_conv_tail adds the S partial tiles in slice
+// order (the result does not depend on which CTA ran which slice).
 // Every barrier wait is bounded (see tc_common.cuh).
 #include <algorithm>
 #include <mutex>
@@ -59,10 +59,11 @@ constexpr int BK = 16;           // fp32 per k-block: one 64-byte swizzle row
 constexpr int KSTEPS = BK / UK;  // 2
 constexpr int BN_MAX = 256;
 constexpr int GATHER_WARPS = 8;
-constexpr int TMA_WARP = 8, MMA_WARP = 9, THREADS = 14 * 32;
+constexpr int TMA_WARP = 8, MMA_WARP = 9, EPI_WARP0 = 10, THREADS = 14 * 32;
 constexpr uint32_t A_COL0 = 256, A_STAGE_COLS = 32;
 constexpr int MAX_TAPS = 1024;  // KH*KW entries of the per-CTA tap table
-constexpr int EPI_STAGE_BYTES = 32 * BM * 4;  // one 32-channel chunk of a tile
+constexpr int EPI_CHUNK_FLOATS = 32 * BM;  // one 32-channel chunk of a tile
+constexpr int EPI_STAGE_BYTES = 2 * EPI_CHUNK_FLOATS * 4;  // two chunk buffers
 constexpr int SMEM_LIMIT = 232448;
 constexpr int kPlanSMs = 152;            // SM count the K-slice plan is made for
 constexpr double kSliceLaunchKb = 8.0;   // fix-up launch, in k-block times
@@ -77,6 +78,8 @@ struct Sched {
   int stages, nacc;         // pipeline stages, accumulator buffers
   int w_bytes;              // weight tiles of a stage (hi [+ lo])
   int tab_bytes;            // tap table
+  int tma_out;              // whole tiles inside one image leave by TMA store
+  int tpi;                  // position tiles per image (0: tiles run across images)
   float* part;              // tail partial sums [units - full][bn][128]
 };
 
@@ -106,27 +109,50 @@ __device__ __forceinline__ Unit decode(const Sched& q, int u) {
   return r;
 }
 
+// Positions of tile pt: p0 .. p0 + count - 1 (global position = b*OH*OW +
+// oh*OW + ow).  With q.tpi > 0 each image has its own tiles (the last one of
+// an image may be short), so no tile runs into the next image.
+struct TilePos {
+  int64_t p0;
+  int count;
+};
+__device__ __forceinline__ TilePos tile_pos(const ConvArgs& c, const Sched& q, int pt) {
+  TilePos t;
+  if (q.tpi > 0) {
+    const int b = pt / q.tpi, pix0 = (pt - b * q.tpi) * BM, P = c.OH * c.OW;
+    t.p0 = (int64_t)b * P + pix0;
+    t.count = P - pix0 < BM ? P - pix0 : BM;
+  } else {
+    t.p0 = (int64_t)pt * BM;
+    t.count = c.N - t.p0 < BM ? (int)(c.N - t.p0) : BM;
+  }
+  return t;
+}
+
 // ------------------------------------------------------- weight pre-pass
 // Column k of row oc takes w[oc, ic, kh, kw]: k = ic*taps + tap (the pages'
 // order) or, with icf, k = tap*IC + ic (tap = kh*KW + kw).  w_hi gets its TF32
-// part (0 for k >= K), w_lo the rest.
-__global__ void k_prep_w(const float* __restrict__ w, int64_t OC, int64_t K, int64_t Kp, int IC,
-                         int taps, int icf, float* __restrict__ w_hi, float* __restrict__ w_lo) {
-  const int64_t total = OC * Kp;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t oc = e / Kp, k = e - oc * Kp;
-    int64_t src = k;
-    if (icf) {
-      const int64_t tap = k / IC;
-      src = (k - tap * IC) * taps + tap;
-    }
-    const float v = k < K ? __ldg(w + oc * K + src) : 0.0f;
-    if (w_lo) {
-      w_hi[e] = tf32_hi(v);
-      w_lo[e] = tf32_lo(v);
-    } else {
-      w_hi[e] = v;
+// part (0 for k >= K), w_lo the rest.  Block (x, y) covers columns of rows
+// y, y + gridDim.y, ...
+__global__ void __launch_bounds__(256) k_prep_w(const float* __restrict__ w, int OC, int K, int Kp,
+                                                int IC, int taps, int icf, float* __restrict__ w_hi,
+                                                float* __restrict__ w_lo) {
+  for (int oc = blockIdx.y; oc < OC; oc += gridDim.y) {
+    const float* wr = w + (int64_t)oc * K;
+    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < Kp; k += gridDim.x * blockDim.x) {
+      int src = k;
+      if (icf) {
+        const int tap = k / IC;
+        src = (k - tap * IC) * taps + tap;
+      }
+      const float v = k < K ? __ldg(wr + src) : 0.0f;
+      const int64_t e = (int64_t)oc * Kp + k;
+      if (w_lo) {
+        w_hi[e] = tf32_hi(v);
+        w_lo[e] = tf32_lo(v);
+      } else {
+        w_hi[e] = v;
+      }
     }
   }
 }
@@ -172,7 +198,7 @@ __device__ __forceinline__ bool epi_any(bool v) {
 template <bool THREE, bool ICF>
 __global__ void __launch_bounds__(THREADS, 1)
     k_tc_conv(const __grid_constant__ CUtensorMap tmWh, const __grid_constant__ CUtensorMap tmWl,
-              const ConvArgs c, const Sched q) {
+              const __grid_constant__ CUtensorMap tmO, const ConvArgs c, const Sched q) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int b_tile = q.bn * BK * 4;  // one weight tile (hi or lo)
@@ -241,8 +267,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     for (int u = blockIdx.x; u < q.units && ok; u += gridDim.x) {
       const Unit un = decode(q, u);
-      const int64_t p = (int64_t)un.pt * BM + quarter * 32 + lane;
-      const bool pok = p < c.N;
+      const TilePos tp = tile_pos(c, q, un.pt);
+      const int64_t p = tp.p0 + quarter * 32 + lane;
+      const bool pok = quarter * 32 + lane < tp.count;
       int b = 0, ih0 = 0, iw0 = 0;
       if (pok) {
         b = (int)(p / P);
@@ -421,13 +448,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ----------------------------------------------------------- epilogue
     // Per 32-channel chunk: TMEM -> registers -> a [32 channels][128
-    // positions] staging block in shared memory; then warp q writes channels
-    // 8q .. 8q+7 of the chunk, each as one 512-byte run of positions (lane l
-    // stores positions 4l .. 4l+3 with one 16-byte store).  The accumulator is
-    // released as soon as its last chunk is in registers.
-    const int quarter = warp & 3;
+    // positions] block in shared memory (two blocks, alternating); the
+    // accumulator is released as soon as its last chunk is in registers.  A
+    // whole tile inside one image (q.tma_out) gets bias / ReLU on the way into
+    // the block and leaves by one TMA store per chunk; otherwise warp q writes
+    // channels 8q .. 8q+7 of the chunk, each as one 512-byte run of positions
+    // (lane l stores positions 4l .. 4l+3 with one 16-byte store).
+    const int quarter = warp & 3, row = quarter * 32 + lane;
+    const bool issuer = warp == EPI_WARP0 && lane == 0;  // TMA stores
     const int64_t P = (int64_t)c.OH * c.OW;
-    int ul = 0;
+    int ul = 0, nchunk = 0;
     for (int u = blockIdx.x; u < q.units; u += gridDim.x, ++ul) {
       const Unit un = decode(q, u);
       const int buf = ul % q.nacc;
@@ -435,9 +465,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool ok = warp_wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd);
       if (epi_any(!ok)) break;
       ptx::tc_fence_after();
+      const TilePos tp = tile_pos(c, q, un.pt);
+      const int64_t p0 = tp.p0, plast = tp.p0 + tp.count - 1;
+      const int b0 = (int)(p0 / P);
+      const bool by_tma = q.tma_out && un.slot < 0 && plast / P == b0;
       // this lane's four positions in the store phase
-      const int64_t pq = (int64_t)un.pt * BM + 4 * lane;
-      const int nvalid = pq >= c.N ? 0 : (int)(c.N - pq < 4 ? c.N - pq : 4);
+      const int64_t pq = p0 + 4 * lane;
+      const int left = tp.count - 4 * lane;
+      const int nvalid = left <= 0 ? 0 : (left < 4 ? left : 4);
       int64_t obase = 0;  // out offset of (b, oc = 0, position pq)
       if (nvalid > 0) {
         const int64_t b = pq / P;
@@ -449,7 +484,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int oc0 = un.ot * q.bn;
       const uint32_t tacc = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)buf * 128u;
 #pragma unroll 1
-      for (int cc = 0; cc < q.bn; cc += 32) {
+      for (int cc = 0; cc < q.bn; cc += 32, ++nchunk) {
         uint32_t r[32];
         ptx::tmem_ld32(tacc + (uint32_t)cc, r);
         ptx::tmem_ld_wait();
@@ -457,20 +492,37 @@ __global__ void __launch_bounds__(THREADS, 1)
           ptx::tc_fence_before();
           ptx::mbar_arrive(&ctl->acce[buf]);
         }
-        epi_sync();  // the previous chunk's readers are done with the block
-#pragma unroll
-        for (int j = 0; j < 32; ++j) epi_stage[j * BM + quarter * 32 + lane] = __uint_as_float(r[j]);
-        epi_sync();
-        // bias of chunk channel `lane`, handed to the rows below by shuffle
+        // bias of chunk channel `lane`, handed out by shuffle
         const int my_oc = oc0 + cc + lane;
         const float my_bias =
             (un.slot < 0 && c.bias && cc + lane < q.bn && my_oc < c.OC) ? __ldg(c.bias + my_oc)
                                                                           : 0.0f;
+        float* blk = epi_stage + (nchunk & 1) * EPI_CHUNK_FLOATS;
+        if (issuer) ptx::bulk_wait_read1();  // the store from this block two chunks ago
+        epi_sync();  // ... and the plain stores of that chunk are done with it
+        if (by_tma) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float o = __uint_as_float(r[j]) + __shfl_sync(0xffffffffu, my_bias, j);
+            if (c.relu) o = fmaxf(o, 0.0f);
+            blk[j * BM + row] = o;
+          }
+          ptx::fence_proxy_async_smem();
+          epi_sync();
+          if (issuer) {
+            ptx::tma_store_3d(&tmO, blk, (int)(p0 - (int64_t)b0 * P), oc0 + cc, b0);
+            ptx::bulk_commit();
+          }
+          continue;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) blk[j * BM + row] = __uint_as_float(r[j]);
+        epi_sync();
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int jj = quarter * 8 + i, col = cc + jj;  // channel in chunk / in tile
           const float bv = __shfl_sync(0xffffffffu, my_bias, jj);
-          const float4 v = *reinterpret_cast<const float4*>(epi_stage + jj * BM + 4 * lane);
+          const float4 v = *reinterpret_cast<const float4*>(blk + jj * BM + 4 * lane);
           if (col >= q.bn) continue;
           if (un.slot >= 0) {  // K-slice partial sums: [slot][col][128 positions]
             *reinterpret_cast<float4*>(q.part + ((int64_t)un.slot * q.bn + col) * BM + 4 * lane) =
@@ -499,6 +551,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
+    if (issuer) ptx::bulk_wait_all();  // every TMA store has landed before the CTA ends
   }
 
   ptx::tc_fence_before();
@@ -509,30 +562,49 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// Adds the K-slice partial sums of the tail tiles in slice order, then bias
-// (and ReLU), and writes NCHW.  Block (tail tile tt, 4 channels), thread =
-// position row: every partial read and output write is a 128-float run.
-constexpr int TAIL_COLS = 4;
-__global__ void __launch_bounds__(BM) k_conv_tail(const ConvArgs c, const Sched q) {
-  const int groups = q.bn / TAIL_COLS;  // bn is a multiple of 16
-  const int tt = blockIdx.x / groups, col0 = (blockIdx.x - tt * groups) * TAIL_COLS;
-  const int row = threadIdx.x;
+// Adds the K-slice partial tiles of the sliced tiles in slice order, then bias
+// (and ReLU), and writes NCHW.  Thread = (tile, channel, 4 positions); the
+// slice loads are unrolled (at most 16) so that they are all in flight.
+constexpr int MAX_SLICES = 16;
+__global__ void __launch_bounds__(256) k_conv_tail(const ConvArgs c, const Sched q, int tail) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int quad = (int)(idx & 31);
+  const int64_t rest = idx >> 5;
+  const int col = (int)(rest % q.bn), tt = (int)(rest / q.bn);
+  if (tt >= tail) return;
   const int t = q.full + tt, pt = t / q.n_oc, ot = t - pt * q.n_oc;
-  const int64_t p = (int64_t)pt * BM + row;
-  if (p >= c.N) return;
-  const int P = c.OH * c.OW;
-  const int b = (int)(p / P), pix = (int)(p - (int64_t)b * P);
+  const TilePos tp = tile_pos(c, q, pt);
+  const int r0 = 4 * quad, oc = ot * q.bn + col;
+  if (r0 >= tp.count || oc >= c.OC) return;
   const int64_t per = (int64_t)q.bn * BM;
-  const float* src = q.part + ((int64_t)tt * q.slices * q.bn + col0) * BM + row;
+  const float4* src =
+      reinterpret_cast<const float4*>(q.part + ((int64_t)tt * q.slices * q.bn + col) * BM + r0);
+  float4 acc = src[0];
 #pragma unroll
-  for (int j = 0; j < TAIL_COLS; ++j) {
-    const int oc = ot * q.bn + col0 + j;
-    if (oc >= c.OC) break;
-    float acc = src[j * BM];
-    for (int sl = 1; sl < q.slices; ++sl) acc += src[sl * per + j * BM];
-    if (c.bias) acc += __ldg(c.bias + oc);
-    if (c.relu) acc = fmaxf(acc, 0.0f);
-    c.out[((int64_t)b * c.OC + oc) * P + pix] = acc;
+  for (int sl = 1; sl < MAX_SLICES; ++sl) {
+    if (sl < q.slices) {
+      const float4 v = src[sl * per / 4];
+      acc = make_float4(acc.x + v.x, acc.y + v.y, acc.z + v.z, acc.w + v.w);
+    }
+  }
+  const float bv = c.bias ? __ldg(c.bias + oc) : 0.0f;
+  float o[4] = {acc.x + bv, acc.y + bv, acc.z + bv, acc.w + bv};
+  if (c.relu) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = fmaxf(o[k], 0.0f);
+  }
+  const int64_t P = (int64_t)c.OH * c.OW, p = tp.p0 + r0, b = p / P;
+  if (c.vec_out && r0 + 3 < tp.count) {  // P % 4 == 0: p .. p+3 are in one image
+    *reinterpret_cast<float4*>(c.out + (b * c.OC + oc) * P + (p - b * P)) =
+        make_float4(o[0], o[1], o[2], o[3]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (r0 + k < tp.count) {
+        const int64_t pk = p + k, bk = pk / P;
+        c.out[(bk * c.OC + oc) * P + (pk - bk * P)] = o[k];
+      }
+    }
   }
 }
 
@@ -589,13 +661,18 @@ struct Plan {
 // fix-up launch, and the partial sums' write + read at HBM speed (one k-block
 // of MMAs takes (3 or 1) * 2 * 128 * BN * 8 / 2047 clocks at ~90 % of the
 // measured TF32 rate, at least 400: below that the gather sets the pace).
-Plan make_plan(int64_t OC, int64_t Npix, int64_t K, bool three, size_t limit) {
+Plan make_plan(const ConvArgs& c, bool three, size_t limit) {
+  const int64_t OC = c.M, Npix = c.N, K = c.K, P = (int64_t)c.OH * c.OW;
   Plan pl{};
   Sched& q = pl.q;
   q.n_oc = (int)((OC + BN_MAX - 1) / BN_MAX);
   q.bn = (int)(((OC + q.n_oc - 1) / q.n_oc + 15) / 16 * 16);
   q.kb = (int)((K + BK - 1) / BK);
-  const int64_t tiles = (Npix + BM - 1) / BM * q.n_oc;
+  // per-image tiles when that adds at most 1/16 empty positions
+  const int64_t tpi = (P + BM - 1) / BM;
+  q.tpi = (P >= BM && (tpi * BM - P) * 16 <= P) ? (int)tpi : 0;
+  const int64_t ptiles = q.tpi > 0 ? (int64_t)c.B * q.tpi : (Npix + BM - 1) / BM;
+  const int64_t tiles = ptiles * q.n_oc;
   const size_t w_bytes = (three ? 2u : 1u) * (size_t)OC * (size_t)padded_k(K) * sizeof(float);
   pl.part_off = (w_bytes + 255) / 256 * 256;
   const int64_t waves = tiles / kPlanSMs, tail = tiles - waves * kPlanSMs;
@@ -630,11 +707,27 @@ Plan make_plan(int64_t OC, int64_t Npix, int64_t K, bool three, size_t limit) {
 bool layout(Plan& pl, const ConvArgs& c, bool three) {
   Sched& q = pl.q;
   q.w_bytes = (three ? 2 : 1) * q.bn * BK * 4;
-  q.tab_bytes = (c.KH * c.KW * 8 + 127) / 128 * 128;
+  q.tab_bytes = (c.KH * c.KW * 8 + 1023) / 1024 * 1024;  // keeps the epilogue blocks 1 KB-aligned
   const int avail = SMEM_LIMIT - 1024 - q.tab_bytes - EPI_STAGE_BYTES - (int)sizeof(Ctl);
   q.stages = avail / q.w_bytes < MAX_STAGES ? avail / q.w_bytes : MAX_STAGES;
   pl.smem = 1024 + q.stages * q.w_bytes + q.tab_bytes + EPI_STAGE_BYTES + (int)sizeof(Ctl);
   return q.stages >= 3;
+}
+
+// out viewed as [B][OC][OH*OW] -> tensor map, box {128 positions, 32
+// channels, 1 image}; positions and channels past the end are not written.
+// Needs OH*OW % 4 == 0 and a 16-byte aligned out.
+bool encode_out(CUtensorMap* m, const ConvArgs& c) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t P = (cuuint64_t)c.OH * c.OW;
+  const cuuint64_t dims[3] = {P, (cuuint64_t)c.OC, (cuuint64_t)c.B};
+  const cuuint64_t strides[2] = {P * 4, P * c.OC * 4};
+  const cuuint32_t box[3] = {(cuuint32_t)BM, 32, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, c.out, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Input channel fastest in the kernel's K order (see the file comment).
@@ -644,7 +737,7 @@ constexpr int kMaxDev = 64;
 
 template <bool THREE, bool ICF>
 cudaError_t launch_main(const ConvArgs& c, const Plan& pl, const CUtensorMap& th,
-                        const CUtensorMap& tl, int grid, cudaStream_t s) {
+                        const CUtensorMap& tl, const CUtensorMap& to, int grid, cudaStream_t s) {
   static bool ready[kMaxDev];
   auto k = k_tc_conv<THREE, ICF>;
   int dev = 0;
@@ -655,7 +748,7 @@ cudaError_t launch_main(const ConvArgs& c, const Plan& pl, const CUtensorMap& th
     if (e != cudaSuccess) return e;
     if (dev < kMaxDev) ready[dev] = true;
   }
-  k<<<grid, THREADS, pl.smem, s>>>(th, tl, c, pl.q);
+  k<<<grid, THREADS, pl.smem, s>>>(th, tl, to, c, pl.q);
   return cudaGetLastError();
 }
 
@@ -667,14 +760,18 @@ cudaError_t run(const ConvArgs& c, Plan pl, const float* w_hi, const float* w_lo
       !encode_w(&tl, THREE ? w_lo : w_hi, (uint64_t)Kp, (uint64_t)c.OC, pl.q.bn))
     return cudaErrorInvalidValue;
   if (!layout(pl, c, THREE)) return cudaErrorInvalidValue;
+  CUtensorMap to;
+  pl.q.tma_out = c.vec_out && encode_out(&to, c) ? 1 : 0;  // vec_out: P % 4 == 0, aligned out
+  if (!pl.q.tma_out) to = th;                                // not read
   pl.q.part = part;
   const int sms = device_sm_count();
   const int grid = pl.q.units < sms ? pl.q.units : sms;
-  cudaError_t e = ic_fastest(c) ? launch_main<THREE, true>(c, pl, th, tl, grid, s)
-                                : launch_main<THREE, false>(c, pl, th, tl, grid, s);
+  cudaError_t e = ic_fastest(c) ? launch_main<THREE, true>(c, pl, th, tl, to, grid, s)
+                                : launch_main<THREE, false>(c, pl, th, tl, to, grid, s);
   note_launch();
   if (e != cudaSuccess || pl.tail == 0) return e;
-  k_conv_tail<<<(unsigned)(pl.tail * (pl.q.bn / TAIL_COLS)), BM, 0, s>>>(c, pl.q);
+  const int64_t threads = (int64_t)pl.tail * pl.q.bn * 32;
+  k_conv_tail<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(c, pl.q, pl.tail);
   note_launch();
   return cudaGetLastError();
 }
@@ -683,36 +780,36 @@ cudaError_t run(const ConvArgs& c, Plan pl, const float* w_hi, const float* w_lo
 
 bool tc_conv_shape_ok(const ConvArgs& c) {
   const int64_t lim30 = int64_t(1) << 30, lim31 = (int64_t(1) << 31) - 1;
-  if ((int64_t)c.KH * c.KW > MAX_TAPS) return false;
+  if ((int64_t)c.KH * c.KW > MAX_TAPS || c.K > lim31 - 8) return false;  // Kp fits an int
   if ((int64_t)(c.KH - 1) * c.dH >= lim30 || (int64_t)(c.KW - 1) * c.dW >= lim30) return false;
   if ((int64_t)c.H + 2 * (int64_t)c.pH >= lim30 || (int64_t)c.W + 2 * (int64_t)c.pW >= lim30)
     return false;
   // the running input-channel offset may pass IC by up to 17 planes
   if (((int64_t)c.IC + 17) * c.H * c.W > lim31) return false;
-  const int64_t tiles = (c.N + BM - 1) / BM * ((c.M + BN_MAX - 1) / BN_MAX);
+  // position tiles are at most one per 128 positions plus one per image
+  const int64_t tiles = ((c.N + BM - 1) / BM + c.B) * ((c.M + BN_MAX - 1) / BN_MAX);
   return tiles < lim31;
 }
 
 bool tc_conv_supported(const ConvArgs& c) { return tc_conv_shape_ok(c) && encode_fn() != nullptr; }
 
 size_t tc_conv_workspace_bytes(const ConvArgs& c, bool three_pass, size_t limit) {
-  return make_plan(c.M, c.N, c.K, three_pass, limit).bytes;
+  return make_plan(c, three_pass, limit).bytes;
 }
 
 cudaError_t launch_tc_conv(const ConvArgs& c, bool three_pass, void* workspace,
                            size_t workspace_bytes, cudaStream_t s) {
   if (!tc_conv_supported(c) || !workspace) return cudaErrorNotSupported;
-  const Plan pl = make_plan(c.M, c.N, c.K, three_pass, workspace_bytes);
+  const Plan pl = make_plan(c, three_pass, workspace_bytes);
   if (pl.bytes > workspace_bytes) return cudaErrorInvalidValue;
   const int64_t Kp = padded_k(c.K);
   float* w_hi = static_cast<float*>(workspace);
   float* w_lo = three_pass ? w_hi + c.OC * Kp : nullptr;
   float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.part_off);
-  const int64_t total = c.OC * Kp;
-  const int64_t cap = (int64_t)device_sm_count() * 8;
-  const int64_t blocks = (total + 255) / 256;
-  k_prep_w<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(
-      c.w, c.OC, c.K, Kp, c.IC, c.KH * c.KW, ic_fastest(c) ? 1 : 0, w_hi, w_lo);
+  const int gx = (int)((Kp + 255) / 256 < 64 ? (Kp + 255) / 256 : 64);
+  const int gy = (int)(c.OC < 1024 ? c.OC : 1024);
+  k_prep_w<<<dim3(gx, gy), 256, 0, s>>>(c.w, c.OC, (int)c.K, (int)Kp, c.IC, c.KH * c.KW,
+                                        ic_fastest(c) ? 1 : 0, w_hi, w_lo);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -207,10 +207,10 @@ def test_conv_argument_errors(lib):
 def test_conv_workspace_size_query(lib):
     q = binding.conv2d_gemm_f32_workspace_bytes
     body = (8, 256, 56, 56, 256, 3, 3, 1, 1, 1, 1, 1, 1)
-    # hi and lo weight planes, then the partial sums of the last wave's 44
-    # tiles (196 tiles of 128 positions on 152 SMs), each cut into 3 K-slices
-    # of a 128 x 256 fp32 tile
-    parts = 44 * 3 * 128 * 256 * 4
+    # hi and lo weight planes, then the partial sums of the last wave's 48
+    # tiles (each 56x56 image in 25 tiles of up to 128 positions: 200 tiles on
+    # 152 SMs), each cut into 3 K-slices of a 128 x 256 fp32 tile
+    parts = 48 * 3 * 128 * 256 * 4
     assert q(*body, 0) == 2 * 256 * 2304 * 4 + parts
     assert q(*body, 1) == 256 * 2304 * 4 + parts
     assert q(*body, 2) == 0

@@ -282,10 +282,12 @@ SCHED_CONV = [  # B, IC, H, W, OC, KH, KW, stride, pad, dil, channels checked (N
     (1, 4, 30, 30, 48, 3, 3, 1, 4, 4, None),
     # 1x1, K = 520 (not a multiple of 16), 290 tiles: two waves, two accumulators
     (2, 520, 136, 136, 96, 1, 1, 1, 0, 1, np.arange(0, 96, 5)),
-    # input rows staged in shared memory: 5x5 stride 2, tiles running into the next image
+    # 5x5 stride 2, tiles running into the next image
     (3, 24, 40, 40, 96, 5, 5, 2, 2, 1, None),
-    # staged, dilation 2 with padding 2
+    # dilation 2 with padding 2
     (2, 16, 32, 32, 64, 3, 3, 1, 2, 2, None),
+    # 1000 positions per image in 8 tiles each, the last one short; 24 tiles, K-sliced
+    (3, 32, 40, 25, 64, 3, 3, 1, 1, 1, None),
 ]
 
 
