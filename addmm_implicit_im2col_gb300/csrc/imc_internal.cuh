@@ -97,4 +97,24 @@ int device_sm_count();
 // Counts one kernel launch (for imc_launch_count()).
 void note_launch();
 
+// Launches `kernel` so that it may start while the previous kernel of the
+// stream (issued by the same call) is still running; the kernel calls
+// ptx::griddep_wait() before it reads that kernel's output.  Used only for a
+// call's second and later kernels.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after_previous(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace imc

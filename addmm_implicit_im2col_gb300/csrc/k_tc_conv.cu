@@ -137,6 +137,7 @@ __device__ __forceinline__ TilePos tile_pos(const ConvArgs& c, const Sched& q, i
 __global__ void __launch_bounds__(256) k_prep_w(const float* __restrict__ w, int OC, int K, int Kp,
                                                 int IC, int taps, int icf, float* __restrict__ w_hi,
                                                 float* __restrict__ w_lo) {
+  ptx::griddep_launch();  // the main kernel may start its prologue and gathers
   for (int oc = blockIdx.y; oc < OC; oc += gridDim.y) {
     const float* wr = w + (int64_t)oc * K;
     for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < Kp; k += gridDim.x * blockDim.x) {
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   // full: the 8 gather warps + the weight TMA
   if (threadIdx.x == 0) init_barriers(ctl, q.stages, GATHER_WARPS + 1, 1);
+  ptx::griddep_launch();  // the slice-sum kernel may launch (it waits for this one)
   if (warp == TMA_WARP && lane == 0) {
     ptx::tma_prefetch_desc(&tmWh);
     if (THREE) ptx::tma_prefetch_desc(&tmWl);
@@ -376,6 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == TMA_WARP) {
     // ------------------------------------------------ weight TMA producer
     if (lane == 0) {
+      ptx::griddep_wait();  // the weight planes come from the pre-pass
       int s = 0, issued = 0;
       uint32_t ph = 0;
       for (int u = blockIdx.x; u < q.units && !*abort; u += gridDim.x) {
@@ -567,6 +570,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 // slice loads are unrolled (at most 16) so that they are all in flight.
 constexpr int MAX_SLICES = 16;
 __global__ void __launch_bounds__(256) k_conv_tail(const ConvArgs c, const Sched q, int tail) {
+  ptx::griddep_wait();  // the partial tiles come from the main kernel
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int quad = (int)(idx & 31);
   const int64_t rest = idx >> 5;
@@ -748,8 +752,8 @@ cudaError_t launch_main(const ConvArgs& c, const Plan& pl, const CUtensorMap& th
     if (e != cudaSuccess) return e;
     if (dev < kMaxDev) ready[dev] = true;
   }
-  k<<<grid, THREADS, pl.smem, s>>>(th, tl, to, c, pl.q);
-  return cudaGetLastError();
+  return launch_after_previous(k, dim3(grid), dim3(THREADS), (size_t)pl.smem, s, th, tl, to, c,
+                               pl.q);
 }
 
 template <bool THREE>
@@ -771,9 +775,10 @@ cudaError_t run(const ConvArgs& c, Plan pl, const float* w_hi, const float* w_lo
   note_launch();
   if (e != cudaSuccess || pl.tail == 0) return e;
   const int64_t threads = (int64_t)pl.tail * pl.q.bn * 32;
-  k_conv_tail<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(c, pl.q, pl.tail);
+  e = launch_after_previous(k_conv_tail, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0,
+                            s, c, pl.q, pl.tail);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace

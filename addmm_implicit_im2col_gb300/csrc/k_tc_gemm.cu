@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(256) k_prep_b(const float* __restrict__ mat2, 
                                                 int64_t N, float* __restrict__ bt_hi,
                                                 float* __restrict__ bt_lo) {
   __shared__ float tile[32][33];
+  ptx::griddep_launch();  // the main kernel may start its prologue
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int64_t tiles_n = (N + 31) / 32, tiles = tiles_n * ((K + 31) / 32);
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(256) k_prep_b(const float* __restrict__ mat2, 
 // (the tensor core truncates to TF32); 3xTF32 needs only w_lo = w - tf32(w).
 __global__ void __launch_bounds__(256) k_prep_blo(const float* __restrict__ w, int64_t total,
                                                   float* __restrict__ w_lo) {
+  ptx::griddep_launch();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x)
     w_lo[i] = tf32_lo(__ldg(w + i));
@@ -179,6 +181,7 @@ struct PartStore {
 // partial tiles, always in that order (deterministic).
 __global__ void __launch_bounds__(256) k_splitk_epilogue(const float* __restrict__ part,
                                                          const int splits, const GemmArgs g) {
+  ptx::griddep_wait();  // the partials come from the main kernel
   const int64_t MN = g.M * g.N;
   if (g.vec_out) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < MN / 4;
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
   int* wd = &g_watchdog_gemm;
 
   if (threadIdx.x == 0) init_barriers(ctl, L.stages, 1, TS ? 4 : 128);
+  ptx::griddep_launch();  // the split-K sum kernel may launch (it waits for this one)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmBh);
@@ -252,6 +256,7 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
+      ptx::griddep_wait();  // mat2^T (or w_lo) comes from the pre-pass
       const uint32_t tx = (uint32_t)(A_BYTES + (THREE ? 2 : 1) * bn * BK * 4);
       int s = 0, issued = 0;
       uint32_t ph = 0;
@@ -560,9 +565,11 @@ size_t plan_bytes(const Plan& p, int64_t M, int64_t N) {
 
 constexpr int kMaxDev = 64;
 
+// after_prep: a pre-pass of this call ran just before (the main kernel may
+// then start early and waits for it before loading B).
 template <bool THREE, bool TS>
 cudaError_t run(const GemmArgs& g, const Plan& p, const float* bt_hi, const float* bt_lo,
-                float* part, cudaStream_t s) {
+                float* part, bool after_prep, cudaStream_t s) {
   constexpr int smem = smem_bytes(TS ? kLts : (THREE ? kL3 : kL1));
   static bool ready[kMaxDev];
   auto k = k_tc_gemm<THREE, TS>;
@@ -584,16 +591,23 @@ cudaError_t run(const GemmArgs& g, const Plan& p, const float* bt_hi, const floa
   const int grid = units < sms ? units : sms;
   const int group = pick_group(p.num_m, p.num_n, kPlanSMs, (double)g.M * g.K * 4.0,
                                (THREE ? 8.0 : 4.0) * (double)g.N * g.K);
-  k<<<grid, THREE ? 320 : 192, smem, s>>>(ta, tbh, tbl, g, p.num_m, p.num_n, group, p.bn,
-                                          p.splits, p.kps, part);
+  const dim3 block(THREE ? 320 : 192);
+  if (after_prep) {
+    e = launch_after_previous(k, dim3(grid), block, (size_t)smem, s, ta, tbh, tbl, g, p.num_m,
+                              p.num_n, group, p.bn, p.splits, p.kps, part);
+  } else {
+    k<<<grid, block, smem, s>>>(ta, tbh, tbl, g, p.num_m, p.num_n, group, p.bn, p.splits, p.kps,
+                                part);
+    e = cudaGetLastError();
+  }
   note_launch();
-  e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1) return e;
   const int64_t items = g.vec_out ? g.M * g.N / 4 : g.M * g.N;
   const int64_t cap = (int64_t)sms * 8, blocks = (items + 255) / 256;
-  k_splitk_epilogue<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(part, p.splits, g);
+  e = launch_after_previous(k_splitk_epilogue, dim3((unsigned)(blocks < cap ? blocks : cap)),
+                            dim3(256), 0, s, (const float*)part, p.splits, g);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
@@ -620,9 +634,11 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
   float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.part_offset);
   const float *b_hi, *b_lo;
   const int64_t cap = (int64_t)device_sm_count() * 8;
+  bool prep = true;
   if (g.b_kmajor) {  // w[N,K] is B_hi; 3xTF32 adds w_lo in the scratch
     b_hi = g.mat2;
     b_lo = three_pass ? ws : nullptr;
+    prep = three_pass;
     if (three_pass) {
       const int64_t total = g.N * g.K, blocks = (total + 255) / 256;
       k_prep_blo<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(g.mat2, total, ws);
@@ -638,9 +654,9 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (!three_pass) return run<false, false>(g, p, b_hi, nullptr, part, s);
-  return p.kps >= kTsMinKb ? run<true, true>(g, p, b_hi, b_lo, part, s)
-                           : run<true, false>(g, p, b_hi, b_lo, part, s);
+  if (!three_pass) return run<false, false>(g, p, b_hi, nullptr, part, prep, s);
+  return p.kps >= kTsMinKb ? run<true, true>(g, p, b_hi, b_lo, part, prep, s)
+                           : run<true, false>(g, p, b_hi, b_lo, part, prep, s);
 }
 
 cudaError_t gemm_take_watchdog(int* value) {

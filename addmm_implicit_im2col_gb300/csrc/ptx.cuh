@@ -70,6 +70,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------------- dependent grid launches
+// A kernel launched with cudaLaunchAttributeProgrammaticStreamSerialization
+// may start while the previous kernel of its stream is still running:
+// griddep_wait() blocks until that kernel has completed and its writes are
+// visible (a no-op for a kernel launched without the attribute), and
+// griddep_launch() in the running kernel lets such a next kernel launch.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
