@@ -26,8 +26,8 @@
 //               memory) and has one accumulator, the other form reads the raw
 //               mat1 tile as A_hi (the tensor core drops the 13 low mantissa
 //               bits itself) and double-buffers the accumulator.  The TS form
-//               is used when a unit runs at least kTsMinKb k-blocks, where the
-//               faster MMAs outweigh the drain of the single accumulator
+//               is used when a unit runs enough k-blocks that the faster MMAs
+//               outweigh the drain of the single accumulator (see kTsMinKb)
 //   warps 2-5   epilogue: tcgen05.ld, 32x32 transpose through shared memory,
 //               beta*self + alpha*acc, 16-byte row-segment stores
 //
@@ -70,8 +70,10 @@ static_assert(kL1.stages <= MAX_STAGES, "stages");
 constexpr uint32_t TS_A_COL0 = 256, TS_A_STAGE_COLS = 32;
 static_assert(TS_A_COL0 + kLts.stages * TS_A_STAGE_COLS <= TMEM_COLS, "TMEM");
 // K-blocks per unit from which the A-from-TMEM form is used: it runs the MMAs
-// faster but holds the MMA while the single accumulator drains.
-constexpr int kTsMinKb = 96;
+// faster but holds the MMA while the single accumulator drains, which is slow
+// when the epilogue reads an [M,N] self (measured on 32768x1024x1024: 305 us
+// with the double-buffered form, 443 us with this one), cheap otherwise.
+constexpr int kTsMinKb = 96, kTsMinKbLightEpilogue = 32;
 
 __device__ int g_watchdog_gemm;
 
@@ -655,8 +657,10 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (!three_pass) return run<false, false>(g, p, b_hi, nullptr, part, prep, s);
-  return p.kps >= kTsMinKb ? run<true, true>(g, p, b_hi, b_lo, part, prep, s)
-                           : run<true, false>(g, p, b_hi, b_lo, part, prep, s);
+  const bool light = !(g.read_self && g.self_2d) || p.splits > 1;  // no [M,N] self read per tile
+  const bool ts = p.kps >= kTsMinKb || (light && p.kps >= kTsMinKbLightEpilogue);
+  return ts ? run<true, true>(g, p, b_hi, b_lo, part, prep, s)
+            : run<true, false>(g, p, b_hi, b_lo, part, prep, s);
 }
 
 cudaError_t gemm_take_watchdog(int* value) {
