@@ -346,10 +346,20 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
     for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++tl) {
       const int buf = tl % NACC;
       const uint32_t use = (uint32_t)(tl / NACC);
-      if (!warp_wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd)) break;
-      ptx::tc_fence_after();
       int mt, nt;
       tile_coords(u % num_tiles, num_m, num_n, group, mt, nt);
+      if (g.read_self && g.self_2d && splits == 1) {
+        // while the tile's MMAs run: pull its [M,N] self rows into L2 (one row
+        // of up to BN floats per thread, 128-byte lines)
+        const int64_t m = (int64_t)mt * BM + (warp - 2) * 32 + lane, n0 = (int64_t)nt * bn;
+        if (m < g.M) {
+          const float* row = g.self + m * g.N + n0;
+          const int64_t cols = g.N - n0 < bn ? g.N - n0 : bn;
+          for (int64_t c = 0; c < cols; c += 32) ptx::prefetch_l2(row + c);
+        }
+      }
+      if (!warp_wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd)) break;
+      ptx::tc_fence_after();
       // the single accumulator is handed back as soon as it is read
       uint64_t* early = TS ? &ctl->acce[buf] : nullptr;
       if (splits == 1)
