@@ -161,11 +161,17 @@ __global__ void k_fill_conv(const ConvArgs c) {
 
 // Direct convolution (the conv page's Problem paragraph: one thread per output
 // element re-reading its receptive field from global memory, no reuse across
-// threads).  Consecutive threads take consecutive ow, so output stores and
-// input loads along a row are coalesced.  fp32 FMA in (ic, kh, kw) order.
+// threads; its "Before" line: scalar, or vec4 over the input channels when
+// their count is a multiple of 4).  Consecutive threads take consecutive ow,
+// so output stores and input loads along a row are coalesced.  fp32 FMA in
+// (ic, kh, kw) order; the VEC4 form adds, per tap, the 4-term dot product of
+// channels ic .. ic+3 (in NCHW / OIHW those are a plane apart, so the loads
+// stay scalar).
+template <bool VEC4>
 __global__ void __launch_bounds__(256) k_direct_conv(const ConvArgs c) {
   const int64_t P = (int64_t)c.OH * c.OW;
   const int64_t total = (int64_t)c.B * c.OC * P;
+  const int64_t HW = (int64_t)c.H * c.W, taps = (int64_t)c.KH * c.KW;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int ow = (int)(e % c.OW);
@@ -174,18 +180,27 @@ __global__ void __launch_bounds__(256) k_direct_conv(const ConvArgs c) {
     const int64_t u = t / c.OH;
     const int oc = (int)(u % c.OC);
     const int b = (int)(u / c.OC);
-    const float* xb = c.x + (int64_t)b * c.IC * c.H * c.W;
+    const float* xb = c.x + (int64_t)b * c.IC * HW;
     const float* wr = c.w + (int64_t)oc * c.K;
     float acc = 0.0f;
-    for (int ic = 0; ic < c.IC; ++ic)
+    for (int ic = 0; ic < c.IC; ic += VEC4 ? 4 : 1)
       for (int kh = 0; kh < c.KH; ++kh) {
         const int ih = oh * c.sH - c.pH + kh * c.dH;
         if (ih < 0 || ih >= c.H) continue;
         for (int kw = 0; kw < c.KW; ++kw) {
           const int iw = ow * c.sW - c.pW + kw * c.dW;
           if (iw < 0 || iw >= c.W) continue;
-          acc = fmaf(__ldg(wr + (ic * c.KH + kh) * c.KW + kw),
-                     __ldg(xb + ((int64_t)ic * c.H + ih) * c.W + iw), acc);
+          const float* wp = wr + (ic * c.KH + kh) * c.KW + kw;
+          const float* xp = xb + ic * HW + (int64_t)ih * c.W + iw;
+          if (VEC4) {  // the 4 channels ic .. ic+3 as one 4-term dot product
+            float d = __ldg(wp) * __ldg(xp);
+            d = fmaf(__ldg(wp + taps), __ldg(xp + HW), d);
+            d = fmaf(__ldg(wp + 2 * taps), __ldg(xp + 2 * HW), d);
+            d = fmaf(__ldg(wp + 3 * taps), __ldg(xp + 3 * HW), d);
+            acc += d;
+          } else {
+            acc = fmaf(__ldg(wp), __ldg(xp), acc);
+          }
         }
       }
     const float v = acc + (c.bias ? __ldg(c.bias + oc) : 0.0f);
@@ -234,7 +249,11 @@ cudaError_t launch_fill_gemm(const GemmArgs& a, cudaStream_t s) {
 cudaError_t launch_direct_conv(const ConvArgs& c, cudaStream_t s) {
   const int64_t total = (int64_t)c.B * c.OC * c.OH * c.OW;
   const int64_t cap = (int64_t)device_sm_count() * 16, blocks = (total + 255) / 256;
-  k_direct_conv<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(c);
+  // as in the pages' direct kernel: the 4-channel form when IC % 4 == 0
+  if (c.IC % 4 == 0)
+    k_direct_conv<true><<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(c);
+  else
+    k_direct_conv<false><<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(c);
   note_launch();
   return cudaGetLastError();
 }

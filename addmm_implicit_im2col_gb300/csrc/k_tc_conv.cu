@@ -179,22 +179,6 @@ __device__ __forceinline__ bool rotate3(int nkb, Gather& gather, Store& store) {
   return true;
 }
 
-// Named barrier 1 over the four epilogue warps; epi_any also ORs a flag
-// across them (so that they leave their loop together).
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ bool epi_any(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v)
-      : "memory");
-  return r != 0;
-}
-
 // ------------------------------------------------------------ main kernel
 template <bool THREE, bool ICF>
 __global__ void __launch_bounds__(THREADS, 1)

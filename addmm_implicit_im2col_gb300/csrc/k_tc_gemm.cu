@@ -52,6 +52,8 @@ constexpr int A_BYTES = BM * BK * 4;      // 8 KB
 constexpr int B_BYTES = BN_MAX * BK * 4;  // 16 KB
 constexpr uint32_t ACC_STRIDE = 256;      // TMEM columns between the two accumulators
 
+constexpr int SROW_BYTES = BN_MAX * 4;  // beta * self[n0 ..) of the tile, for a vector self
+
 struct Layout {
   int a, a_lo, b_hi, b_lo, bytes, stages;
 };
@@ -60,7 +62,7 @@ constexpr Layout kL1 = {0, 0, A_BYTES, 0, A_BYTES + B_BYTES, 8};
 // 3xTF32 with A from TMEM: no A_lo tile in shared memory
 constexpr Layout kLts = {0, 0, A_BYTES, A_BYTES + B_BYTES, A_BYTES + 2 * B_BYTES, 5};
 constexpr int smem_bytes(const Layout& L) {
-  return 1024 + L.stages * L.bytes + EPI_BYTES + (int)sizeof(Ctl);
+  return 1024 + L.stages * L.bytes + EPI_BYTES + SROW_BYTES + (int)sizeof(Ctl);
 }
 static_assert(smem_bytes(kL3) <= 232448 && smem_bytes(kL1) <= 232448 &&
                   smem_bytes(kLts) <= 232448, "shared memory");
@@ -127,6 +129,7 @@ __global__ void __launch_bounds__(256) k_prep_blo(const float* __restrict__ w, i
 struct Store {
   const GemmArgs& g;
   int64_t m0, n0;
+  const float* srow;  // beta * self[n0 + c] in shared memory (vector self), else nullptr
   // beta * self for the segment (row r, columns c .. c+3 of the tile), read
   // before any output of the block is written (out may be self: each element
   // is read before its own write).
@@ -134,6 +137,7 @@ struct Store {
     const int64_t m = m0 + r, n = n0 + c;
     float4 sv = make_float4(0.f, 0.f, 0.f, 0.f);
     if (!g.read_self || m >= g.M || n >= g.N) return sv;
+    if (srow) return *reinterpret_cast<const float4*>(srow + c);
     const float* sp = g.self + (g.self_2d ? m * g.N : 0) + n;
     if (g.vec_out) {
       sv = *reinterpret_cast<const float4*>(sp);  // plain load: self may be out
@@ -229,7 +233,8 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   float* epi = reinterpret_cast<float*>(smem + L.stages * L.bytes);
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + L.stages * L.bytes + EPI_BYTES);
+  float* srow = reinterpret_cast<float*>(smem + L.stages * L.bytes + EPI_BYTES);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + L.stages * L.bytes + EPI_BYTES + SROW_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Work unit u = (tile u % num_tiles, K-slice u / num_tiles); a slice covers
   // k-blocks [slice*kps, min(num_kb, (slice+1)*kps)).  splits == 1: whole K.
@@ -358,13 +363,25 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
           for (int64_t c = 0; c < cols; c += 32) ptx::prefetch_l2(row + c);
         }
       }
-      if (!warp_wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd)) break;
+      // A vector self is the same for every row of the tile: beta * self of the
+      // tile's columns goes to shared memory while its MMAs run.
+      const bool vec_self = g.read_self && !g.self_2d && splits == 1;
+      if (vec_self) {
+        epi_sync();  // the previous tile's drain has read the row
+        const int64_t n0 = (int64_t)nt * bn;
+        for (int c = (warp - 2) * 32 + lane; c < bn; c += 128)
+          srow[c] = n0 + c < g.N ? g.beta * g.self[n0 + c] : 0.0f;
+        epi_sync();
+      }
+      const bool ok = warp_wait_bar(&ctl->accf[buf], use & 1u, abort, kSiteEpilogueAccFull, wd);
+      if (epi_any(!ok)) break;
       ptx::tc_fence_after();
       // the single accumulator is handed back as soon as it is read
       uint64_t* early = TS ? &ctl->acce[buf] : nullptr;
       if (splits == 1)
         drain_accumulator(tmem, q, (uint32_t)buf * ACC_STRIDE, bn, stage,
-                          Store{g, (int64_t)mt * BM, (int64_t)nt * bn}, early);
+                          Store{g, (int64_t)mt * BM, (int64_t)nt * bn, vec_self ? srow : nullptr},
+                          early);
       else
         drain_accumulator(tmem, q, (uint32_t)buf * ACC_STRIDE, bn, stage,
                           PartStore{part + (int64_t)(u / num_tiles) * g.M * g.N, g.M, g.N,

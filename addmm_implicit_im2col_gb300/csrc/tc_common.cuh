@@ -77,6 +77,22 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Named barrier 1 over the four epilogue warps; epi_any also ORs a flag
+// across them (so that they leave their loop together).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void init_barriers(Ctl* ctl, int stages, uint32_t full_count,
                                               uint32_t split_count) {
   for (int s = 0; s < stages; ++s) {

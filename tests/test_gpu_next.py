@@ -110,11 +110,12 @@ def test_conv_relu(mode):
     within(out.cpu().numpy(), np.maximum(ref, 0.0), S, TOL[mode], f"conv relu {mode}")
 
 
-DIRECT = [  # B, IC, H, W, OC, KH, KW, stride, pad, dil
+DIRECT = [  # B, IC, H, W, OC, KH, KW, stride, pad, dil (IC % 4 == 0: the 4-channel form)
     (2, 3, 9, 9, 4, 3, 3, 1, 1, 1),
     (1, 3, 64, 64, 128, 7, 7, 4, 3, 1),
     (2, 32, 14, 14, 64, 3, 3, 1, 2, 2),
     (1, 5, 12, 40, 36, 3, 2, (2, 3), (1, 0), (1, 2)),
+    (1, 8, 12, 40, 20, 3, 2, (2, 3), (1, 0), (1, 2)),
 ]
 
 
