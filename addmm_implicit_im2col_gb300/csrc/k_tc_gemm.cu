@@ -165,6 +165,51 @@ struct Store {
   }
 };
 
+// Drains a tile by TMA stores (whole-tile units, no [M,N] self, aligned out
+// with N % 4 == 0): per 32-column chunk each warp computes alpha*acc +
+// beta*self (+ ReLU) for its 32 rows, writes them to its 4 KB block of shared
+// memory in the 128-byte swizzled layout (row r, 16-byte unit u at
+// r*128 + ((u ^ (r % 8)) * 16)), and lane 0 stores the 32 x 32 block with one
+// 2-D tensor store.  `srow` holds beta * self of the tile's columns (nullptr:
+// no self).  The accumulator is released after its last TMEM load.
+__device__ __forceinline__ void drain_tma(uint32_t tmem, int q, int bn, uint8_t* blk,
+                                          const CUtensorMap* tm_out, const GemmArgs& g,
+                                          int64_t m0, int64_t n0, const float* srow,
+                                          uint64_t* release) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+  for (int c = 0; c < bn; c += 32) {
+    uint32_t v[32];
+    ptx::tmem_ld32(tbase + (uint32_t)c, v);
+    ptx::tmem_ld_wait();
+    if (release && c + 32 >= bn) {
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(release);
+    }
+    if (lane == 0) ptx::bulk_wait_read0();  // the previous chunk's store has read the block
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float4 s4 = srow ? *reinterpret_cast<const float4*>(srow + c + 4 * u)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 o = make_float4(fmaf(g.alpha, __uint_as_float(v[4 * u]), s4.x),
+                             fmaf(g.alpha, __uint_as_float(v[4 * u + 1]), s4.y),
+                             fmaf(g.alpha, __uint_as_float(v[4 * u + 2]), s4.z),
+                             fmaf(g.alpha, __uint_as_float(v[4 * u + 3]), s4.w));
+      if (g.relu)
+        o = make_float4(fmaxf(o.x, 0.f), fmaxf(o.y, 0.f), fmaxf(o.z, 0.f), fmaxf(o.w, 0.f));
+      *reinterpret_cast<float4*>(blk + lane * 128 + ((u ^ (lane & 7)) << 4)) = o;
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_2d(tm_out, blk, (int)(n0 + c), (int)(m0 + q * 32));
+      ptx::bulk_commit();
+    }
+  }
+}
+
 // Split-K: a unit's raw partial tile goes to part[slice][M][N].
 struct PartStore {
   float* p;
@@ -224,7 +269,8 @@ __global__ void __launch_bounds__(256) k_splitk_epilogue(const float* __restrict
 template <bool THREE, bool TS>
 __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBh,
-              const __grid_constant__ CUtensorMap tmBl, const GemmArgs g, const int num_m,
+              const __grid_constant__ CUtensorMap tmBl, const __grid_constant__ CUtensorMap tmOut,
+              const int tma_out, const GemmArgs g, const int num_m,
               const int num_n, const int group, const int bn, const int splits, const int kps,
               float* __restrict__ part) {
   static_assert(!TS || THREE, "the A-from-TMEM form is 3xTF32");
@@ -378,7 +424,10 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
       ptx::tc_fence_after();
       // the single accumulator is handed back as soon as it is read
       uint64_t* early = TS ? &ctl->acce[buf] : nullptr;
-      if (splits == 1)
+      if (tma_out && splits == 1 && !(g.read_self && g.self_2d))
+        drain_tma(tmem + (uint32_t)buf * ACC_STRIDE, q, bn, reinterpret_cast<uint8_t*>(epi) + (warp - 2) * 4096,
+                  &tmOut, g, (int64_t)mt * BM, (int64_t)nt * bn, vec_self ? srow : nullptr, early);
+      else if (splits == 1)
         drain_accumulator(tmem, q, (uint32_t)buf * ACC_STRIDE, bn, stage,
                           Store{g, (int64_t)mt * BM, (int64_t)nt * bn, vec_self ? srow : nullptr},
                           early);
@@ -392,6 +441,7 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
         ptx::mbar_arrive(&ctl->acce[buf]);
       }
     }
+    if (lane == 0) ptx::bulk_wait_all();  // every TMA store has landed before the CTA ends
   } else if (TS) {
     // ------------------------------- split warps: A_hi / A_lo into TMEM
     // Thread = row r of the A tile (TMEM lane r): its 16 values of a k-block
@@ -540,6 +590,20 @@ int pick_group(int64_t num_m, int64_t num_n, int sms, double a_bytes, double b_b
   return best;
 }
 
+// out [M, N] -> tensor map with a {32, 32} box, 128-byte swizzle (the
+// epilogue's staging layout); rows and columns past the end are not written.
+bool encode_out(CUtensorMap* m, const GemmArgs& g) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)g.N, (cuuint64_t)g.M};
+  const cuuint64_t strides[1] = {(cuuint64_t)g.N * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, g.out, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Launch plan.  It depends on the problem only (not on the device), so the
 // scratch size can be queried before a device is chosen; kPlanSMs is the SM
 // count of the GB300 it is tuned for.
@@ -621,12 +685,16 @@ cudaError_t run(const GemmArgs& g, const Plan& p, const float* bt_hi, const floa
   const int group = pick_group(p.num_m, p.num_n, kPlanSMs, (double)g.M * g.K * 4.0,
                                (THREE ? 8.0 : 4.0) * (double)g.N * g.K);
   const dim3 block(THREE ? 320 : 192);
+  // whole-tile units leave by TMA store when out allows it (N % 4 == 0, aligned)
+  CUtensorMap tout;
+  const int tma_out = p.splits == 1 && g.vec_out && encode_out(&tout, g) ? 1 : 0;
+  if (!tma_out) tout = ta;  // not read
   if (after_prep) {
-    e = launch_after_previous(k, dim3(grid), block, (size_t)smem, s, ta, tbh, tbl, g, p.num_m,
-                              p.num_n, group, p.bn, p.splits, p.kps, part);
+    e = launch_after_previous(k, dim3(grid), block, (size_t)smem, s, ta, tbh, tbl, tout, tma_out,
+                              g, p.num_m, p.num_n, group, p.bn, p.splits, p.kps, part);
   } else {
-    k<<<grid, block, smem, s>>>(ta, tbh, tbl, g, p.num_m, p.num_n, group, p.bn, p.splits, p.kps,
-                                part);
+    k<<<grid, block, smem, s>>>(ta, tbh, tbl, tout, tma_out, g, p.num_m, p.num_n, group, p.bn,
+                                p.splits, p.kps, part);
     e = cudaGetLastError();
   }
   note_launch();

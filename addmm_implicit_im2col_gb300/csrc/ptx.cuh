@@ -115,6 +115,19 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, 
       "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// 2-D tiled bulk tensor store shared -> global (x innermost), likewise.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* src, int32_t x,
+                                             int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          tmap),
+      "r"(smem_addr(src)), "r"(x), "r"(y)
+      : "memory");
+}
+// Waits until none of this thread's bulk groups still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
