@@ -117,6 +117,48 @@ __global__ void __launch_bounds__(256) k_prep_b(const float* __restrict__ mat2, 
 
 // linear: the weight w[N,K] is already K-major and serves as B_hi as it is
 // (the tensor core truncates to TF32); 3xTF32 needs only w_lo = w - tf32(w).
+// The same for N % 4 == 0 and a 16-byte aligned mat2 (K % 4 == 0 on this
+// path): 64 x 64 tiles, 16-byte loads along N and 16-byte stores along K.
+__global__ void __launch_bounds__(256) k_prep_b4(const float* __restrict__ mat2, int64_t K,
+                                                 int64_t N, float* __restrict__ bt_hi,
+                                                 float* __restrict__ bt_lo) {
+  __shared__ float tile[64][65];
+  ptx::griddep_launch();  // the main kernel may start its prologue
+  const int t = threadIdx.x, r0 = t >> 4, q4 = t & 15;
+  const int64_t tiles_n = (N + 63) / 64, tiles = tiles_n * ((K + 63) / 64);
+  for (int64_t tt = blockIdx.x; tt < tiles; tt += gridDim.x) {
+    const int64_t k0 = (tt / tiles_n) * 64, n0 = (tt % tiles_n) * 64;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // rows k0 + r, columns n0 + 4*q4 .. +3
+      const int r = r0 + 16 * i;
+      const int64_t k = k0 + r, n = n0 + 4 * q4;
+      const float4 v = (k < K && n < N) ? __ldg(reinterpret_cast<const float4*>(mat2 + k * N + n))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      tile[r][4 * q4] = v.x;
+      tile[r][4 * q4 + 1] = v.y;
+      tile[r][4 * q4 + 2] = v.z;
+      tile[r][4 * q4 + 3] = v.w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // output rows n0 + r, columns k0 + 4*q4 .. +3
+      const int r = r0 + 16 * i;
+      const int64_t n = n0 + r, k = k0 + 4 * q4;
+      if (n < N && k < K) {
+        const float4 v = make_float4(tile[4 * q4][r], tile[4 * q4 + 1][r], tile[4 * q4 + 2][r],
+                                     tile[4 * q4 + 3][r]);
+        if (bt_lo) {
+          *reinterpret_cast<float4*>(bt_hi + n * K + k) = tf32_hi4(v);
+          *reinterpret_cast<float4*>(bt_lo + n * K + k) = tf32_lo4(v);
+        } else {
+          *reinterpret_cast<float4*>(bt_hi + n * K + k) = v;
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
 __global__ void __launch_bounds__(256) k_prep_blo(const float* __restrict__ w, int64_t total,
                                                   float* __restrict__ w_lo) {
   ptx::griddep_launch();
@@ -744,9 +786,15 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
   } else {  // transpose mat2[K,N] into Bt_hi[N,K] (+ Bt_lo)
     b_hi = ws;
     b_lo = three_pass ? ws + g.N * g.K : nullptr;
-    const int64_t tiles = ((g.N + 31) / 32) * ((g.K + 31) / 32);
-    k_prep_b<<<(unsigned)(tiles < cap ? tiles : cap), dim3(32, 8), 0, s>>>(
-        g.mat2, g.K, g.N, ws, three_pass ? ws + g.N * g.K : nullptr);
+    if (g.N % 4 == 0 && (reinterpret_cast<uintptr_t>(g.mat2) & 15u) == 0) {
+      const int64_t tiles = ((g.N + 63) / 64) * ((g.K + 63) / 64);
+      k_prep_b4<<<(unsigned)(tiles < cap ? tiles : cap), 256, 0, s>>>(
+          g.mat2, g.K, g.N, ws, three_pass ? ws + g.N * g.K : nullptr);
+    } else {
+      const int64_t tiles = ((g.N + 31) / 32) * ((g.K + 31) / 32);
+      k_prep_b<<<(unsigned)(tiles < cap ? tiles : cap), dim3(32, 8), 0, s>>>(
+          g.mat2, g.K, g.N, ws, three_pass ? ws + g.N * g.K : nullptr);
+    }
     note_launch();
   }
   cudaError_t e = cudaGetLastError();
