@@ -91,22 +91,24 @@ def test_addmm_integer_inputs_are_bit_exact(mode, mnk):
 
 def test_addmm_long_k_tile_path():
     # 160 output tiles of 128 x 256 and 96 k-blocks of 16 per tile: the form of
-    # the 3xTF32 kernel that keeps A in tensor memory and one accumulator
+    # the 3xTF32 kernel that keeps A in tensor memory and one accumulator; the
+    # single-product modes run the shared-memory form on the same shape
     M, N, K = 2560, 2048, 1536
     rows = synth.sample_rows(synth.stream_key(0, 30, 9), M, 192)
     for self_2d, alpha, beta in [(False, 1.0, 1.0), (True, -0.5, 2.0)]:
         s, a, b = synth.addmm_inputs(M, N, K, self_2d=self_2d, workload=30 + self_2d,
                                      mat1=("N", 0.0, 1.0), mat2=("N", 0.0, 1.0 / np.sqrt(K)),
                                      self_=("N", 0.0, 1.0))
-        for mode in ("default", "force_tc3"):
+        for mode in ("default", "force_tc3", "tf32", "force_tc1"):
             got, ref, S, kern = run_addmm(s, a, b, beta, alpha, mode, rows=rows)
-            assert kern == "tc3"
-            within(got, ref, S, 1e-5, f"long-K {mode} self_2d={self_2d}")
+            assert kern == ("tc1" if mode in ("tf32", "force_tc1") else "tc3")
+            within(got, ref, S, TOL[mode], f"long-K {mode} self_2d={self_2d}")
     spec = ("I", -2, 2)
     s, a, b = synth.addmm_inputs(M, N, K, self_2d=True, workload=32, mat1=spec, mat2=spec,
                                  self_=spec)
-    got, ref, _, kern = run_addmm(s, a, b, 1.0, 1.0, "force_tc3", rows=rows)
-    assert np.array_equal(got.astype(np.float64), ref)
+    for mode in ("force_tc3", "force_tc1"):
+        got, ref, _, _ = run_addmm(s, a, b, 1.0, 1.0, mode, rows=rows)
+        assert np.array_equal(got.astype(np.float64), ref), mode
 
 
 def test_addmm_k_not_multiple_of_4_takes_simt():
