@@ -51,11 +51,15 @@ SIGNATURES = {
     "linear_f32": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]),
     "linear_f32_ws": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, ctypes.c_size_t, _vp]),
     "linear_f32_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64, _int]),
+    "gemm_addmm_f32_host": (_int, [_vp, _int, _vp, _vp, _vp, _i64, _i64, _i64, _dbl, _dbl, _int,
+                                   _vp]),
+    "conv2d_gemm_f32_host": (_int, [_vp, _vp, _vp, _vp] + [_i64] * 13 + [_int, _vp]),
     "imc_status_string": (ctypes.c_char_p, [_int]),
     "imc_last_kernel": (_int, []),
     "imc_launch_count": (ctypes.c_uint64, []),
     "imc_check_device_error": (_int, [_vp]),
     "imc_version": (_int, []),
+    "imc_release_memory": (_int, []),
 }
 
 _lock = threading.Lock()
@@ -157,6 +161,22 @@ def linear_f32_workspace_bytes(M, N, K, mode) -> int:
     return int(load().linear_f32_workspace_bytes(M, N, K, mode))
 
 
+def gemm_addmm_f32_host(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode,
+                        stream) -> int:
+    return load().gemm_addmm_f32_host(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode,
+                                      stream)
+
+
+def conv2d_gemm_f32_host(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, mode,
+                         stream) -> int:
+    return load().conv2d_gemm_f32_host(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW,
+                                       dH, dW, mode, stream)
+
+
+def release_memory() -> int:
+    return load().imc_release_memory()
+
+
 def status_string(status: int) -> str:
     return load().imc_status_string(status).decode()
 
@@ -183,14 +203,16 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
-def _check_tensor(t, name, ndim=None):
+def _check_tensor(t, name, ndim=None, host=False):
     import torch
     if t is None:
         return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    where = "CPU" if host else "CUDA"
+    placed = t.device.type == "cpu" if host else t.is_cuda
+    if not placed or t.dtype != torch.float32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 {where} tensor")
     if ndim is not None and t.dim() not in ndim:
         raise ValueError(f"{name} must have {ndim} dimensions")
 
@@ -199,17 +221,10 @@ def _mode(mode, relu):
     return MODES[mode] | (ACT_RELU if relu else 0)
 
 
-def addmm(self, mat1, mat2, *, beta=1.0, alpha=1.0, mode="default", relu=False, out=None):
-    """out = beta*self + alpha*(mat1 @ mat2) on the GPU (aten.addmm semantics).
-
-    self is [N] or [M, N]; alpha and beta default to 1.0.  ``mode`` is one of
-    ``MODES``; ``relu`` fuses max(v, 0) into the epilogue.  Returns ``out``
-    (allocated with torch when not given).
-    """
-    import torch
-    _check_tensor(mat1, "mat1", (2,))
-    _check_tensor(mat2, "mat2", (2,))
-    _check_tensor(self, "self", (1, 2))
+def _addmm_dims(self, mat1, mat2, host):
+    _check_tensor(mat1, "mat1", (2,), host)
+    _check_tensor(mat2, "mat2", (2,), host)
+    _check_tensor(self, "self", (1, 2), host)
     M, K = mat1.shape
     K2, N = mat2.shape
     if K2 != K:
@@ -222,6 +237,18 @@ def addmm(self, mat1, mat2, *, beta=1.0, alpha=1.0, mode="default", relu=False, 
             self_2d = 1
         elif self.shape[0] != N:
             raise ValueError("a 1-D self must be [N]")
+    return M, N, K, self_2d
+
+
+def addmm(self, mat1, mat2, *, beta=1.0, alpha=1.0, mode="default", relu=False, out=None):
+    """out = beta*self + alpha*(mat1 @ mat2) on the GPU (aten.addmm semantics).
+
+    self is [N] or [M, N]; alpha and beta default to 1.0.  ``mode`` is one of
+    ``MODES``; ``relu`` fuses max(v, 0) into the epilogue.  Returns ``out``
+    (allocated with torch when not given).
+    """
+    import torch
+    M, N, K, self_2d = _addmm_dims(self, mat1, mat2, host=False)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=mat1.device)
     else:
@@ -274,17 +301,10 @@ def _pair(v):
     return (int(v[0]), int(v[1])) if isinstance(v, (tuple, list)) else (int(v), int(v))
 
 
-def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, *, mode="default", relu=False,
-           out=None):
-    """groups==1 NCHW conv2d via the implicit-im2col GEMM.
-
-    x [B, IC, H, W], w [OC, IC, KH, KW], bias [OC] or None; stride, padding and
-    dilation are ints or (h, w) pairs.  Returns out [B, OC, OH, OW].
-    """
-    import torch
-    _check_tensor(x, "x", (4,))
-    _check_tensor(w, "w", (4,))
-    _check_tensor(bias, "bias", (1,))
+def _conv_dims(x, w, bias, stride, padding, dilation, host):
+    _check_tensor(x, "x", (4,), host)
+    _check_tensor(w, "w", (4,), host)
+    _check_tensor(bias, "bias", (1,), host)
     B, IC, H, W = x.shape
     OC, IC2, KH, KW = w.shape
     if IC2 != IC:
@@ -298,6 +318,19 @@ def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, *, mode="default", 
     OW = conv_out_size(W, KW, sW, pW, dW)
     if OH < 1 or OW < 1:
         raise ValueError("empty convolution output")
+    return B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, OH, OW
+
+
+def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, *, mode="default", relu=False,
+           out=None):
+    """groups==1 NCHW conv2d via the implicit-im2col GEMM.
+
+    x [B, IC, H, W], w [OC, IC, KH, KW], bias [OC] or None; stride, padding and
+    dilation are ints or (h, w) pairs.  Returns out [B, OC, OH, OW].
+    """
+    import torch
+    B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, OH, OW = _conv_dims(
+        x, w, bias, stride, padding, dilation, host=False)
     if out is None:
         out = torch.empty((B, OC, OH, OW), dtype=torch.float32, device=x.device)
     else:
@@ -310,4 +343,49 @@ def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, *, mode="default", 
                             _stream_ptr(x.device))
     if rc != IMC_OK:
         raise ImcError(rc, "conv2d_gemm_f32")
+    return out
+
+
+# ------------------------------------------------- host-buffer entry points
+def _host_stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def addmm_host(self, mat1, mat2, *, beta=1.0, alpha=1.0, mode="default", relu=False, out=None,
+               stream=None):
+    """addmm on CPU tensors through gemm_addmm_f32_host: the library copies the
+    inputs to the GPU, computes there and copies ``out`` back, all enqueued on
+    ``stream`` (a torch.cuda.Stream; None: the current stream).  Returns ``out``
+    at once; it holds the result after ``stream.synchronize()``.  Page-locked
+    tensors (``pin_memory()``) let the copies run asynchronously.
+    """
+    import torch
+    M, N, K, self_2d = _addmm_dims(self, mat1, mat2, host=True)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, pin_memory=mat1.is_pinned())
+    else:
+        _check_tensor(out, "out", (2,), host=True)
+    rc = gemm_addmm_f32_host(_ptr(self), self_2d, _ptr(mat1), _ptr(mat2), _ptr(out), M, N, K,
+                             float(beta), float(alpha), _mode(mode, relu), _host_stream(stream))
+    if rc != IMC_OK:
+        raise ImcError(rc, "gemm_addmm_f32_host")
+    return out
+
+
+def conv2d_host(x, w, bias=None, stride=1, padding=0, dilation=1, *, mode="default", relu=False,
+                out=None, stream=None):
+    """conv2d on CPU tensors through conv2d_gemm_f32_host (as ``addmm_host``)."""
+    import torch
+    B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, OH, OW = _conv_dims(
+        x, w, bias, stride, padding, dilation, host=True)
+    if out is None:
+        out = torch.empty((B, OC, OH, OW), dtype=torch.float32, pin_memory=x.is_pinned())
+    else:
+        _check_tensor(out, "out", (4,), host=True)
+    rc = conv2d_gemm_f32_host(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), B, IC, H, W, OC, KH, KW,
+                              sH, sW, pH, pW, dH, dW, _mode(mode, relu), _host_stream(stream))
+    if rc != IMC_OK:
+        raise ImcError(rc, "conv2d_gemm_f32_host")
     return out

@@ -72,6 +72,46 @@ int finish(cudaError_t e, int kernel) {
   t_last_kernel = kernel;
   return IMC_OK;
 }
+
+// The library's stream-ordered memory pool of each device, created on first
+// use.  It keeps the memory it has handed out for later calls (release
+// threshold: all of it; imc_release_memory gives it back), and hands a block
+// freed on one stream to a call on another stream only once that free has
+// completed: no dependency is added between the streams of separate calls.
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[kMaxDevices];
+
+cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t s) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    if (!g_pool[dev]) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t created;
+      e = cudaMemPoolCreate(&created, &props);
+      if (e != cudaSuccess) return e;
+      uint64_t keep = UINT64_MAX;
+      int no = 0;
+      if ((e = cudaMemPoolSetAttribute(created, cudaMemPoolAttrReleaseThreshold, &keep)) !=
+              cudaSuccess ||
+          (e = cudaMemPoolSetAttribute(created, cudaMemPoolReuseAllowInternalDependencies,
+                                       &no)) != cudaSuccess) {
+        cudaMemPoolDestroy(created);
+        return e;
+      }
+      g_pool[dev] = created;
+    }
+    pool = g_pool[dev];
+  }
+  return cudaMallocFromPoolAsync(p, bytes, pool, s);
+}
 }  // namespace
 
 int device_sm_count() {
@@ -116,13 +156,16 @@ int plan_gemm(int64_t M, int64_t N, int64_t K, double alpha, int mode, bool tc_o
 }
 
 // workspace == nullptr and !caller_ws: the transposed-mat2 workspace comes
-// from the device's stream-ordered pool (cudaMallocAsync / cudaFreeAsync on
+// from the library's stream-ordered pool (pool_alloc / cudaFreeAsync on
 // `stream`).  caller_ws: the caller's buffer of ws_bytes is used, nothing is
 // allocated.
 // b_kmajor: mat2 is given transposed as [N,K] (linear).
+// validate_only: run every argument check (pointers taken as 16-byte aligned,
+// as the device copies of host buffers are) and return before any CUDA call.
 int gemm_impl(const float* self, int self_2d, const float* mat1, const float* mat2, float* out,
               int64_t M, int64_t N, int64_t K, double beta, double alpha, int mode_arg,
-              bool b_kmajor, void* workspace, size_t ws_bytes, bool caller_ws, void* stream) {
+              bool b_kmajor, void* workspace, size_t ws_bytes, bool caller_ws, void* stream,
+              bool validate_only = false) {
   if (self_2d != 0 && self_2d != 1) return IMC_ERR_ARG;
   int mode = 0, relu = 0;
   if (!parse_mode(mode_arg, false, &mode, &relu)) return IMC_ERR_ARG;
@@ -164,10 +207,11 @@ int gemm_impl(const float* self, int self_2d, const float* mat1, const float* ma
   a.vec_out = (N % 4 == 0) && aligned16(out) && (!read_self || aligned16(self)) ? 1 : 0;
   a.relu = relu;
   a.b_kmajor = b_kmajor ? 1 : 0;
-  const bool tc_ok =
-      read_ops && K % 4 == 0 && aligned16(mat1) && (!b_kmajor || aligned16(mat2));
+  const bool tc_ok = read_ops && K % 4 == 0 &&
+                     (validate_only || (aligned16(mat1) && (!b_kmajor || aligned16(mat2))));
   const int kernel = plan_gemm(M, N, K, alpha, mode, tc_ok);
   if (kernel < 0) return IMC_ERR_SHAPE;
+  if (validate_only) return IMC_OK;
   const bool tc = kernel == IMC_KERNEL_TC3 || kernel == IMC_KERNEL_TC1;
   const bool three = kernel == IMC_KERNEL_TC3;
   // minimum (no split-K) and the scratch the call will use
@@ -190,7 +234,7 @@ int gemm_impl(const float* self, int self_2d, const float* mat1, const float* ma
   if (!tc_gemm_supported(a)) return IMC_ERR_DEVICE;  // driver without tensor-map support
   void* ws = workspace;
   const bool pool = !caller_ws && need > 0;
-  if (pool && cudaMallocAsync(&ws, need, s) != cudaSuccess) return IMC_ERR_CUDA;
+  if (pool && pool_alloc(&ws, need, s) != cudaSuccess) return IMC_ERR_CUDA;
   const cudaError_t e = launch_tc_gemm(a, three, ws, need, s);
   if (pool) {
     const cudaError_t f = cudaFreeAsync(ws, s);
@@ -343,10 +387,12 @@ ConvArgs conv_args(const float* x, const float* w, const float* bias, float* out
   return c;
 }
 
+// validate_only: as for gemm_impl.
 int conv_impl(const float* x, const float* w, const float* bias, float* out, int64_t B,
               int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW, int64_t sH,
               int64_t sW, int64_t pH, int64_t pW, int64_t dH, int64_t dW, int mode_arg,
-              void* workspace, size_t ws_bytes, bool caller_ws, void* stream) {
+              void* workspace, size_t ws_bytes, bool caller_ws, void* stream,
+              bool validate_only = false) {
   int mode = 0, relu = 0;
   if (!parse_mode(mode_arg, true, &mode, &relu)) return IMC_ERR_ARG;
   ConvShape cs;
@@ -368,6 +414,7 @@ int conv_impl(const float* x, const float* w, const float* bias, float* out, int
                                cs, relu);
   const int kernel = plan_conv(OC, B * OH * OW, K, mode, tc_conv_shape_ok(c));
   if (kernel < 0) return IMC_ERR_SHAPE;
+  if (validate_only) return IMC_OK;
   const bool tc = kernel == IMC_KERNEL_TC3 || kernel == IMC_KERNEL_TC1;
   const bool three = kernel == IMC_KERNEL_TC3;
   // minimum (no K-slices) and the scratch the call will use
@@ -391,7 +438,7 @@ int conv_impl(const float* x, const float* w, const float* bias, float* out, int
   if (!tc_conv_supported(c)) return IMC_ERR_DEVICE;  // driver without tensor-map support
   void* ws = workspace;
   if (!caller_ws) {
-    if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return IMC_ERR_CUDA;
+    if (pool_alloc(&ws, need, s) != cudaSuccess) return IMC_ERR_CUDA;
   }
   const cudaError_t e = launch_tc_conv(c, three, ws, need, s);
   if (!caller_ws) {
@@ -451,6 +498,154 @@ int conv2d_gemm_f32(const float* x, const float* w, const float* bias, float* ou
                             dilation, dilation, IMC_MODE_DEFAULT, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+size_t round256(uint64_t b) { return (size_t)((b + 255) & ~uint64_t(255)); }
+
+// The library's two copy queues of each device (created on first use):
+// every host-buffer call puts its host->device copies on the first and its
+// device->host copy on the second, tied to the caller's stream by events.
+// The copies of calls issued on different streams then run one after another
+// in call order, one per direction at a time: the link's bandwidth drops
+// when several copies in one direction share it.
+std::mutex g_queue_mu;
+cudaStream_t g_copy_in[kMaxDevices], g_copy_out[kMaxDevices];
+
+cudaError_t copy_queues(cudaStream_t* in, cudaStream_t* out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_queue_mu);
+  if (!g_copy_in[dev]) {
+    cudaStream_t a, b;
+    if ((e = cudaStreamCreateWithFlags(&a, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&b, cudaStreamNonBlocking)) != cudaSuccess) {
+      cudaStreamDestroy(a);
+      return e;
+    }
+    g_copy_in[dev] = a;
+    g_copy_out[dev] = b;
+  }
+  *in = g_copy_in[dev];
+  *out = g_copy_out[dev];
+  return cudaSuccess;
+}
+
+// Work enqueued on `to` after this call waits for the work on `from` so far.
+cudaError_t link(cudaStream_t from, cudaStream_t to) {
+  cudaEvent_t ev;
+  cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) return e;
+  e = cudaEventRecord(ev, from);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(to, ev, 0);
+  const cudaError_t d = cudaEventDestroy(ev);  // released once it has completed
+  return e != cudaSuccess ? e : d;
+}
+
+// Device copies of a call's host buffers in one stream-ordered allocation on
+// the caller's stream `s`: `n` host ranges (nullptr / 0 bytes: absent) at
+// 256-byte boundaries; dev[i] is the device address of range i.  take()
+// copies the inputs in on the copy-in queue, after the work already on `s`,
+// and makes `s` wait for them; finish() copies the result out on the copy-out
+// queue once the work on `s` (the computation) is done, makes `s` wait for
+// that copy and releases the allocation on `s`.
+struct DeviceCopies {
+  char* base = nullptr;
+  cudaStream_t s, q_in = nullptr, q_out = nullptr;
+  explicit DeviceCopies(cudaStream_t st) : s(st) {}
+  int take(const void* const* host, const uint64_t* bytes, const bool* copy_in, int n,
+           float** dev) {
+    if (copy_queues(&q_in, &q_out) != cudaSuccess) return IMC_ERR_CUDA;
+    size_t total = 0;
+    for (int i = 0; i < n; ++i) total += round256(bytes[i]);
+    if (pool_alloc((void**)&base, total, s) != cudaSuccess) {
+      base = nullptr;
+      return IMC_ERR_CUDA;
+    }
+    if (link(s, q_in) != cudaSuccess) return IMC_ERR_CUDA;
+    int rc = IMC_OK;
+    size_t off = 0;
+    for (int i = 0; i < n; ++i) {
+      dev[i] = bytes[i] ? reinterpret_cast<float*>(base + off) : nullptr;
+      off += round256(bytes[i]);
+      if (rc == IMC_OK && copy_in[i] && bytes[i] &&
+          cudaMemcpyAsync(dev[i], host[i], bytes[i], cudaMemcpyHostToDevice, q_in) != cudaSuccess)
+        rc = IMC_ERR_CUDA;
+    }
+    // `s` waits for the copies even after a failed one: the allocation is
+    // released on `s`.
+    if (link(q_in, s) != cudaSuccess) rc = IMC_ERR_CUDA;
+    return rc;
+  }
+  int finish(int rc, void* host_out, const float* dev_out, uint64_t bytes) {
+    if (rc == IMC_OK) {
+      if (link(s, q_out) != cudaSuccess ||
+          cudaMemcpyAsync(host_out, dev_out, bytes, cudaMemcpyDeviceToHost, q_out) !=
+              cudaSuccess)
+        rc = IMC_ERR_CUDA;
+      if (link(q_out, s) != cudaSuccess) rc = IMC_ERR_CUDA;
+    }
+    if (base && cudaFreeAsync(base, s) != cudaSuccess && rc == IMC_OK) rc = IMC_ERR_CUDA;
+    return rc;
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+int gemm_addmm_f32_host(const float* self, int self_2d, const float* mat1, const float* mat2,
+                        float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                        int mode, void* stream) {
+  const int v = gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, false,
+                          nullptr, 0, false, stream, true);
+  if (v != IMC_OK || M == 0 || N == 0) return v;
+  const int dev = check_device();
+  if (dev != IMC_OK) return dev;
+  const bool read_self = beta != 0.0, read_ops = alpha != 0.0 && K > 0;
+  const void* host[4] = {self, mat1, mat2, out};
+  const uint64_t bytes[4] = {read_self ? (uint64_t)(self_2d ? M * N : N) * 4u : 0,
+                             read_ops ? (uint64_t)(M * K) * 4u : 0,
+                             read_ops ? (uint64_t)(K * N) * 4u : 0, (uint64_t)(M * N) * 4u};
+  const bool copy_in[4] = {true, true, true, false};
+  float* d[4];
+  DeviceCopies dc((cudaStream_t)stream);
+  int rc = dc.take(host, bytes, copy_in, 4, d);
+  if (rc == IMC_OK)
+    rc = gemm_impl(d[0], self_2d, d[1], d[2], d[3], M, N, K, beta, alpha, mode, false, nullptr, 0,
+                   false, stream);
+  return dc.finish(rc, out, d[3], bytes[3]);
+}
+
+int conv2d_gemm_f32_host(const float* x, const float* w, const float* bias, float* out,
+                         int64_t B, int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH,
+                         int64_t KW, int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH,
+                         int64_t dW, int mode, void* stream) {
+  const int v = conv_impl(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, mode,
+                          nullptr, 0, false, stream, true);
+  if (v != IMC_OK || B == 0 || OC == 0) return v;
+  const int dev = check_device();
+  if (dev != IMC_OK) return dev;
+  ConvShape cs;
+  conv_shape(B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, &cs);  // checked above
+  const void* host[4] = {x, w, bias, out};
+  const uint64_t bytes[4] = {cs.K > 0 ? (uint64_t)(B * IC * H * W) * 4u : 0,
+                             cs.K > 0 ? (uint64_t)(OC * cs.K) * 4u : 0,
+                             bias ? (uint64_t)OC * 4u : 0,
+                             (uint64_t)(B * OC * cs.OH * cs.OW) * 4u};
+  const bool copy_in[4] = {true, true, true, false};
+  float* d[4];
+  DeviceCopies dc((cudaStream_t)stream);
+  int rc = dc.take(host, bytes, copy_in, 4, d);
+  if (rc == IMC_OK)
+    rc = conv_impl(d[0], d[1], d[2], d[3], B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, mode,
+                   nullptr, 0, false, stream);
+  return dc.finish(rc, out, d[3], bytes[3]);
+}
+
 const char* imc_status_string(int status) {
   switch (status) {
     case IMC_OK: return "IMC_OK";
@@ -482,7 +677,14 @@ int imc_check_device_error(void* stream) {
   return (vg != 0 || vc != 0) ? IMC_ERR_TIMEOUT : IMC_OK;
 }
 
-int imc_version(void) { return 101; }
+int imc_version(void) { return 102; }
+
+int imc_release_memory(void) {
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  for (int d = 0; d < kMaxDevices; ++d)
+    if (g_pool[d] && cudaMemPoolTrimTo(g_pool[d], 0) != cudaSuccess) return IMC_ERR_CUDA;
+  return IMC_OK;
+}
 
 }  // extern "C"
 

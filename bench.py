@@ -241,81 +241,55 @@ def run_gpu(args):
     ms_step = max_over_ranks(ms_step_local, dist_mod, device)
     value = whole_job_rate(flops_step, ws, ms_step)
 
-    # ---- end to end: pinned host inputs -> device -> kernels -> host, every step.
-    # Each step copies its six inputs from pinned host memory, runs the addmm and
-    # the conv through the public API and copies both results back.  The steps
-    # are pipelined over three streams (inputs of step i+1 go in while step i
-    # computes and step i-1's results come out) on two sets of device buffers;
-    # the per-step inputs (229 MB) are larger than L2.  The same steps run one
-    # after another on a single stream are reported beside it.
+    # ---- end to end through the host-buffer entry points: every step hands the
+    # library its six inputs in pinned host memory and takes both results back
+    # in pinned host memory (gemm_addmm_f32_host + conv2d_gemm_f32_host: the
+    # library copies the inputs in, computes and copies the results out, all on
+    # the step's stream).  Steps rotate over --e2e-streams streams, so step i+1's
+    # inputs go in while step i computes and its results come out; the per-step
+    # inputs (229 MB) are larger than L2.  The same steps on one stream are
+    # reported beside it.
     h_in = [torch.from_numpy(t).pin_memory() for t in (s_np, a_np, b_np, x_np, w_np, bias_np)]
     h_out = [torch.empty(out_a.shape, dtype=torch.float32).pin_memory(),
              torch.empty(out_c.shape, dtype=torch.float32).pin_memory()]
     h2d = sum(t.numel() * 4 for t in h_in)
     d2h = sum(t.numel() * 4 for t in h_out)
     e2e_steps = max(4, min(args.steps, 12))
-    sets = [[S, A, Bm, X, Wt, Bias, out_a, out_c],
-            [torch.empty_like(t) for t in (S, A, Bm, X, Wt, Bias, out_a, out_c)]]
+    # the addmm and the conv are independent problems: each has its own ring
+    e2e_streams = [(torch.cuda.Stream(device), torch.cuda.Stream(device))
+                   for _ in range(args.e2e_streams)]
 
-    def compute(d):
-        binding.addmm(d[0], d[1], d[2], beta=ca["beta"], alpha=ca["alpha"], out=d[6])
-        binding.conv2d(d[3], d[4], d[5], cc["stride"], cc["pad"], cc["dilation"], out=d[7])
+    def host_step(st):
+        binding.addmm_host(h_in[0], h_in[1], h_in[2], beta=ca["beta"], alpha=ca["alpha"],
+                           out=h_out[0], stream=st[0])
+        binding.conv2d_host(h_in[3], h_in[4], h_in[5], cc["stride"], cc["pad"], cc["dilation"],
+                            out=h_out[1], stream=st[1])
 
-    def e2e_serial(n):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n):
-            d = sets[0]
-            for h, t in zip(h_in, d[:6]):
-                t.copy_(h, non_blocking=True)
-            compute(d)
-            h_out[0].copy_(d[6], non_blocking=True)
-            h_out[1].copy_(d[7], non_blocking=True)
-        e1.record(stream)
-        e1.synchronize()
-        return e0.elapsed_time(e1) / n
-
-    s_in, s_comp, s_out = (torch.cuda.Stream(device) for _ in range(3))
-
-    def e2e_pipelined(n):
-        new_ev = lambda: torch.cuda.Event(enable_timing=True)
-        start, end = new_ev(), new_ev()
-        in_done, comp_done, out_done = [None] * n, [None] * n, [None] * n
+    def e2e_run(n, rings):
+        streams = list(dict.fromkeys(st for pair in rings for st in pair))
+        first = streams[0]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(device)
-        start.record(s_in)
+        start.record(first)
+        for st in streams[1:]:
+            st.wait_event(start)
         for i in range(n):
-            d = sets[i % 2]
-            with torch.cuda.stream(s_in):  # inputs of set i%2: free once step i-2 computed
-                if i >= 2:
-                    s_in.wait_event(comp_done[i - 2])
-                for h, t in zip(h_in, d[:6]):
-                    t.copy_(h, non_blocking=True)
-                in_done[i] = new_ev()
-                in_done[i].record(s_in)
-            with torch.cuda.stream(s_comp):
-                s_comp.wait_event(in_done[i])
-                if i >= 2:  # outputs of set i%2: free once step i-2's results are out
-                    s_comp.wait_event(out_done[i - 2])
-                compute(d)
-                comp_done[i] = new_ev()
-                comp_done[i].record(s_comp)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(comp_done[i])
-                h_out[0].copy_(d[6], non_blocking=True)
-                h_out[1].copy_(d[7], non_blocking=True)
-                out_done[i] = new_ev()
-                out_done[i].record(s_out)
-        end.record(s_out)
+            host_step(rings[i % len(rings)])
+        for st in streams[1:]:
+            done = torch.cuda.Event()
+            done.record(st)
+            first.wait_event(done)
+        end.record(first)
         end.synchronize()
-        torch.cuda.synchronize(device)
         return start.elapsed_time(end) / n
 
-    e2e_serial(1)
-    e2e_pipelined(2)
+    one_stream = [(e2e_streams[0][0], e2e_streams[0][0])]
+    e2e_run(2, one_stream)
+    e2e_run(len(e2e_streams), e2e_streams)
     barrier(dist_mod, device)
-    serial_ms = max_over_ranks(e2e_serial(e2e_steps), dist_mod, device)
+    serial_ms = max_over_ranks(e2e_run(e2e_steps, one_stream), dist_mod, device)
     barrier(dist_mod, device)
-    e2e_ms = max_over_ranks(e2e_pipelined(e2e_steps), dist_mod, device)
+    e2e_ms = max_over_ranks(e2e_run(e2e_steps, e2e_streams), dist_mod, device)
     e2e_value = whole_job_rate(flops_step, ws, e2e_ms)
     # the last step's results, as copied to the host, equal the device-resident run's
     e2e_ok = (torch.equal(h_out[0], out_a.cpu()) and torch.equal(h_out[1], out_c.cpu()))
@@ -376,9 +350,11 @@ def run_gpu(args):
         },
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
-                "path": "every step: pinned host -> device copies of its 6 inputs, addmm + "
-                        "conv2d through the C ABI, device -> pinned host copies of both "
-                        "results; steps pipelined over 3 streams on 2 device buffer sets",
+                "path": "every step: gemm_addmm_f32_host + conv2d_gemm_f32_host on pinned "
+                        "host buffers (the library copies the 6 inputs in, computes and "
+                        "copies both results out on the call's stream; one copy queue per "
+                        "direction); the addmm and the conv each rotate over "
+                        f"{args.e2e_streams} streams",
                 "serial_ms_per_step": round(serial_ms, 4), "results_match_device_run": e2e_ok,
                 "serial_value": round(whole_job_rate(flops_step, ws, serial_ms), 1)},
         "gpu_launches": launches,
@@ -500,6 +476,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-direct-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=1.0)
+    ap.add_argument("--e2e-streams", type=int, default=3,
+                    help="streams each problem's end-to-end calls rotate over")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # the timing rules want at least 3 warm-up steps
     line = run_reference(args) if args.impl == "reference" else run_gpu(args)

@@ -11,8 +11,12 @@
  *    mat2 transposed and split into TF32 hi / lo parts, conv2d the weight
  *    split the same way in zero-padded rows.  The *_ws entry points take it
  *    from the caller and allocate nothing; the others take it from the
- *    device's stream-ordered memory pool (cudaMallocAsync / cudaFreeAsync on
- *    `stream`).  The scratch is dead once the call's work completes.
+ *    library's own stream-ordered memory pool on the current device
+ *    (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`).  The scratch is
+ *    dead once the call's work completes.  The pool keeps the memory it has
+ *    handed out for later calls until imc_release_memory(), and gives a block
+ *    freed on one stream to another stream only once that free has completed
+ *    (calls on different streams never wait for each other through it).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *    enqueued asynchronously on it; no entry point synchronises the host.
  *  - Every argument is checked before anything is launched.  A call that
@@ -252,6 +256,37 @@ int linear_f32_ws(const float* x, const float* w, const float* bias, float* out,
                   int64_t N, int64_t K, int mode, void* workspace, size_t workspace_bytes,
                   void* stream);
 
+/*
+ * gemm_addmm_f32_host, conv2d_gemm_f32_host -- gemm_addmm_f32_ex and
+ * conv2d_gemm_f32_nd on HOST buffers.  (The pages have no counterpart: this
+ * is the library's call for callers that hold their tensors in host memory.)
+ *
+ * Every tensor pointer (self, mat1, mat2, out; x, w, bias, out) is a host
+ * pointer to contiguous row-major fp32 data, with the layouts, the other
+ * arguments, the checks and the status codes of the device entry points.
+ * All argument checks run first (aliasing is checked on the host ranges;
+ * out may equal a 2-D self, as there).  The call then enqueues on `stream`:
+ * one device buffer from the library's pool, the host->device copies of the
+ * inputs the call reads, the computation (the device entry point on those
+ * copies), the device->host copy of out, and the buffer's release.  It
+ * returns once that is enqueued; out holds the result when the stream's work
+ * up to that point has completed (cudaStreamSynchronize).  Calls on separate
+ * streams overlap one call's copies with another's computation.
+ * Host memory: page-locked (cudaHostAlloc, cudaMallocHost, cudaHostRegister)
+ * for copies that run asynchronously and overlap other streams' work;
+ * pageable memory is accepted, but the copies then hold the calling thread.
+ * The caller keeps the input buffers unchanged, and out unread, until the
+ * stream's work completes.  A failure after the checks (a CUDA error while
+ * copying or launching) returns IMC_ERR_CUDA.
+ */
+int gemm_addmm_f32_host(const float* self, int self_2d, const float* mat1, const float* mat2,
+                        float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                        int mode, void* stream);
+int conv2d_gemm_f32_host(const float* x, const float* w, const float* bias, float* out,
+                         int64_t B, int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH,
+                         int64_t KW, int64_t sH, int64_t sW, int64_t pH, int64_t pW, int64_t dH,
+                         int64_t dW, int mode, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* imc_status_string(int status);
 
@@ -269,6 +304,11 @@ int imc_check_device_error(void* stream);
 
 /* Library ABI version (major * 100 + minor). */
 int imc_version(void);
+
+/* Returns the device memory the library's pools hold but no call in flight
+ * uses (cudaMemPoolTrimTo) on every device the library has used.  Call it
+ * once the library's work has completed.  IMC_OK or IMC_ERR_CUDA. */
+int imc_release_memory(void);
 
 #ifdef __cplusplus
 }

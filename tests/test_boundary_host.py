@@ -270,3 +270,41 @@ def test_torch_wrappers_validate_before_calling(lib):
         binding.addmm(torch.zeros(3), x, torch.zeros(3, 4))  # CPU tensors are refused
     with pytest.raises(TypeError):
         binding.addmm(None, [[1.0]], x)
+
+
+def test_host_buffer_entry_points_check_before_any_cuda_call(lib):
+    # Host pointers are checked like device ones (aliasing on the host
+    # ranges); a well-formed call then needs a GPU and fails loudly without one.
+    H = binding.gemm_addmm_f32_host
+    assert H(P1, 0, P2, P3, None, 8, 8, 8, 1.0, 1.0, 0, None) == binding.IMC_ERR_NULL
+    assert H(P1, 0, None, P3, P4, 8, 8, 8, 1.0, 1.0, 0, None) == binding.IMC_ERR_NULL
+    assert H(P1, 0, P2, P3, P4, -1, 8, 8, 1.0, 1.0, 0, None) == binding.IMC_ERR_SHAPE
+    assert H(P1, 2, P2, P3, P4, 8, 8, 8, 1.0, 1.0, 0, None) == binding.IMC_ERR_ARG
+    assert H(P1, 0, P2, P3, P4, 8, 8, 8, 1.0, 1.0, 9, None) == binding.IMC_ERR_ARG
+    assert H(P1, 0, P2, P3, P2 + 16, 8, 8, 8, 1.0, 1.0, 0, None) == binding.IMC_ERR_ALIAS
+    assert H(P1, 0, P2, P3, P4, 8, 8, 10, 1.0, 1.0, 3, None) == binding.IMC_ERR_SHAPE  # K % 4
+    assert H(P1, 0, P2, P3, P4, 0, 8, 8, 1.0, 1.0, 0, None) == binding.IMC_OK  # empty: no work
+    C = binding.conv2d_gemm_f32_host
+    conv = [P1, P2, P3, P4, 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 1, 0, None]
+    assert C(*conv[:3], None, *conv[4:]) == binding.IMC_ERR_NULL
+    assert C(*conv[:3], P1 + 64, *conv[4:]) == binding.IMC_ERR_ALIAS
+    bad = list(conv)
+    bad[11] = 0  # stride 0
+    assert C(*bad) == binding.IMC_ERR_SHAPE
+    got = without_gpu([["gemm_addmm_f32_host", [P1, 0, P2, P3, P4, 8, 8, 8, 1.0, 1.0, 0, None]],
+                       ["conv2d_gemm_f32_host", conv]])
+    assert got == [binding.IMC_ERR_DEVICE] * 2
+
+
+def test_host_wrappers_take_cpu_tensors_only(lib):
+    with pytest.raises(ValueError):
+        binding.addmm_host(None, torch.zeros(2, 3, device="meta"), torch.zeros(3, 4))
+    with pytest.raises(ValueError):
+        binding.addmm_host(None, torch.zeros(2, 3, dtype=torch.float64), torch.zeros(3, 4))
+    with pytest.raises(ValueError):
+        binding.conv2d_host(torch.zeros(1, 3, 8, 8), torch.zeros(4, 2, 3, 3))
+
+
+def test_release_memory_without_work_is_ok(lib):
+    # no pool exists before the first call that needs scratch: nothing to trim
+    assert without_gpu([["release_memory", []]]) == [binding.IMC_OK]
