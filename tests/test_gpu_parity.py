@@ -111,6 +111,33 @@ def test_addmm_long_k_tile_path():
         assert np.array_equal(got.astype(np.float64), ref), mode
 
 
+@pytest.mark.parametrize("mode", ["default", "tf32"])
+def test_addmm_ragged_partial_last_wave(mode):
+    # 160 to 180 output tiles on 152 SMs with ~96 k-blocks each (a short last
+    # wave); ragged M, N and K; [M,N] self with negative alpha, and ReLU
+    M, N, K = 2523, 1948, 1532
+    rows = np.unique(np.concatenate([synth.sample_rows(synth.stream_key(0, 34, 9), M, 160),
+                                     np.arange(M - 40, M)]))
+    for self_2d, alpha, beta, relu in [(True, -0.5, 2.0, False), (False, 1.0, 1.0, True)]:
+        s, a, b = synth.addmm_inputs(M, N, K, self_2d=self_2d, workload=34 + self_2d,
+                                     mat1=("N", 0.0, 1.0), mat2=("N", 0.0, 1.0 / np.sqrt(K)),
+                                     self_=("N", 0.0, 1.0))
+        out = binding.addmm(dev(s), dev(a), dev(b), beta=beta, alpha=alpha, mode=mode,
+                            relu=relu)
+        torch.cuda.synchronize()
+        assert binding.last_kernel() == ("tc3" if mode == "default" else "tc1")
+        got = out.cpu().numpy()[rows]
+        ref, S = oracle.addmm(s, a, b, beta=beta, alpha=alpha, rows=rows, self_2d=self_2d)
+        if relu:
+            ref = np.maximum(ref, 0.0)
+        within(got, ref, S, TOL[mode], f"ragged last wave {mode} self_2d={self_2d} relu={relu}")
+    spec = ("I", -2, 2)
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=True, workload=36, mat1=spec, mat2=spec,
+                                 self_=spec)
+    got, ref, _, _ = run_addmm(s, a, b, 1.0, 1.0, mode, rows=rows)
+    assert np.array_equal(got.astype(np.float64), ref), mode
+
+
 def test_addmm_k_not_multiple_of_4_takes_simt():
     for M, N, K in [(70, 40, 33), (5, 7, 3), (300, 260, 130)]:
         s, a, b = synth.addmm_inputs(M, N, K, self_2d=False, workload=5)
