@@ -33,8 +33,10 @@
 //   warp 9      TMEM owner + MMA issuer, A from TMEM and B from shared memory:
 //               A_lo*B_hi + A_hi*B_lo + A_hi*B_hi per k-step of 8, or A*B
 //   warps 10-13 epilogue: tcgen05.ld (one position per lane), transposed
-//               through shared memory, + bias, written to NCHW as 512-byte
-//               runs of positions per channel
+//               through shared memory, + bias; a whole tile inside one image
+//               leaves by one 3-D TMA store per 32-channel chunk, other tiles
+//               (and K-slice partial sums) as 512-byte runs of positions per
+//               channel
 // TMEM columns 0-255 hold the accumulator (two of 128 when BN <= 128, so the
 // epilogue of one tile overlaps the next), columns 256-511 the A stages (32
 // columns each: hi 0-15, lo 16-31).

@@ -28,8 +28,12 @@
 //               bits itself) and double-buffers the accumulator.  The TS form
 //               is used when a unit runs enough k-blocks that the faster MMAs
 //               outweigh the drain of the single accumulator (see kTsMinKb)
-//   warps 2-5   epilogue: tcgen05.ld, 32x32 transpose through shared memory,
-//               beta*self + alpha*acc, 16-byte row-segment stores
+//   warps 2-5   epilogue: tcgen05.ld, then beta*self + alpha*acc: a whole
+//               tile with N % 4 == 0 and no [M,N] self leaves by 2-D TMA
+//               stores of 32 x 32 blocks from a 128-byte-swizzled staging
+//               block (beta*self of a vector self staged once per tile in
+//               shared memory); otherwise a 32x32 transpose through shared
+//               memory and 16-byte row-segment stores
 //
 // One persistent CTA per SM walks 128 x BN tiles in a grouped raster; BN (32
 // to 256) is picked per problem to fill the SMs with few waves.  Every
