@@ -46,6 +46,7 @@
 // order (the result does not depend on which CTA ran which slice).
 // Every barrier wait is bounded (see tc_common.cuh).
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "imc.h"
@@ -728,15 +729,15 @@ constexpr int kMaxDev = 64;
 template <bool THREE, bool ICF>
 cudaError_t launch_main(const ConvArgs& c, const Plan& pl, const CUtensorMap& th,
                         const CUtensorMap& tl, const CUtensorMap& to, int grid, cudaStream_t s) {
-  static bool ready[kMaxDev];
+  static std::atomic<bool> ready[kMaxDev];  // per device: the attribute is set (calls may race)
   auto k = k_tc_conv<THREE, ICF>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= kMaxDev || !ready[dev]) {
+  if (dev >= kMaxDev || !ready[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (e != cudaSuccess) return e;
-    if (dev < kMaxDev) ready[dev] = true;
+    if (dev < kMaxDev) ready[dev].store(true, std::memory_order_release);
   }
   return launch_after_previous(k, dim3(grid), dim3(THREADS), (size_t)pl.smem, s, th, tl, to, c,
                                pl.q);

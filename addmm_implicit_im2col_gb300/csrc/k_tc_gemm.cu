@@ -38,6 +38,7 @@
 // One persistent CTA per SM walks 128 x BN tiles in a grouped raster; BN (32
 // to 256) is picked per problem to fill the SMs with few waves.  Every
 // barrier wait is bounded (see tc_common.cuh).
+#include <atomic>
 #include <mutex>
 
 #include "imc.h"
@@ -710,15 +711,15 @@ template <bool THREE, bool TS>
 cudaError_t run(const GemmArgs& g, const Plan& p, const float* bt_hi, const float* bt_lo,
                 float* part, bool after_prep, cudaStream_t s) {
   constexpr int smem = smem_bytes(TS ? kLts : (THREE ? kL3 : kL1));
-  static bool ready[kMaxDev];
+  static std::atomic<bool> ready[kMaxDev];  // per device: the attribute is set (calls may race)
   auto k = k_tc_gemm<THREE, TS>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= kMaxDev || !ready[dev]) {
+  if (dev >= kMaxDev || !ready[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (dev < kMaxDev) ready[dev] = true;
+    if (dev < kMaxDev) ready[dev].store(true, std::memory_order_release);
   }
   const int sms = device_sm_count();
   CUtensorMap ta, tbh, tbl;

@@ -19,6 +19,9 @@
  *    (calls on different streams never wait for each other through it).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *    enqueued asynchronously on it; no entry point synchronises the host.
+ *  - Host threads may call the entry points at the same time (the library's
+ *    per-device state is set up once, under locks or atomics); calls whose
+ *    buffers overlap must still be ordered by the caller's streams.
  *  - Every argument is checked before anything is launched.  A call that
  *    returns an error has enqueued nothing and written nothing.
  *  - Return value: IMC_OK (0) or one of the negative IMC_ERR_* codes below;

@@ -113,3 +113,37 @@ def test_release_memory_after_work():
     out2 = binding.addmm_host(host(s, True), host(a, True), host(b, True))
     torch.cuda.synchronize()
     assert torch.equal(out, out2)
+
+
+def test_calls_from_several_host_threads():
+    # four host threads call the device and host entry points at once, each on
+    # its own stream; every result is that of its own inputs
+    import threading
+    cases = [synth.addmm_inputs(384 + 64 * i, 512, 320, self_2d=bool(i % 2), workload=750 + i)
+             for i in range(4)]
+    results, errors = [None] * 4, []
+
+    def work(i):
+        try:
+            s, a, b = cases[i]
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                d = binding.addmm(torch.from_numpy(s).cuda(), torch.from_numpy(a).cuda(),
+                                  torch.from_numpy(b).cuda(), beta=0.5)
+                h = binding.addmm_host(host(s, True), host(a, True), host(b, True), beta=0.5,
+                                       stream=st)
+            st.synchronize()
+            results[i] = (d.cpu(), h)
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for (s, a, b), (d, h) in zip(cases, results):
+        ref, S = oracle.addmm(s, a, b, beta=0.5, alpha=1.0, self_2d=s.ndim == 2)
+        within(d.numpy(), ref, S, 1e-5, "device call from a thread")
+        assert torch.equal(d, h)
