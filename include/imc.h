@@ -19,6 +19,10 @@
  *    (calls on different streams never wait for each other through it).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *    enqueued asynchronously on it; no entry point synchronises the host.
+ *  - The *_ws entry points enqueue only kernels on `stream` (no allocation,
+ *    no host synchronisation), so they can be captured into a CUDA graph and
+ *    replayed on new data written into the same buffers; make one call on the
+ *    device before the capture (it sets per-device kernel attributes).
  *  - Host threads may call the entry points at the same time (the library's
  *    per-device state is set up once, under locks or atomics); calls whose
  *    buffers overlap must still be ordered by the caller's streams.

@@ -385,3 +385,32 @@ def test_launch_counter_and_watchdog():
     torch.cuda.synchronize()
     assert binding.launch_count() == n0 + 3
     assert binding.check_device_error(None) == binding.IMC_OK
+
+
+def test_calls_captured_in_a_cuda_graph():
+    # the device entry points enqueue only stream-ordered work (scratch from the
+    # caller, launches with programmatic-dependent-launch edges), so a graph
+    # captured once replays them on new inputs written into the same buffers
+    M, N, K = 640, 768, 512
+    s0, a0, b0 = synth.addmm_inputs(M, N, K, self_2d=False, workload=60)
+    x0, w0, bias0 = synth.conv_inputs(2, 32, 20, 20, 96, 3, 3, workload=61)
+    S, A, B = dev(s0), dev(a0), dev(b0)
+    X, W, Bias = dev(x0), dev(w0), dev(bias0)
+    binding.addmm(S, A, B)  # first calls set per-device attributes outside the capture
+    binding.conv2d(X, W, Bias, 1, 1, 1)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        out = binding.addmm(S, A, B, beta=0.5, alpha=2.0)
+        y = binding.conv2d(X, W, Bias, 1, 1, 1)
+    for rep in range(3):
+        s, a, b = synth.addmm_inputs(M, N, K, self_2d=False, workload=62 + rep)
+        x, w, bias = synth.conv_inputs(2, 32, 20, 20, 96, 3, 3, workload=65 + rep)
+        for t, v in ((S, s), (A, a), (B, b), (X, x), (W, w), (Bias, bias)):
+            t.copy_(torch.from_numpy(v))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref, Sa = oracle.addmm(s, a, b, beta=0.5, alpha=2.0, self_2d=False)
+        within(out.cpu().numpy(), ref, Sa, 1e-5, f"graph replay {rep} addmm")
+        ref, Sc = oracle.conv2d(x, w, bias, 1, 1, 1)
+        within(y.cpu().numpy(), ref, Sc, 1e-5, f"graph replay {rep} conv")
