@@ -264,6 +264,9 @@ SMALL_CONV = [  # B, IC, H, W, OC, KH, KW, stride, pad, dil
     (3, 8, 17, 13, 200, 5, 3, 2, 1, 1),
     (1, 5, 12, 40, 36, 3, 2, (2, 3), (1, 0), (1, 2)),
     (2, 64, 9, 9, 32, 1, 1, 1, 0, 1),
+    # channel-fastest K order with IC not a multiple of 16 (per-element tap steps)
+    (2, 9, 11, 13, 40, 3, 3, 1, 1, 1),
+    (2, 12, 15, 9, 70, 3, 5, (1, 2), (1, 2), (2, 1)),
 ]
 
 
@@ -287,7 +290,7 @@ def test_conv_small(mode, idx):
 
 
 @pytest.mark.parametrize("mode", ["simt", "force_tc3", "force_tc1"])
-@pytest.mark.parametrize("idx", [0, 1, 3, 5])
+@pytest.mark.parametrize("idx", [0, 1, 3, 5, 7, 8])
 def test_conv_integer_inputs_are_bit_exact(mode, idx):
     x, w, b, s, p, d = _conv_case(SMALL_CONV[idx], 400 + idx, spec=("I", -4, 4))
     got, ref, _, kern = run_conv(x, w, b, s, p, d, mode)
