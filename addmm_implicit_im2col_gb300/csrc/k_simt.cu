@@ -137,6 +137,38 @@ __global__ __launch_bounds__(THREADS) void k_simt(const Ops ops) {
   }
 }
 
+// Small problems (few outputs, short K): one thread per output, the k loop
+// unrolled so that its loads are in flight together, no shared-memory staging
+// (whose load / barrier rounds per k-tile are the whole cost at this size).
+// Consecutive threads take consecutive n: mat2 loads are coalesced, mat1
+// loads broadcast.  fp32 FMA in k order.
+__global__ void __launch_bounds__(256) k_simt_small(const GemmArgs a) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= a.M * a.N) return;
+  const int64_t m = e / a.N, n = e - m * a.N;
+  const float* ar = a.mat1 + m * a.K;
+  float acc = 0.0f;
+  const int K = (int)a.K;  // <= kSmallK
+  int k = 0;
+  for (; k + 32 <= K; k += 32) {  // 64 loads in flight, then 32 FMAs in k order
+    float av[32], bv[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      av[j] = __ldg(ar + k + j);
+      bv[j] = a.b_kmajor ? __ldg(a.mat2 + n * a.K + k + j) : __ldg(a.mat2 + (int64_t)(k + j) * a.N + n);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc = fmaf(av[j], bv[j], acc);
+  }
+  for (; k < K; ++k) {
+    const float b = a.b_kmajor ? __ldg(a.mat2 + n * a.K + k) : __ldg(a.mat2 + (int64_t)k * a.N + n);
+    acc = fmaf(__ldg(ar + k), b, acc);
+  }
+  const float v = a.read_self ? fmaf(a.alpha, acc, a.beta * a.self[a.self_2d ? e : n])
+                              : a.alpha * acc;
+  a.out[e] = a.relu ? fmaxf(v, 0.f) : v;
+}
+
 __global__ void k_fill_gemm(const GemmArgs a) {
   const int64_t total = a.M * a.N;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
@@ -216,6 +248,9 @@ unsigned fill_blocks(int64_t total) {
 
 }  // namespace
 
+// Up to this many outputs and k, the addmm takes k_simt_small.
+constexpr int64_t kSmallOutputs = 1 << 16, kSmallK = 256;
+
 // One CTA per 64x64 output tile, linear tile index (no per-dimension grid cap).
 static bool simt_grid(int64_t M, int64_t N, unsigned* blocks) {
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
@@ -225,6 +260,11 @@ static bool simt_grid(int64_t M, int64_t N, unsigned* blocks) {
 }
 
 cudaError_t launch_simt_gemm(const GemmArgs& a, cudaStream_t s) {
+  if (a.M * a.N <= kSmallOutputs && a.K <= kSmallK) {
+    k_simt_small<<<(unsigned)((a.M * a.N + 255) / 256), 256, 0, s>>>(a);
+    note_launch();
+    return cudaGetLastError();
+  }
   unsigned grid;
   if (!simt_grid(a.M, a.N, &grid)) return cudaErrorInvalidConfiguration;
   k_simt<GemmOperands><<<grid, THREADS, 0, s>>>(GemmOperands{a});
