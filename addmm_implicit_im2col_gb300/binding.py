@@ -60,6 +60,7 @@ SIGNATURES = {
     "imc_check_device_error": (_int, [_vp]),
     "imc_version": (_int, []),
     "imc_release_memory": (_int, []),
+    "imc_selftest_wait_timeout": (_int, [_int, _vp]),
 }
 
 _lock = threading.Lock()
@@ -171,6 +172,10 @@ def conv2d_gemm_f32_host(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, p
                          stream) -> int:
     return load().conv2d_gemm_f32_host(x, w, bias, out, B, IC, H, W, OC, KH, KW, sH, sW, pH, pW,
                                        dH, dW, mode, stream)
+
+
+def selftest_wait_timeout(limit_us, stream=None) -> int:
+    return load().imc_selftest_wait_timeout(int(limit_us), stream)
 
 
 def release_memory() -> int:

@@ -677,7 +677,15 @@ int imc_check_device_error(void* stream) {
   return (vg != 0 || vc != 0) ? IMC_ERR_TIMEOUT : IMC_OK;
 }
 
-int imc_version(void) { return 102; }
+int imc_version(void) { return 103; }
+
+int imc_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1000 || limit_us > 1000000) return IMC_ERR_ARG;
+  const int dev = check_device();
+  if (dev != IMC_OK) return dev;
+  return launch_wait_selftest(limit_us, (cudaStream_t)stream) == cudaSuccess ? IMC_OK
+                                                                            : IMC_ERR_CUDA;
+}
 
 int imc_release_memory(void) {
   std::lock_guard<std::mutex> lk(g_pool_mu);

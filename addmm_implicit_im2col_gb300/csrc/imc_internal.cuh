@@ -79,6 +79,9 @@ cudaError_t launch_tc_conv(const ConvArgs& a, bool three_pass, void* workspace,
 // Read and clear the watchdog word of the addmm / conv tensor-core kernels on
 // the current device (the caller synchronises first).
 cudaError_t gemm_take_watchdog(int* value);
+// A one-thread kernel whose barrier wait gives up after limit_us (addmm
+// watchdog word).
+cudaError_t launch_wait_selftest(int limit_us, cudaStream_t s);
 cudaError_t conv_take_watchdog(int* value);
 
 // Used by the fixed-scratch addmm entry point: the scratch bytes the call

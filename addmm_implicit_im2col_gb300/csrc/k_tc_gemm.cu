@@ -811,6 +811,28 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
             : run<true, false>(g, p, b_hi, b_lo, part, prep, s);
 }
 
+namespace {
+// One thread waits on a barrier that nothing will complete: the wait gives up
+// after limit_ns and reports through the addmm watchdog word, as a real
+// timeout does (imc_selftest_wait_timeout).
+__global__ void k_wait_selftest(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+    wait_bar(&bar, 0, &abort_flag, kSiteSelfTest, &g_watchdog_gemm, limit_ns);
+  }
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(int limit_us, cudaStream_t s) {
+  k_wait_selftest<<<1, 32, 0, s>>>((uint64_t)limit_us * 1000ull);
+  note_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t gemm_take_watchdog(int* value) {
   cudaError_t e = cudaMemcpyFromSymbol(value, g_watchdog_gemm, sizeof(int));
   if (e != cudaSuccess) return e;

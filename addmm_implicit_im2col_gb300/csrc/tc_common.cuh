@@ -26,6 +26,7 @@ enum WaitSite {
   kSiteMmaAccEmpty = 3,
   kSiteMmaOperands = 4,
   kSiteEpilogueAccFull = 5,
+  kSiteSelfTest = 6,  // imc_selftest_wait_timeout: a wait nothing completes
 };
 
 struct Ctl {
@@ -39,18 +40,19 @@ struct Ctl {
   int abort;
 };
 
-// Waits for the phase with the given parity; gives up after kWaitLimitNs
+// Waits for the phase with the given parity; gives up after limit_ns
 // (recording `site` in *watchdog and raising the CTA's abort flag) or when
 // another role has raised the abort flag.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                         int site, int* watchdog) {
+                                         int site, int* watchdog,
+                                         uint64_t limit_ns = kWaitLimitNs) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((it & 127u) == 0) {
       if (*abort) return false;
-      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (ptx::globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
         atomicCAS(watchdog, 0, site);
         return false;

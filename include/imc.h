@@ -312,6 +312,15 @@ int imc_check_device_error(void* stream);
 /* Library ABI version (major * 100 + minor). */
 int imc_version(void);
 
+/* Diagnostic of the failure path: enqueues on `stream` a one-thread kernel
+ * that waits on a barrier nothing completes, with the bounded wait of the
+ * library's kernels shortened to limit_us microseconds (1000 .. 1000000).
+ * The wait gives up, the kernel records it in the watchdog word and returns,
+ * so that imc_check_device_error(stream) then reports IMC_ERR_TIMEOUT (and
+ * clears it) while the CUDA context stays usable.  IMC_OK once enqueued,
+ * IMC_ERR_ARG for a limit out of range, IMC_ERR_DEVICE without a usable GPU. */
+int imc_selftest_wait_timeout(int limit_us, void* stream);
+
 /* Returns the device memory the library's pools hold but no call in flight
  * uses (cudaMemPoolTrimTo) on every device the library has used.  Call it
  * once the library's work has completed.  IMC_OK or IMC_ERR_CUDA. */

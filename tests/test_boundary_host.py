@@ -308,3 +308,9 @@ def test_host_wrappers_take_cpu_tensors_only(lib):
 def test_release_memory_without_work_is_ok(lib):
     # no pool exists before the first call that needs scratch: nothing to trim
     assert without_gpu([["release_memory", []]]) == [binding.IMC_OK]
+
+
+def test_wait_timeout_selftest_checks_its_limit(lib):
+    assert binding.selftest_wait_timeout(999) == binding.IMC_ERR_ARG
+    assert binding.selftest_wait_timeout(1000001) == binding.IMC_ERR_ARG
+    assert without_gpu([["selftest_wait_timeout", [20000, None]]]) == [binding.IMC_ERR_DEVICE]

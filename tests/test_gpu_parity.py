@@ -417,3 +417,17 @@ def test_calls_captured_in_a_cuda_graph():
         within(out.cpu().numpy(), ref, Sa, 1e-5, f"graph replay {rep} addmm")
         ref, Sc = oracle.conv2d(x, w, bias, 1, 1, 1)
         within(y.cpu().numpy(), ref, Sc, 1e-5, f"graph replay {rep} conv")
+
+
+def test_a_wait_that_runs_out_is_reported_and_the_context_stays_usable():
+    # failure path of the bounded barrier waits, without a fault: a kernel
+    # waits on a barrier nothing completes, gives up after 20 ms, and the host
+    # reads IMC_ERR_TIMEOUT; afterwards the library works as before
+    assert binding.check_device_error(None) == binding.IMC_OK
+    assert binding.selftest_wait_timeout(20000) == binding.IMC_OK
+    assert binding.check_device_error(None) == binding.IMC_ERR_TIMEOUT
+    assert binding.check_device_error(None) == binding.IMC_OK  # read and cleared
+    s, a, b = synth.addmm_inputs(300, 260, 132, self_2d=True, workload=70)
+    got, ref, S, kern = run_addmm(s, a, b, 0.5, 1.5, "default")
+    assert kern == "tc3"
+    within(got, ref, S, 1e-5, "after a timeout")
