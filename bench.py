@@ -119,6 +119,22 @@ CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+def device_record(device):
+    """Name, SM count, driver and CUDA runtime of the GPU the numbers come from."""
+    import torch
+    props = torch.cuda.get_device_properties(device)
+    rec = {"name": props.name, "sms": props.multi_processor_count,
+           "cc": f"{props.major}.{props.minor}", "cuda_runtime": torch.version.cuda}
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                              "-i", str(device.index or 0)], capture_output=True, text=True,
+                             timeout=20).stdout.strip()
+        rec["driver"] = out or None
+    except (OSError, subprocess.SubprocessError):
+        rec["driver"] = None
+    return rec
+
+
 class ClockSampler:
     def __init__(self, gpu_index: int):
         self.path = tempfile.mktemp(prefix="imc_clocks_", suffix=".csv")
@@ -360,6 +376,7 @@ def run_gpu(args):
         "gpu_launches": launches,
         "conv_gemm_vs_direct": direct,
         "clocks": clocks,
+        "device": device_record(device),
         "watchdog": status,
     }
     if not args.no_cpu_baseline:
