@@ -44,7 +44,10 @@ def build(force: bool = False, extra_flags=(), out_path: str | None = None) -> s
              or os.path.getmtime(out_path) < max(os.path.getmtime(_SRC), os.path.getmtime(_HDR)))
     if force or stale:
         tmp = out_path + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", *extra_flags,
+        # -ffp-contract=off: no fused multiply-adds, so the fp32 loop rounds
+        # every product and every partial sum to fp32 on any host
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+               *extra_flags,
                "-o", tmp, _SRC, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, out_path)

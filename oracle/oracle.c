@@ -21,7 +21,8 @@
  *   1 addmm subtracts products      2 addmm drops beta*self
  *   3 addmm ignores self_2d         4 conv uses dH on the width axis
  *   5 conv drops the bias           6 conv shifts ih by one
- *   7 conv output size misses -1    8 S sums signed products */
+ *   7 conv output size misses -1    8 S sums signed products
+ *   9 the fp32 loop accumulates in fp64 */
 #ifndef ORACLE_PLANT
 #define ORACLE_PLANT 0
 #endif
@@ -146,7 +147,11 @@ int oracle_addmm_fp32_naive(const float* self, int self_2d, const float* mat1,
     if (M < 0 || N < 0 || K < 0 || !self || !mat1 || !mat2 || !out) return ORACLE_EARG;
     for (int64_t i = 0; i < M; ++i)
         for (int64_t j = 0; j < N; ++j) {
+#if ORACLE_PLANT == 9
+            double acc = 0.0;
+#else
             float acc = 0.0f;
+#endif
             for (int64_t k = 0; k < K; ++k) acc += mat1[i * K + k] * mat2[k * N + j];
             float sv = self_2d ? self[i * N + j] : self[j];
             out[i * N + j] = beta * sv + alpha * acc;

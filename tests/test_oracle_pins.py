@@ -134,6 +134,32 @@ def pin_addmm_rows(L):
     assert np.array_equal(part, full[rows]) and np.array_equal(pS, fS[rows])
 
 
+def pin_addmm_fp32_naive_rounds_in_fp32(L):
+    # 2^24 + 1 is not an fp32 number: one fp32 accumulator loses the 1 that a
+    # wider sum keeps, so the terms 2^24, 1, -2^24 (in k order) sum to 0 in
+    # fp32 and to 1 in fp64
+    a = np.array([[2.0 ** 24, 1.0, -(2.0 ** 24)]], np.float32)
+    b = np.ones((3, 1), np.float32)
+    got = oracle.addmm_fp32_naive(np.zeros(1, np.float32), a, b, _lib=L)
+    assert got.dtype == np.float32 and got[0, 0] == 0.0, got
+    # bit for bit against a sequential loop of np.float32 operations: every
+    # product, partial sum and epilogue term rounded to fp32, terms in k order
+    M, K, N = 5, 37, 6
+    a, b = _rand(M, K), _rand(K, N)
+    for self_2d, alpha, beta in [(False, 1.0, 1.0), (True, 2.0, 0.5), (True, -0.75, 1.25)]:
+        s = _rand(M, N) if self_2d else _rand(N)
+        got = oracle.addmm_fp32_naive(s, a, b, beta=beta, alpha=alpha, _lib=L)
+        want = np.empty((M, N), np.float32)
+        for i in range(M):
+            for j in range(N):
+                acc = np.float32(0.0)
+                for k in range(K):
+                    acc = np.float32(acc + np.float32(a[i, k] * b[k, j]))
+                sv = s[i, j] if self_2d else s[j]
+                want[i, j] = np.float32(np.float32(beta) * sv) + np.float32(np.float32(alpha) * acc)
+        assert np.array_equal(got, want), np.abs(got - want).max()
+
+
 CONV_SHAPES = [
     # B, IC, H, W, OC, KH, KW, stride, pad, dil
     (2, 3, 7, 7, 4, 3, 3, (1, 1), (1, 1), (1, 1)),
@@ -304,7 +330,8 @@ def test_synth_streams_are_distinct_and_stable():
 PLANTS = {1: "addmm subtracts products", 2: "addmm drops beta*self",
           3: "addmm ignores self_2d", 4: "conv uses dH on the width axis",
           5: "conv drops the bias", 6: "conv shifts ih by one",
-          7: "conv output size misses -1", 8: "S sums signed products"}
+          7: "conv output size misses -1", 8: "S sums signed products",
+          9: "fp32 loop accumulates in fp64"}
 
 
 @pytest.mark.parametrize("plant", sorted(PLANTS), ids=lambda n: PLANTS[n].replace(" ", "_"))
