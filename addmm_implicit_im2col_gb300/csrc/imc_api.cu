@@ -699,6 +699,13 @@ int imc_release_memory(void) {
 // Hooks for the fixed-scratch addmm entry point (noalloc.cu).
 namespace imc {
 
+int gemm_check_args(const float* self, int self_2d, const float* mat1, const float* mat2,
+                    float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                    int mode) {
+  return gemm_impl(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, false, nullptr, 0,
+                   false, nullptr, true);
+}
+
 size_t gemm_scratch_needed(const float* mat1, int64_t M, int64_t N, int64_t K, double alpha,
                            int mode_arg) {
   if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;

@@ -84,9 +84,14 @@ cudaError_t gemm_take_watchdog(int* value);
 cudaError_t launch_wait_selftest(int limit_us, cudaStream_t s);
 cudaError_t conv_take_watchdog(int* value);
 
-// Used by the fixed-scratch addmm entry point: the scratch bytes the call
-// with these arguments would use (0 when no tensor-core kernel runs), the
-// addmm itself on a caller-held scratch buffer, and the device check.
+// Used by the fixed-scratch addmm entry point: the argument checks of
+// gemm_addmm_f32_ex alone (host only, no CUDA call; IMC_OK or its status),
+// the scratch bytes the call with these arguments would use (0 when no
+// tensor-core kernel runs), the addmm itself on a caller-held scratch
+// buffer, and the device check.
+int gemm_check_args(const float* self, int self_2d, const float* mat1, const float* mat2,
+                    float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
+                    int mode);
 size_t gemm_scratch_needed(const float* mat1, int64_t M, int64_t N, int64_t K, double alpha,
                            int mode);
 int gemm_with_scratch(const float* self, int self_2d, const float* mat1, const float* mat2,

@@ -12,12 +12,16 @@
 //
 // The scratch (mat2 transposed and split into TF32 hi / lo parts, the same
 // data the pool-backed path builds) lives in the file-scope device array
-// below.  Every GPU that loads the library holds those kNoallocScratchBytes
-// until the process exits.  Host code cannot use the array's name as a device
-// address, so the first call on each device looks the address up with
-// cudaGetSymbolAddress (with that device current) and caches it.
+// below.  Every GPU that loads this file's device code holds those
+// kNoallocScratchBytes until the process exits.  With CUDA's lazy module
+// loading (the default) that load -- and so the reservation of the buffer --
+// happens the first time the array is used on a device: the first call of
+// this entry point there, which is its set-up.  Host code cannot use the
+// array's name as a device address, so every call looks the address up with
+// cudaGetSymbolAddress on the current device (after the first call this only
+// reads the loaded module's symbol table; it allocates nothing), which also
+// keeps the address right if the program resets the device in between.
 #include <cmath>
-#include <mutex>
 
 #include "imc.h"
 #include "imc_internal.cuh"
@@ -30,28 +34,15 @@ static_assert(kNoallocScratchBytes == IMC_NOALLOC_SCRATCH_BYTES, "header and lib
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices];
-
-// Device address of g_noalloc_scratch on the current device (set-up on the
-// first call per device).  IMC_OK, IMC_ERR_DEVICE or IMC_ERR_CUDA.
+// Device address of g_noalloc_scratch on the current device.  IMC_OK or
+// IMC_ERR_CUDA.
 int scratch_address(void** ptr) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
     cudaGetLastError();
-    return IMC_ERR_DEVICE;
+    return IMC_ERR_CUDA;
   }
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-      cudaGetLastError();
-      return IMC_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = p;
-  }
-  *ptr = g_scratch_ptr[dev];
+  *ptr = p;
   return IMC_OK;
 }
 
@@ -63,19 +54,17 @@ extern "C" int gemm_addmm_f32_noalloc(const float* self, int self_2d, const floa
                                       int64_t K, double beta, double alpha, int mode,
                                       void* stream) {
   using namespace imc;
-  // Size check first, so that an oversized problem is rejected before any
-  // CUDA call.  Nothing in the buffer needs clearing: the mat2 pre-pass
-  // writes every element the main kernel reads.
+  // 1. The argument checks of gemm_addmm_f32_ex, on the host, in its order
+  //    (flags, scalars, sizes, pointers, overlaps); no CUDA call.
+  const int v = gemm_check_args(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode);
+  if (v != IMC_OK) return v;
+  // 2. The size check against the fixed buffer, still before any CUDA call.
+  //    Nothing in the buffer needs clearing: the mat2 pre-pass writes every
+  //    element the main kernel reads, and split-K partial sums are written
+  //    in full before they are summed.
   const size_t need = gemm_scratch_needed(mat1, M, N, K, alpha, mode);
   if (need > kNoallocScratchBytes) return IMC_ERR_SCRATCH;
-  // The argument errors gemm_addmm_f32_ex reports before touching the device
-  // come first here too (the scratch set-up below needs the device).
-  if (need > 0) {
-    if (self_2d != 0 && self_2d != 1) return IMC_ERR_ARG;
-    if (!std::isfinite(beta) || !std::isfinite(alpha)) return IMC_ERR_ARG;
-    if (!out || !mat1 || !mat2 || (beta != 0.0 && !self)) return IMC_ERR_NULL;
-  }
-  if (need == 0)  // SIMT, epilogue-only or invalid arguments: no scratch involved
+  if (need == 0)  // SIMT, epilogue-only or empty: no scratch involved
     return gemm_with_scratch(self, self_2d, mat1, mat2, out, M, N, K, beta, alpha, mode, nullptr,
                              0, stream);
   const int dev = require_device();

@@ -200,21 +200,39 @@ int conv2d_gemm_f32_nd(const float* x, const float* w, const float* bias, float*
  * fail under memory pressure mid-run.  Inputs and output are still the
  * caller's.  The tensor-core path's scratch (mat2 transposed, split into hi /
  * lo parts) lives in a fixed device buffer of IMC_NOALLOC_SCRATCH_BYTES
- * inside the library, which every GPU that loads the library holds until the
- * process exits; no call allocates or frees anything.
+ * inside the library, which every GPU that loads it holds until the process
+ * exits; no call takes memory from a pool or frees any.
  *
  * Limit: a problem whose mat2 copy alone would exceed
  * IMC_NOALLOC_SCRATCH_BYTES -- N*K above 4 Mi elements in the default mode,
  * 8 Mi in IMC_MODE_TF32 -- returns IMC_ERR_SCRATCH before any CUDA call; the
  * kernel plans its split-K partial sums within what is left of the buffer.
  * Problems that take the SIMT kernel need no scratch.
- * Set-up: the first call on a device looks up the buffer's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before capturing any stream.
- * Sharing: every call uses the same buffer.  Nothing in it needs to start at
- * zero (each call writes all it reads), but calls whose work overlaps on the
- * GPU -- on different streams, or from different host threads -- race on it.
- * Other arguments, status codes and results are those of gemm_addmm_f32_ex.
+ * Order of checks: the argument checks of gemm_addmm_f32_ex come first (the
+ * same statuses in the same order, IMC_ERR_ARG, IMC_ERR_SHAPE, IMC_ERR_NULL,
+ * IMC_ERR_ALIAS), then the size check (IMC_ERR_SCRATCH); none of them makes
+ * a CUDA call.
+ * Set-up, and when the buffer is reserved: CUDA loads a library's device
+ * code into each device's memory when it is first used there (lazy module
+ * loading, the default), and the buffer is part of that code's image.  So
+ * the FIRST call on a device is the set-up: it loads the buffer (reserving
+ * IMC_NOALLOC_SCRATCH_BYTES of device memory at that moment, which can fail
+ * with IMC_ERR_CUDA if the device is full) and looks its address up with
+ * cudaGetSymbolAddress, with that device current.  The same holds for the
+ * code of each kernel the first time it runs.  Make the first calls -- one
+ * per shape class and mode the program will use -- at start-up, before any
+ * memory budget is fixed and before any stream is captured, or set the
+ * environment variable CUDA_MODULE_LOADING=EAGER before the process
+ * initialises CUDA, so that everything is loaded when the context is made.
+ * After the set-up, calls allocate nothing (each looks the address up again,
+ * which only reads the loaded code's symbol table).
+ * Sharing: every call uses the same buffer, which keeps what the last call
+ * left in it.  Nothing in it needs to start at zero (each call writes all it
+ * reads before reading it), but calls whose work overlaps on the GPU -- on
+ * different streams, or from different host threads -- race on it.
+ * Other arguments, status codes and results are those of gemm_addmm_f32_ex;
+ * the results equal, bit for bit, those of gemm_addmm_f32_ws given a
+ * workspace of IMC_NOALLOC_SCRATCH_BYTES (the same plan runs).
  */
 #define IMC_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int gemm_addmm_f32_noalloc(const float* self, int self_2d, const float* mat1, const float* mat2,
