@@ -15,8 +15,13 @@ write) before every step, outside the step's own CUDA events.
 
 Under torchrun every rank runs the same per-GPU step on its own GPU (weak
 scaling, no collective on the data path); rank 0 prints one JSON line.
+``--gpus N`` with N > 1 outside torchrun starts the N ranks itself (one
+process per GPU through torch.distributed.run on 127.0.0.1).
 ``--impl reference`` times the CPU oracle (fp64, the plain definition) on a
 bounded sample of the same workload instead.
+After the timed steps the same step is repeated back to back for
+``--sustain-seconds`` (default 3 s) and reported as the sustained rate with the
+SM clock sampled during it.
 """
 from __future__ import annotations
 
@@ -46,6 +51,10 @@ FLUSH_BYTES = 256 << 20
 # Nominal dense TF32 / BF16 tensor throughput of the GB300 (1.1 vs 2.25 PFLOP/s).
 TF32_PER_BF16 = 1.1 / 2.25
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# tcgen05.mma kind::tf32 multiply-adds per clock per SM, measured on GB300 with
+# back-to-back 128x256x8 MMAs (a probe outside the product); times the SM
+# count and the SM clock sampled during the run it gives a clock-true peak.
+TF32_MAC_PER_CLK_SM = 2047.0
 
 
 def addmm_flops(M, N, K):
@@ -74,6 +83,12 @@ def roofline_peaks(peaks):
     return tf32 / 3.0, tf32, peaks["hbm_gbs"]
 
 
+def probe_peak_3xtf32(sms: int, sm_mhz: float) -> float:
+    """3xTF32 peak in TFLOP/s of metric flops from the probed MMA rate at the
+    given SM count and clock (three MMAs per product)."""
+    return TF32_MAC_PER_CLK_SM * 2.0 * sms * sm_mhz * 1e6 / 3.0 / 1e12
+
+
 # ------------------------------------------------------------ distributed
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -88,6 +103,26 @@ def init_dist(ws, backend):
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         dist.init_process_group(backend=backend)
     return dist if ws > 1 else None
+
+
+def _free_port() -> int:
+    import socket
+    sk = socket.socket()
+    sk.bind(("127.0.0.1", 0))
+    port = sk.getsockname()[1]
+    sk.close()
+    return port
+
+
+def launch_ranks(n: int, argv, script: str | None = None) -> int:
+    """Runs `script` (this file by default) as n ranks on one node, one
+    process per GPU, through torch.distributed.run with its rendezvous on
+    127.0.0.1; returns the exit status.  The ranks inherit stdout, so rank 0's
+    JSON line is the output."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", "--master-port",
+           str(_free_port()), script or os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd).returncode
 
 
 def barrier(dist_mod, device=None):
@@ -328,6 +363,40 @@ def run_gpu(args):
         direct = {"workload": "the step's conv2d", "direct_ms": round(dm, 4),
                   "gemm_ms": round(sum(ms_conv) / len(ms_conv), 4),
                   "speedup": round(dm / (sum(ms_conv) / len(ms_conv)), 2)}
+    # ---- sustained: the same step (with its L2 flush) back to back for
+    # --sustain-seconds, long enough for the power limit to set the clock;
+    # device time of the steps from per-step events, SM clock sampled meanwhile
+    sustained = None
+    if args.sustain_seconds > 0:
+        n_sus = max(args.steps, int(np.ceil(args.sustain_seconds * 1e3 / max(ms_step, 1e-3))))
+        sampler_s = ClockSampler(local) if rank == 0 else None
+        time.sleep(0.3 if sampler_s else 0.0)
+        sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_sus)]
+        barrier(dist_mod, device)
+        torch.cuda.synchronize(device)
+        ts0 = time.time()
+        for i in range(n_sus):
+            flush.fill_(float(i))
+            sev[i][0].record(stream)
+            step()
+            sev[i][1].record(stream)
+            if i % 256 == 255:
+                sev[i][1].synchronize()  # keeps the queue of launches short
+        torch.cuda.synchronize(device)
+        ts1 = time.time()
+        barrier(dist_mod, device)
+        sus_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in sev) / n_sus, dist_mod, device)
+        clocks_s = None
+        if sampler_s:
+            time.sleep(0.1)
+            sampler_s.stop()
+            clocks_s = sampler_s.summary(ts0, ts1)
+        sustained = {"value": round(whole_job_rate(flops_step, ws, sus_ms), 1), "unit": UNIT,
+                     "ms_per_step": round(sus_ms, 4), "steps": n_sus,
+                     "wall_s": round(ts1 - ts0, 2), "clocks": clocks_s,
+                     "how": "the timed step (L2 flush outside each step's events) repeated back "
+                            "to back; device time summed over per-step CUDA events"}
     status = binding.check_device_error(None)
 
     if rank != 0:
@@ -342,6 +411,9 @@ def run_gpu(args):
     ach_a = fl_addmm / (avg_addmm * 1e-3) / 1e12
     ach_c = fl_conv / (avg_conv * 1e-3) / 1e12
     traffic = load_profiled_traffic("k_tc_gemm")
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    p_probe = probe_peak_3xtf32(sms, sm_mhz)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -357,13 +429,18 @@ def run_gpu(args):
                      "kernel": f"addmm {kern_a} (k_tc_gemm)",
                      "peak_source": f"{peak_src}: bf16 {peaks['bf16_tflops']} TFLOP/s x 1.1/2.25 "
                                     f"(nominal TF32/BF16) = {ptf32:.1f} TF32, /3 for 3xTF32",
-                     "achieved_basis": "2*M*N*K metric flops / CUDA-event average launch time"},
+                     "achieved_basis": "2*M*N*K metric flops / CUDA-event average launch time",
+                     "peak_probe": round(p_probe, 2), "frac_probe": round(ach_a / p_probe, 4),
+                     "peak_probe_basis": f"{TF32_MAC_PER_CLK_SM:.0f} MAC/clk/SM (tcgen05 kind::tf32 "
+                                         f"probe) x 2 x {sms} SMs x {sm_mhz:.0f} MHz (median SM "
+                                         f"clock sampled in the timed region) / 3"},
         "parts": {
             "addmm": {"ms": round(avg_addmm, 4), "TFLOP/s": round(ach_a, 2),
                       "frac": round(ach_a / p3, 4)},
             "conv2d": {"ms": round(avg_conv, 4), "TFLOP/s": round(ach_c, 2),
-                       "frac": round(ach_c / p3, 4)},
+                       "frac": round(ach_c / p3, 4), "frac_probe": round(ach_c / p_probe, 4)},
         },
+        "sustained": sustained,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
                 "path": "every step: gemm_addmm_f32_host + conv2d_gemm_f32_host on pinned "
@@ -379,7 +456,7 @@ def run_gpu(args):
         "device": device_record(device),
         "watchdog": status,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and ws == 1:  # the host cores' baseline is an N=1 figure
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if dist_mod is not None:
         dist_mod.destroy_process_group()
@@ -495,8 +572,14 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=1.0)
     ap.add_argument("--e2e-streams", type=int, default=3,
                     help="streams each problem's end-to-end calls rotate over")
-    args = ap.parse_args(argv)
+    ap.add_argument("--sustain-seconds", type=float, default=3.0,
+                    help="repeat the step back to back this long for the sustained rate "
+                         "(0: skip)")
+    raw = list(sys.argv[1:] if argv is None else argv)
+    args = ap.parse_args(raw)
     args.warmup = max(args.warmup, 3)  # the timing rules want at least 3 warm-up steps
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_ranks(args.gpus, raw))
     line = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if line is not None:
         print(json.dumps(line), flush=True)
