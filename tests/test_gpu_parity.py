@@ -239,9 +239,46 @@ def test_addmm_workloads(name):
 def test_addmm_large_workloads_sampled_rows(name):
     c, s, a, b = synth.make_addmm_case(name)
     rows = synth.checked_rows(name, c["M"], c["rows"])
-    got, ref, S, kern = run_addmm(s, a, b, c["beta"], c["alpha"], "default", rows=rows)
-    assert kern == "tc3"
-    within(got, ref, S, 1e-5, f"{name}")
+    ref, S = oracle.addmm(s, a, b, beta=c["beta"], alpha=c["alpha"], rows=rows,
+                          self_2d=c["self_2d"])
+    for mode in ("default", "tf32"):
+        out = binding.addmm(dev(s), dev(a), dev(b), beta=c["beta"], alpha=c["alpha"], mode=mode)
+        torch.cuda.synchronize()
+        assert binding.last_kernel() == ("tc3" if mode == "default" else "tc1")
+        within(out.cpu().numpy()[rows], ref, S, TOL[mode], f"{name} {mode}")
+        del out
+
+
+def test_exact_boundary_signatures():
+    """gemm_addmm_f32 and conv2d_gemm_f32 exactly as declared (default mode,
+    scratch from the library's stream-ordered pool), against the oracle."""
+    stream = torch.cuda.current_stream().cuda_stream
+    for M, N, K, self_2d, beta, alpha in [(600, 520, 388, 1, 0.5, 1.5),
+                                          (1000, 2304, 768, 0, 1.0, 1.0)]:
+        s, a, b = synth.addmm_inputs(M, N, K, self_2d=bool(self_2d), workload=90 + M)
+        S, A, B = dev(s), dev(a), dev(b)
+        out = torch.full((M, N), float("nan"), device="cuda")
+        rc = binding.gemm_addmm_f32(S.data_ptr(), self_2d, A.data_ptr(), B.data_ptr(),
+                                    out.data_ptr(), M, N, K, beta, alpha, stream)
+        assert rc == binding.IMC_OK, binding.status_string(rc)
+        assert binding.last_kernel() == "tc3"
+        torch.cuda.synchronize()
+        ref, Sr = oracle.addmm(s, a, b, beta=beta, alpha=alpha)
+        within(out.cpu().numpy(), ref, Sr, 1e-5, f"gemm_addmm_f32 {M}x{N}x{K}")
+    for (Bn, IC, H, W, OC, KH, KW, st, pd, dl) in [(2, 16, 20, 20, 130, 3, 3, 2, 1, 1),
+                                                   (1, 3, 96, 96, 128, 7, 7, 4, 3, 1)]:
+        x, w, bias = synth.conv_inputs(Bn, IC, H, W, OC, KH, KW, workload=95 + IC)
+        X, Wt, Bias = dev(x), dev(w), dev(bias)
+        OH = (H + 2 * pd - dl * (KH - 1) - 1) // st + 1
+        OW = (W + 2 * pd - dl * (KW - 1) - 1) // st + 1
+        y = torch.full((Bn, OC, OH, OW), float("nan"), device="cuda")
+        rc = binding.conv2d_gemm_f32(X.data_ptr(), Wt.data_ptr(), Bias.data_ptr(), y.data_ptr(),
+                                     Bn, IC, H, W, OC, KH, KW, st, pd, dl, stream)
+        assert rc == binding.IMC_OK, binding.status_string(rc)
+        assert binding.last_kernel() == "tc3"
+        torch.cuda.synchronize()
+        ref, Sr = oracle.conv2d(x, w, bias, st, pd, dl)
+        within(y.cpu().numpy(), ref, Sr, 1e-5, f"conv2d_gemm_f32 {Bn}x{IC}x{H}x{W}->{OC}")
 
 
 # ------------------------------------------------------------------- conv
