@@ -265,7 +265,7 @@ def test_exact_boundary_signatures():
         torch.cuda.synchronize()
         ref, Sr = oracle.addmm(s, a, b, beta=beta, alpha=alpha)
         within(out.cpu().numpy(), ref, Sr, 1e-5, f"gemm_addmm_f32 {M}x{N}x{K}")
-    for (Bn, IC, H, W, OC, KH, KW, st, pd, dl) in [(2, 16, 20, 20, 130, 3, 3, 2, 1, 1),
+    for (Bn, IC, H, W, OC, KH, KW, st, pd, dl) in [(2, 16, 40, 40, 130, 3, 3, 2, 1, 1),
                                                    (1, 3, 96, 96, 128, 7, 7, 4, 3, 1)]:
         x, w, bias = synth.conv_inputs(Bn, IC, H, W, OC, KH, KW, workload=95 + IC)
         X, Wt, Bias = dev(x), dev(w), dev(bias)
