@@ -56,6 +56,7 @@ SIGNATURES = {
     "conv2d_gemm_f32_host": (_int, [_vp, _vp, _vp, _vp] + [_i64] * 13 + [_int, _vp]),
     "imc_status_string": (ctypes.c_char_p, [_int]),
     "imc_last_kernel": (_int, []),
+    "imc_last_kernel_name": (ctypes.c_char_p, []),
     "imc_launch_count": (ctypes.c_uint64, []),
     "imc_check_device_error": (_int, [_vp]),
     "imc_version": (_int, []),
@@ -188,6 +189,11 @@ def status_string(status: int) -> str:
 
 def last_kernel() -> str:
     return KERNELS.get(load().imc_last_kernel(), "unknown")
+
+
+def last_kernel_name() -> str:
+    """Name and form of the main kernel of this thread's last successful call."""
+    return load().imc_last_kernel_name().decode()
 
 
 def launch_count() -> int:

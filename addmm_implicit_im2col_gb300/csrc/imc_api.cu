@@ -21,8 +21,11 @@ namespace imc {
 
 static std::atomic<uint64_t> g_launches{0};
 static thread_local int t_last_kernel = IMC_KERNEL_NONE;
+static thread_local const char* t_last_name = "none";
+static thread_local const char* t_pending_name = "none";
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+void note_kernel_name(const char* name) { t_pending_name = name; }
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -70,7 +73,13 @@ constexpr int64_t kTinyMacs = int64_t(1) << 22;
 int finish(cudaError_t e, int kernel) {
   if (e != cudaSuccess) return IMC_ERR_CUDA;
   t_last_kernel = kernel;
+  t_last_name = t_pending_name;
   return IMC_OK;
+}
+
+void set_none() {
+  t_last_kernel = IMC_KERNEL_NONE;
+  t_last_name = "none";
 }
 
 // The library's stream-ordered memory pool of each device, created on first
@@ -172,7 +181,7 @@ int gemm_impl(const float* self, int self_2d, const float* mat1, const float* ma
   if (!std::isfinite(beta) || !std::isfinite(alpha)) return IMC_ERR_ARG;
   if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return IMC_ERR_SHAPE;
   if (M == 0 || N == 0) {
-    t_last_kernel = IMC_KERNEL_NONE;
+    set_none();
     return IMC_OK;
   }
   const bool read_self = beta != 0.0;
@@ -399,7 +408,7 @@ int conv_impl(const float* x, const float* w, const float* bias, float* out, int
   const int sh = conv_shape(B, IC, H, W, OC, KH, KW, sH, sW, pH, pW, dH, dW, &cs);
   if (sh != IMC_OK) return sh;
   if (B == 0 || OC == 0) {
-    t_last_kernel = IMC_KERNEL_NONE;
+    set_none();
     return IMC_OK;
   }
   const int64_t K = cs.K, OH = cs.OH, OW = cs.OW;
@@ -664,6 +673,8 @@ const char* imc_status_string(int status) {
 }
 
 int imc_last_kernel(void) { return t_last_kernel; }
+
+const char* imc_last_kernel_name(void) { return t_last_name; }
 
 uint64_t imc_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

@@ -104,6 +104,9 @@ int device_sm_count();
 
 // Counts one kernel launch (for imc_launch_count()).
 void note_launch();
+// Names the main kernel of the call in progress (imc_last_kernel_name()
+// reports it once the call succeeds); a static string.
+void note_kernel_name(const char* name);
 
 // Launches `kernel` so that it may start while the previous kernel of the
 // stream (issued by the same call) is still running; the kernel calls

@@ -263,12 +263,14 @@ cudaError_t launch_simt_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.M * a.N <= kSmallOutputs && a.K <= kSmallK) {
     k_simt_small<<<(unsigned)((a.M * a.N + 255) / 256), 256, 0, s>>>(a);
     note_launch();
+    note_kernel_name("k_simt_small");
     return cudaGetLastError();
   }
   unsigned grid;
   if (!simt_grid(a.M, a.N, &grid)) return cudaErrorInvalidConfiguration;
   k_simt<GemmOperands><<<grid, THREADS, 0, s>>>(GemmOperands{a});
   note_launch();
+  note_kernel_name("k_simt<gemm>");
   return cudaGetLastError();
 }
 
@@ -277,12 +279,14 @@ cudaError_t launch_simt_conv(const ConvArgs& c, cudaStream_t s) {
   if (!simt_grid(c.M, c.N, &grid)) return cudaErrorInvalidConfiguration;
   k_simt<ConvOperands><<<grid, THREADS, 0, s>>>(ConvOperands{c});
   note_launch();
+  note_kernel_name("k_simt<conv>");
   return cudaGetLastError();
 }
 
 cudaError_t launch_fill_gemm(const GemmArgs& a, cudaStream_t s) {
   k_fill_gemm<<<fill_blocks(a.M * a.N), 256, 0, s>>>(a);
   note_launch();
+  note_kernel_name("k_fill_gemm");
   return cudaGetLastError();
 }
 
@@ -295,12 +299,14 @@ cudaError_t launch_direct_conv(const ConvArgs& c, cudaStream_t s) {
   else
     k_direct_conv<false><<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(c);
   note_launch();
+  note_kernel_name("k_direct_conv");
   return cudaGetLastError();
 }
 
 cudaError_t launch_fill_conv(const ConvArgs& c, cudaStream_t s) {
   k_fill_conv<<<fill_blocks((int64_t)c.B * c.OC * c.OH * c.OW), 256, 0, s>>>(c);
   note_launch();
+  note_kernel_name("k_fill_conv");
   return cudaGetLastError();
 }
 

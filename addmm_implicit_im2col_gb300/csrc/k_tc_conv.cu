@@ -760,6 +760,7 @@ cudaError_t run(const ConvArgs& c, Plan pl, const float* w_hi, const float* w_lo
   cudaError_t e = ic_fastest(c) ? launch_main<THREE, true>(c, pl, th, tl, to, grid, s)
                                 : launch_main<THREE, false>(c, pl, th, tl, to, grid, s);
   note_launch();
+  note_kernel_name(THREE ? "k_tc_conv<3xtf32>" : "k_tc_conv<1xtf32>");
   if (e != cudaSuccess || pl.tail == 0) return e;
   const int64_t threads = (int64_t)pl.tail * pl.q.bn * 32;
   e = launch_after_previous(k_conv_tail, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0,

@@ -745,6 +745,7 @@ cudaError_t run(const GemmArgs& g, const Plan& p, const float* bt_hi, const floa
     e = cudaGetLastError();
   }
   note_launch();
+  note_kernel_name(TS ? "k_tc_gemm<3xtf32,a_tmem>" : (THREE ? "k_tc_gemm<3xtf32>" : "k_tc_gemm<1xtf32>"));
   if (e != cudaSuccess || p.splits == 1) return e;
   const int64_t items = g.vec_out ? g.M * g.N / 4 : g.M * g.N;
   const int64_t cap = (int64_t)sms * 8, blocks = (items + 255) / 256;

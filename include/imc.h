@@ -319,6 +319,12 @@ const char* imc_status_string(int status);
  * call launched. */
 int imc_last_kernel(void);
 
+/* Name of the main kernel the calling host thread's last successful call
+ * launched, with its form, e.g. "k_tc_gemm<3xtf32,a_tmem>",
+ * "k_tc_conv<3xtf32>", "k_simt_small"; "none" when nothing ran.  A static
+ * string, never NULL. */
+const char* imc_last_kernel_name(void);
+
 /* Number of kernels this library has launched in this process. */
 uint64_t imc_launch_count(void);
 

@@ -414,6 +414,7 @@ def test_conv_workloads(name):
     for mode in ("default", "tf32"):
         got, ref, S, kern = run_conv(x, w, b, c["stride"], c["pad"], c["dilation"], mode)
         assert kern == ("tc3" if mode == "default" else "tc1")
+        assert binding.last_kernel_name().startswith("k_tc_conv<"), binding.last_kernel_name()
         within(got, ref, S, TOL[mode], f"{name} {mode}")
 
 
