@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     k_tc_conv(const __grid_constant__ CUtensorMap tmWh, const __grid_constant__ CUtensorMap tmWl,
               const __grid_constant__ CUtensorMap tmO, const ConvArgs c, const Sched q) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = smem_align1024(smem_raw);
   const int b_tile = q.bn * BK * 4;  // one weight tile (hi or lo)
   // [weight stages][tap table][epilogue staging][barriers]
   int2* tab = reinterpret_cast<int2*>(smem + q.stages * q.w_bytes);
