@@ -81,10 +81,6 @@ static_assert(TS_A_COL0 + kLts.stages * TS_A_STAGE_COLS <= TMEM_COLS, "TMEM");
 // when the epilogue reads an [M,N] self (measured on 32768x1024x1024: 305 us
 // with the double-buffered form, 443 us with this one), cheap otherwise.
 constexpr int kTsMinKb = 96, kTsMinKbLightEpilogue = 32;
-// k-blocks the split warps of the A-from-TMEM form write before they wait for
-// their TMEM stores and hand the k-blocks to the MMA (fewer than the stages)
-constexpr int kSplitGroup = 1;
-static_assert(kSplitGroup < kLts.stages, "the split warps need a free stage per grouped k-block");
 
 __device__ int g_watchdog_gemm;
 
@@ -497,10 +493,7 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
     // ------------------------------- split warps: A_hi / A_lo into TMEM
     // Thread = row r of the A tile (TMEM lane r): its 16 values of a k-block
     // are read from the swizzled tile, split, and written to the stage's
-    // TMEM columns.  The stores of kSplitGroup k-blocks are waited for
-    // together, then the warp arrives on each of their split[] barriers: a
-    // warp waiting for its TMEM stores after every k-block took ~900 clk per
-    // k-block, more than the k-block's MMAs.
+    // TMEM columns; one arrival per warp on split[s].
     const int r = (warp & 3) * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TS_A_COL0;
     int s = 0;
@@ -508,47 +501,35 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       bool ok = true;
       const int kb0 = (u / num_tiles) * kps, kb1 = min(num_kb, kb0 + kps);
-      for (int kb = kb0; kb < kb1 && ok; kb += kSplitGroup) {
-        const int n = min(kSplitGroup, kb1 - kb);
-        int done[kSplitGroup];
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd) ||
+            !warp_wait_bar(&ctl->full[s], ph, abort, kSiteSplitFull, wd)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint8_t* row = smem + s * L.bytes + L.a + sw64_row_base(r);
+        float hi[16], lo[16];
 #pragma unroll
-        for (int g = 0; g < kSplitGroup; ++g) {
-          if (g >= n) break;
-          if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd) ||
-              !warp_wait_bar(&ctl->full[s], ph, abort, kSiteSplitFull, wd)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint8_t* row = smem + s * L.bytes + L.a + sw64_row_base(r);
-          float hi[16], lo[16];
+        for (int j = 0; j < 4; ++j) {
+          const float4 v = *reinterpret_cast<const float4*>(row + sw64_unit(r, j));
+          const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float4 v = *reinterpret_cast<const float4*>(row + sw64_unit(r, j));
-            const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              hi[4 * j + e] = tf32_hi(vv[e]);
-              lo[4 * j + e] = tf32_lo(vv[e]);
-            }
-          }
-          const uint32_t ta = trow + (uint32_t)s * TS_A_STAGE_COLS;
-          ptx::tmem_st16(ta, hi);
-          ptx::tmem_st16(ta + 16, lo);
-          done[g] = s;
-          if (++s == L.stages) {
-            s = 0;
-            ph ^= 1u;
+          for (int e = 0; e < 4; ++e) {
+            hi[4 * j + e] = tf32_hi(vv[e]);
+            lo[4 * j + e] = tf32_lo(vv[e]);
           }
         }
-        if (!ok) break;
+        const uint32_t ta = trow + (uint32_t)s * TS_A_STAGE_COLS;
+        ptx::tmem_st16(ta, hi);
+        ptx::tmem_st16(ta + 16, lo);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-#pragma unroll
-          for (int g = 0; g < kSplitGroup; ++g)
-            if (g < n) ptx::mbar_arrive(&ctl->split[done[g]]);
+        if (lane == 0) ptx::mbar_arrive(&ctl->split[s]);
+        if (++s == L.stages) {
+          s = 0;
+          ph ^= 1u;
         }
       }
       if (!ok) break;
