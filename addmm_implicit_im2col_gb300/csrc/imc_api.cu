@@ -153,7 +153,8 @@ bool parse_mode(int mode, bool conv, int* base, int* relu) {
 }
 
 // Which kernel a well-formed addmm takes.  `tc_ok` is whether the tcgen05
-// path can take the operands (K % 4 == 0, aligned mat1).
+// path can take the operands (it reads operands whose rows are not 16-byte
+// aligned through padded copies in its scratch, so: whether they are read).
 int plan_gemm(int64_t M, int64_t N, int64_t K, double alpha, int mode, bool tc_ok) {
   if (M == 0 || N == 0) return IMC_KERNEL_NONE;
   if (alpha == 0.0 || K == 0) return IMC_KERNEL_FILL;
@@ -216,17 +217,30 @@ int gemm_impl(const float* self, int self_2d, const float* mat1, const float* ma
   a.vec_out = (N % 4 == 0) && aligned16(out) && (!read_self || aligned16(self)) ? 1 : 0;
   a.relu = relu;
   a.b_kmajor = b_kmajor ? 1 : 0;
-  const bool tc_ok = read_ops && K % 4 == 0 &&
-                     (validate_only || (aligned16(mat1) && (!b_kmajor || aligned16(mat2))));
-  const int kernel = plan_gemm(M, N, K, alpha, mode, tc_ok);
+  const bool tc_ok = read_ops;
+  int kernel = plan_gemm(M, N, K, alpha, mode, tc_ok);
   if (kernel < 0) return IMC_ERR_SHAPE;
   if (validate_only) return IMC_OK;
-  const bool tc = kernel == IMC_KERNEL_TC3 || kernel == IMC_KERNEL_TC1;
+  bool tc = kernel == IMC_KERNEL_TC3 || kernel == IMC_KERNEL_TC1;
   const bool three = kernel == IMC_KERNEL_TC3;
+  // operand copies with aligned rows: from K alone, or also from the pointers
+  const bool pad_a = tc_gemm_pad_a(a), pad_b = tc_gemm_pad_b(a);
+  const bool pad_a_k = K % 4 != 0, pad_b_k = b_kmajor && K % 4 != 0;
+  // A caller workspace sized by the size query (which assumes 16-byte aligned
+  // pointers) may lack room for the copies an unaligned operand needs: such a
+  // call takes the SIMT kernel, unless a tensor-core mode was forced.
+  if (tc && caller_ws && (pad_a != pad_a_k || pad_b != pad_b_k) &&
+      ws_bytes < tc_gemm_workspace_bytes(M, N, K, three, b_kmajor, pad_a, pad_b, 0) &&
+      mode != IMC_MODE_FORCE_TC3 && mode != IMC_MODE_FORCE_TC1) {
+    kernel = IMC_KERNEL_SIMT;
+    tc = false;
+  }
   // minimum (no split-K) and the scratch the call will use
-  const size_t need_min = tc ? tc_gemm_workspace_bytes(M, N, K, three, b_kmajor, 0) : 0;
-  const size_t need =
-      tc ? tc_gemm_workspace_bytes(M, N, K, three, b_kmajor, caller_ws ? ws_bytes : SIZE_MAX) : 0;
+  const size_t need_min =
+      tc ? tc_gemm_workspace_bytes(M, N, K, three, b_kmajor, pad_a, pad_b, 0) : 0;
+  const size_t need = tc ? tc_gemm_workspace_bytes(M, N, K, three, b_kmajor, pad_a, pad_b,
+                                                   caller_ws ? ws_bytes : SIZE_MAX)
+                         : 0;
   if (caller_ws && need_min > 0) {
     if (!workspace || ws_bytes < need_min || !aligned16(workspace)) return IMC_ERR_ARG;
     if (overlaps(workspace, need, out, out_bytes) || overlaps(workspace, need, mat1, mat1_bytes) ||
@@ -284,9 +298,13 @@ size_t gemm_query(int64_t M, int64_t N, int64_t K, int mode_arg, bool b_kmajor) 
   if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
   int mode = 0, relu = 0;
   if (!parse_mode(mode_arg, false, &mode, &relu)) return 0;
-  const int kernel = plan_gemm(M, N, K, 1.0, mode, K % 4 == 0);
-  if (kernel == IMC_KERNEL_TC3) return tc_gemm_workspace_bytes(M, N, K, true, b_kmajor, SIZE_MAX);
-  if (kernel == IMC_KERNEL_TC1) return tc_gemm_workspace_bytes(M, N, K, false, b_kmajor, SIZE_MAX);
+  const int kernel = plan_gemm(M, N, K, 1.0, mode, true);
+  // pointers taken as 16-byte aligned: copies only when K % 4 != 0
+  const bool pad_a = K % 4 != 0, pad_b = b_kmajor && K % 4 != 0;
+  if (kernel == IMC_KERNEL_TC3)
+    return tc_gemm_workspace_bytes(M, N, K, true, b_kmajor, pad_a, pad_b, SIZE_MAX);
+  if (kernel == IMC_KERNEL_TC1)
+    return tc_gemm_workspace_bytes(M, N, K, false, b_kmajor, pad_a, pad_b, SIZE_MAX);
   return 0;
 }
 }  // namespace
@@ -722,10 +740,10 @@ size_t gemm_scratch_needed(const float* mat1, int64_t M, int64_t N, int64_t K, d
   if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
   int mode = 0, relu = 0;
   if (!parse_mode(mode_arg, false, &mode, &relu)) return 0;
-  const bool tc_ok = alpha != 0.0 && K % 4 == 0 && aligned16(mat1);
-  const int kernel = plan_gemm(M, N, K, alpha, mode, tc_ok);
+  const int kernel = plan_gemm(M, N, K, alpha, mode, alpha != 0.0);
   if (kernel != IMC_KERNEL_TC3 && kernel != IMC_KERNEL_TC1) return 0;
-  return tc_gemm_workspace_bytes(M, N, K, kernel == IMC_KERNEL_TC3, false, 0);
+  const bool pad_a = K % 4 != 0 || !aligned16(mat1);
+  return tc_gemm_workspace_bytes(M, N, K, kernel == IMC_KERNEL_TC3, false, pad_a, false, 0);
 }
 
 int gemm_with_scratch(const float* self, int self_2d, const float* mat1, const float* mat2,

@@ -53,15 +53,19 @@ cudaError_t launch_direct_conv(const ConvArgs& a, cudaStream_t s);
 // tcgen05 tensor-core kernels.  three_pass selects 3xTF32 (fp32 accuracy)
 // over a single TF32 product.  Return cudaErrorNotSupported when the shape
 // does not meet the kernel's requirements (the caller falls back to SIMT).
-// The addmm kernel needs a 16-byte aligned workspace for the transposed mat2
-// and, for problems with few output tiles, split-K partial sums; it is dead
-// once the launch completes.  tc_gemm_workspace_bytes(.., limit) is the size
-// of the best plan whose scratch fits in `limit` bytes: SIZE_MAX gives the
-// preferred size, 0 the minimum (no split-K); launch_tc_gemm plans within the
-// workspace it is given.
+// The addmm kernel needs a 16-byte aligned workspace for the transposed mat2,
+// a copy of mat1 with 16-byte aligned rows when its rows are not (pad_a:
+// K % 4 != 0 or an unaligned mat1; pad_b likewise for a K-major linear
+// weight) and, for problems with few output tiles, split-K partial sums; it
+// is dead once the launch completes.  tc_gemm_workspace_bytes(.., limit) is
+// the size of the best plan whose scratch fits in `limit` bytes: SIZE_MAX
+// gives the preferred size, 0 the minimum (no split-K); launch_tc_gemm plans
+// within the workspace it is given.
 bool tc_gemm_supported(const GemmArgs& a);
+bool tc_gemm_pad_a(const GemmArgs& a);
+bool tc_gemm_pad_b(const GemmArgs& a);
 size_t tc_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool three_pass, bool b_kmajor,
-                               size_t limit);
+                               bool pad_a, bool pad_b, size_t limit);
 cudaError_t launch_tc_gemm(const GemmArgs& a, bool three_pass, void* workspace,
                            size_t workspace_bytes, cudaStream_t s);
 // The conv kernel needs a 16-byte aligned workspace for the padded hi / lo

@@ -10,7 +10,11 @@
 // mat1 [M,K] already is; mat2 [K,N] is N-contiguous, so a pre-pass
 // (k_prep_b) writes it once per call, transposed, into a caller- or
 // pool-provided workspace: Bt_hi[n][k] and Bt_lo[n][k] (3xTF32) or Bt[n][k]
-// (1xTF32).  The main kernel is then a plain pipeline:
+// (1xTF32), rows of Kp = K rounded up to 4 floats.  TMA needs 16-byte aligned
+// rows: when K % 4 != 0 (or mat1 is not 16-byte aligned) mat1 is copied
+// into the workspace with rows of Kp floats too (k_pad_rows).  The tensor maps
+// keep the extent K, so the TMA reads zeros for k >= K and the columns
+// between K and Kp are never read.  The main kernel is then a plain pipeline:
 //
 //   warp 0      TMA producer: mat1 tile (128 x 16), Bt_hi / Bt_lo tiles (BN x 16),
 //               64-byte swizzle, into a 4-stage ring (5 for the TS form, 8 for
@@ -85,11 +89,11 @@ constexpr int kTsMinKb = 96, kTsMinKbLightEpilogue = 32;
 __device__ int g_watchdog_gemm;
 
 // ----------------------------------------------------------- mat2 pre-pass
-// Bt_hi[n*K + k] = tf32 part of mat2[k*N + n] and Bt_lo[n*K + k] = the rest
-// (3xTF32), or Bt_hi = mat2 transposed (bt_lo == nullptr).  32x32 tiles through
-// shared memory: reads and writes are 128-byte rows.
+// Bt_hi[n*ldk + k] = tf32 part of mat2[k*N + n] and Bt_lo[n*ldk + k] = the
+// rest (3xTF32), or Bt_hi = mat2 transposed (bt_lo == nullptr); ldk >= K.
+// 32x32 tiles through shared memory: reads and writes are 128-byte rows.
 __global__ void __launch_bounds__(256) k_prep_b(const float* __restrict__ mat2, int64_t K,
-                                                int64_t N, float* __restrict__ bt_hi,
+                                                int64_t N, int64_t ldk, float* __restrict__ bt_hi,
                                                 float* __restrict__ bt_lo) {
   __shared__ float tile[32][33];
   ptx::griddep_launch();  // the main kernel may start its prologue
@@ -109,10 +113,10 @@ __global__ void __launch_bounds__(256) k_prep_b(const float* __restrict__ mat2, 
       if (n < N && k < K) {
         const float v = tile[tx][i];
         if (bt_lo) {
-          bt_hi[n * K + k] = tf32_hi(v);
-          bt_lo[n * K + k] = tf32_lo(v);
+          bt_hi[n * ldk + k] = tf32_hi(v);
+          bt_lo[n * ldk + k] = tf32_lo(v);
         } else {
-          bt_hi[n * K + k] = v;
+          bt_hi[n * ldk + k] = v;
         }
       }
     }
@@ -120,12 +124,12 @@ __global__ void __launch_bounds__(256) k_prep_b(const float* __restrict__ mat2, 
   }
 }
 
-// linear: the weight w[N,K] is already K-major and serves as B_hi as it is
-// (the tensor core truncates to TF32); 3xTF32 needs only w_lo = w - tf32(w).
-// The same for N % 4 == 0 and a 16-byte aligned mat2 (K % 4 == 0 on this
-// path): 64 x 64 tiles, 16-byte loads along N and 16-byte stores along K.
+// The same for N % 4 == 0 and a 16-byte aligned mat2 (ldk % 4 == 0): 64 x 64
+// tiles, 16-byte loads along N and 16-byte stores along K (a group of four k
+// is written whole when its first k < K; ldk >= K rounded up to 4).
 __global__ void __launch_bounds__(256) k_prep_b4(const float* __restrict__ mat2, int64_t K,
-                                                 int64_t N, float* __restrict__ bt_hi,
+                                                 int64_t N, int64_t ldk,
+                                                 float* __restrict__ bt_hi,
                                                  float* __restrict__ bt_lo) {
   __shared__ float tile[64][65];
   ptx::griddep_launch();  // the main kernel may start its prologue
@@ -153,10 +157,10 @@ __global__ void __launch_bounds__(256) k_prep_b4(const float* __restrict__ mat2,
         const float4 v = make_float4(tile[4 * q4][r], tile[4 * q4 + 1][r], tile[4 * q4 + 2][r],
                                      tile[4 * q4 + 3][r]);
         if (bt_lo) {
-          *reinterpret_cast<float4*>(bt_hi + n * K + k) = tf32_hi4(v);
-          *reinterpret_cast<float4*>(bt_lo + n * K + k) = tf32_lo4(v);
+          *reinterpret_cast<float4*>(bt_hi + n * ldk + k) = tf32_hi4(v);
+          *reinterpret_cast<float4*>(bt_lo + n * ldk + k) = tf32_lo4(v);
         } else {
-          *reinterpret_cast<float4*>(bt_hi + n * K + k) = v;
+          *reinterpret_cast<float4*>(bt_hi + n * ldk + k) = v;
         }
       }
     }
@@ -164,12 +168,35 @@ __global__ void __launch_bounds__(256) k_prep_b4(const float* __restrict__ mat2,
   }
 }
 
+// linear: the weight w[N,K] is already K-major and serves as B_hi as it is
+// (the tensor core truncates to TF32); 3xTF32 needs only w_lo = w - tf32(w).
 __global__ void __launch_bounds__(256) k_prep_blo(const float* __restrict__ w, int64_t total,
                                                   float* __restrict__ w_lo) {
   ptx::griddep_launch();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x)
     w_lo[i] = tf32_lo(__ldg(w + i));
+}
+
+// A [rows, K] operand whose rows are not 16-byte aligned (K % 4 != 0 or an
+// unaligned base) copied to rows of ld floats: dst[r*ld + k] = src[r*K + k]
+// for k < K (dst_lo, when given, gets the TF32 lo part and dst the value
+// itself); the columns K .. ld-1 are left as they are (the TMA never reads
+// them).  Thread = one element of a row, rows in turn: coalesced reads and
+// writes.
+__global__ void __launch_bounds__(256) k_pad_rows(const float* __restrict__ src, int64_t rows,
+                                                  int64_t K, int64_t ld, float* __restrict__ dst,
+                                                  float* __restrict__ dst_lo) {
+  ptx::griddep_launch();
+  const int64_t cols_blocks = (K + 255) / 256;
+  for (int64_t b = blockIdx.x; b < rows * cols_blocks; b += gridDim.x) {
+    const int64_t r = b / cols_blocks, k = (b - r * cols_blocks) * 256 + threadIdx.x;
+    if (k < K) {
+      const float v = __ldg(src + r * K + k);
+      dst[r * ld + k] = v;
+      if (dst_lo) dst_lo[r * ld + k] = tf32_lo(v);
+    }
+  }
 }
 
 // ------------------------------------------------------------ main kernel
@@ -593,14 +620,15 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major fp32 matrix [outer, inner] -> tensor map with a {16, box_outer}
-// box (64-byte rows), 64-byte swizzle, zero fill outside the matrix.
+// Row-major fp32 matrix [outer, inner] with rows ld >= inner floats apart
+// (ld % 4 == 0) -> tensor map with a {16, box_outer} box (64-byte rows),
+// 64-byte swizzle, zero fill outside the matrix.
 bool encode_k16(CUtensorMap* m, const float* base, uint64_t inner, uint64_t outer,
-                uint32_t box_outer) {
+                uint32_t box_outer, uint64_t ld) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 4};
+  const cuuint64_t strides[1] = {ld * 4};
   const cuuint32_t box[2] = {(cuuint32_t)BK, box_outer};
   const cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
@@ -658,6 +686,8 @@ constexpr int kPlanSMs = 152;
 
 struct Plan {
   int bn, num_m, num_n, splits, kps;
+  int64_t ld;           // row length (floats) of the B copies and of a padded A copy
+  int64_t a_offset;     // byte offset of the padded mat1 copy (when there is one)
   int64_t part_offset;  // byte offset of the split-K partials in the scratch
 };
 
@@ -666,14 +696,22 @@ struct Plan {
 // 32), plus, when split, the slice-sum pass ((splits + 1) * M*N*4 bytes at
 // HBM speed, ~1.5 ns per unit).  Ties go to wider tiles and fewer slices.
 // Only plans whose scratch fits in `limit` bytes are considered (a single
-// slice is always allowed: its scratch is the mat2 copy alone).
-Plan make_plan(int64_t M, int64_t N, int64_t K, bool three, bool b_kmajor, size_t limit) {
+// slice is always allowed: its scratch is the operand copies alone).
+// pad_a / pad_b: mat1 / a K-major B (linear weight) needs a copy with
+// 16-byte aligned rows.
+Plan make_plan(int64_t M, int64_t N, int64_t K, bool three, bool b_kmajor, bool pad_a,
+               bool pad_b, size_t limit) {
   const int64_t num_kb = (K + BK - 1) / BK;
-  Plan best{BN_MAX, (int)((M + BM - 1) / BM), 0, 1, (int)num_kb, 0};
-  // mat2 copy: transposed hi (+ lo); a K-major B needs only its lo part
-  const int64_t copies = b_kmajor ? (three ? 1 : 0) : (three ? 2 : 1);
-  const int64_t bt = copies * N * K * (int64_t)sizeof(float);
-  const int64_t part_offset = (bt + 255) / 256 * 256;
+  const int64_t ld = (K + 3) / 4 * 4;
+  Plan best{BN_MAX, (int)((M + BM - 1) / BM), 0, 1, (int)num_kb, ld, 0, 0};
+  // B copies: mat2 transposed, hi (+ lo); a K-major B needs only its lo part,
+  // or hi (+ lo) copies when its rows are not 16-byte aligned
+  const int64_t copies =
+      b_kmajor ? (pad_b ? (three ? 2 : 1) : (three ? 1 : 0)) : (three ? 2 : 1);
+  const int64_t bt = copies * N * ld * (int64_t)sizeof(float);
+  const int64_t a_offset = (bt + 255) / 256 * 256;
+  const int64_t a_bytes = pad_a ? M * ld * (int64_t)sizeof(float) : 0;
+  const int64_t part_offset = (a_offset + a_bytes + 255) / 256 * 256;
   double best_cost = 1e300;
   for (int bn = BN_MAX; bn >= 32; bn -= 32) {
     const int64_t tiles = best.num_m * ((N + bn - 1) / bn);
@@ -695,6 +733,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bool three, bool b_kmajor, size_
     }
   }
   best.num_n = (int)((N + best.bn - 1) / best.bn);
+  best.a_offset = a_offset;
   best.part_offset = part_offset;
   return best;
 }
@@ -707,9 +746,11 @@ constexpr int kMaxDev = 64;
 
 // after_prep: a pre-pass of this call ran just before (the main kernel may
 // then start early and waits for it before loading B).
+// a / lda: the A operand as the TMA reads it (mat1, or its padded copy);
+// ldb: the row length of the B operand (bt_hi / bt_lo).
 template <bool THREE, bool TS>
-cudaError_t run(const GemmArgs& g, const Plan& p, const float* bt_hi, const float* bt_lo,
-                float* part, bool after_prep, cudaStream_t s) {
+cudaError_t run(const GemmArgs& g, const Plan& p, const float* a, int64_t lda, const float* bt_hi,
+                const float* bt_lo, int64_t ldb, float* part, bool after_prep, cudaStream_t s) {
   constexpr int smem = smem_bytes(TS ? kLts : (THREE ? kL3 : kL1));
   static std::atomic<bool> ready[kMaxDev];  // per device: the attribute is set (calls may race)
   auto k = k_tc_gemm<THREE, TS>;
@@ -723,9 +764,10 @@ cudaError_t run(const GemmArgs& g, const Plan& p, const float* bt_hi, const floa
   }
   const int sms = device_sm_count();
   CUtensorMap ta, tbh, tbl;
-  if (!encode_k16(&ta, g.mat1, (uint64_t)g.K, (uint64_t)g.M, BM) ||
-      !encode_k16(&tbh, bt_hi, (uint64_t)g.K, (uint64_t)g.N, (uint32_t)p.bn) ||
-      !encode_k16(&tbl, THREE ? bt_lo : bt_hi, (uint64_t)g.K, (uint64_t)g.N, (uint32_t)p.bn))
+  if (!encode_k16(&ta, a, (uint64_t)g.K, (uint64_t)g.M, BM, (uint64_t)lda) ||
+      !encode_k16(&tbh, bt_hi, (uint64_t)g.K, (uint64_t)g.N, (uint32_t)p.bn, (uint64_t)ldb) ||
+      !encode_k16(&tbl, THREE ? bt_lo : bt_hi, (uint64_t)g.K, (uint64_t)g.N, (uint32_t)p.bn,
+                  (uint64_t)ldb))
     return cudaErrorInvalidValue;
   const int units = p.num_m * p.num_n * p.splits;
   const int grid = units < sms ? units : sms;
@@ -758,58 +800,88 @@ cudaError_t run(const GemmArgs& g, const Plan& p, const float* bt_hi, const floa
 }  // namespace
 
 bool tc_gemm_supported(const GemmArgs& a) {
-  const bool aligned = (reinterpret_cast<uintptr_t>(a.mat1) & 15u) == 0 &&
-                       (!a.b_kmajor || (reinterpret_cast<uintptr_t>(a.mat2) & 15u) == 0);
   const double tiles = (double)((a.M + BM - 1) / BM) * (double)((a.N + 31) / 32);
-  return a.K % 4 == 0 && aligned && tiles < 2147483647.0 && encode_fn() != nullptr;
+  return tiles < 2147483647.0 && encode_fn() != nullptr;
+}
+
+bool tc_gemm_pad_a(const GemmArgs& a) {
+  return a.K % 4 != 0 || (reinterpret_cast<uintptr_t>(a.mat1) & 15u) != 0;
+}
+
+bool tc_gemm_pad_b(const GemmArgs& a) {
+  return a.b_kmajor && (a.K % 4 != 0 || (reinterpret_cast<uintptr_t>(a.mat2) & 15u) != 0);
 }
 
 size_t tc_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool three_pass, bool b_kmajor,
-                               size_t limit) {
-  return plan_bytes(make_plan(M, N, K, three_pass, b_kmajor, limit), M, N);
+                               bool pad_a, bool pad_b, size_t limit) {
+  return plan_bytes(make_plan(M, N, K, three_pass, b_kmajor, pad_a, pad_b, limit), M, N);
 }
 
 cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
                            size_t workspace_bytes, cudaStream_t s) {
   if (!tc_gemm_supported(g)) return cudaErrorNotSupported;
-  const Plan p = make_plan(g.M, g.N, g.K, three_pass, g.b_kmajor != 0, workspace_bytes);
+  const bool pad_a = tc_gemm_pad_a(g), pad_b = tc_gemm_pad_b(g);
+  const Plan p =
+      make_plan(g.M, g.N, g.K, three_pass, g.b_kmajor != 0, pad_a, pad_b, workspace_bytes);
   if (plan_bytes(p, g.M, g.N) > workspace_bytes || (plan_bytes(p, g.M, g.N) > 0 && !workspace))
     return cudaErrorInvalidValue;
   float* ws = static_cast<float*>(workspace);
   float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.part_offset);
-  const float *b_hi, *b_lo;
+  const int64_t ld = p.ld;
+  const float *b_hi, *b_lo, *a = g.mat1;
+  int64_t lda = g.K, ldb = ld;
   const int64_t cap = (int64_t)device_sm_count() * 8;
-  bool prep = true;
-  if (g.b_kmajor) {  // w[N,K] is B_hi; 3xTF32 adds w_lo in the scratch
+  bool prep = false;
+  if (pad_a) {  // mat1 rows to 16-byte aligned rows of ld floats
+    float* a_copy = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.a_offset);
+    const int64_t blocks = g.M * ((g.K + 255) / 256);
+    k_pad_rows<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(g.mat1, g.M, g.K, ld,
+                                                                          a_copy, nullptr);
+    note_launch();
+    a = a_copy;
+    lda = ld;
+    prep = true;
+  }
+  if (g.b_kmajor && pad_b) {  // w[N,K] to aligned rows, hi (+ lo)
+    b_hi = ws;
+    b_lo = three_pass ? ws + g.N * ld : nullptr;
+    const int64_t blocks = g.N * ((g.K + 255) / 256);
+    k_pad_rows<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(
+        g.mat2, g.N, g.K, ld, ws, three_pass ? ws + g.N * ld : nullptr);
+    note_launch();
+    prep = true;
+  } else if (g.b_kmajor) {  // w[N,K] is B_hi; 3xTF32 adds w_lo in the scratch
     b_hi = g.mat2;
     b_lo = three_pass ? ws : nullptr;
-    prep = three_pass;
+    ldb = g.K;  // == ld: K % 4 == 0 here
     if (three_pass) {
       const int64_t total = g.N * g.K, blocks = (total + 255) / 256;
       k_prep_blo<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(g.mat2, total, ws);
       note_launch();
+      prep = true;
     }
-  } else {  // transpose mat2[K,N] into Bt_hi[N,K] (+ Bt_lo)
+  } else {  // transpose mat2[K,N] into Bt_hi[N,ld] (+ Bt_lo)
     b_hi = ws;
-    b_lo = three_pass ? ws + g.N * g.K : nullptr;
+    b_lo = three_pass ? ws + g.N * ld : nullptr;
     if (g.N % 4 == 0 && (reinterpret_cast<uintptr_t>(g.mat2) & 15u) == 0) {
       const int64_t tiles = ((g.N + 63) / 64) * ((g.K + 63) / 64);
       k_prep_b4<<<(unsigned)(tiles < cap ? tiles : cap), 256, 0, s>>>(
-          g.mat2, g.K, g.N, ws, three_pass ? ws + g.N * g.K : nullptr);
+          g.mat2, g.K, g.N, ld, ws, three_pass ? ws + g.N * ld : nullptr);
     } else {
       const int64_t tiles = ((g.N + 31) / 32) * ((g.K + 31) / 32);
       k_prep_b<<<(unsigned)(tiles < cap ? tiles : cap), dim3(32, 8), 0, s>>>(
-          g.mat2, g.K, g.N, ws, three_pass ? ws + g.N * g.K : nullptr);
+          g.mat2, g.K, g.N, ld, ws, three_pass ? ws + g.N * ld : nullptr);
     }
     note_launch();
+    prep = true;
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (!three_pass) return run<false, false>(g, p, b_hi, nullptr, part, prep, s);
+  if (!three_pass) return run<false, false>(g, p, a, lda, b_hi, nullptr, ldb, part, prep, s);
   const bool light = !(g.read_self && g.self_2d) || p.splits > 1;  // no [M,N] self read per tile
   const bool ts = p.kps >= kTsMinKb || (light && p.kps >= kTsMinKbLightEpilogue);
-  return ts ? run<true, true>(g, p, b_hi, b_lo, part, prep, s)
-            : run<true, false>(g, p, b_hi, b_lo, part, prep, s);
+  return ts ? run<true, true>(g, p, a, lda, b_hi, b_lo, ldb, part, prep, s)
+            : run<true, false>(g, p, a, lda, b_hi, b_lo, ldb, part, prep, s);
 }
 
 namespace {

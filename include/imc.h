@@ -109,9 +109,11 @@ extern "C" {
  *   beta, alpha  finite scalars (the pages default both to 1.0, which the
  *           Python binding supplies); used in fp32.
  *   stream  cudaStream_t or NULL.
- * Kernel choice: the tcgen05 path needs K % 4 == 0 and a 16-byte aligned
- * mat1 (its rows are TMA-loaded); other shapes, and tiny problems, take the
- * SIMT kernel.  imc_last_kernel() reports which ran.
+ * Kernel choice: the tcgen05 path takes any K and any alignment: it reads
+ * mat2 through a transposed copy in its scratch whose rows are padded to a
+ * multiple of 4 floats, and copies mat1 there too when its rows are not
+ * 16-byte aligned (K % 4 != 0 or an unaligned base).  Tiny problems take the
+ * SIMT kernel.  imc_last_kernel() / imc_last_kernel_name() report which ran.
  */
 int gemm_addmm_f32(const float* self, int self_2d, const float* mat1, const float* mat2,
                    float* out, int64_t M, int64_t N, int64_t K, double beta, double alpha,
@@ -125,11 +127,15 @@ int gemm_addmm_f32_ex(const float* self, int self_2d, const float* mat1, const f
                       int mode, void* stream);
 
 /* Bytes of device scratch the addmm prefers for these sizes and mode: the
- * copy of mat2 transposed and split (2*N*K*4 bytes when the 3xTF32
- * tensor-core kernel would run, N*K*4 for 1xTF32), plus split-K partial sums
- * (slices*M*N*4) for problems with too few output tiles to fill the GPU; 0
- * when the SIMT or epilogue-only kernel would run (assuming alpha != 0 and an
- * aligned mat1).  Returns 0 for invalid sizes or mode. */
+ * copy of mat2 transposed and split (2*N*Kp*4 bytes when the 3xTF32
+ * tensor-core kernel would run, N*Kp*4 for 1xTF32; Kp = K rounded up to a
+ * multiple of 4), a copy of mat1 (M*Kp*4) when K % 4 != 0, plus split-K
+ * partial sums (slices*M*N*4) for problems with too few output tiles to fill
+ * the GPU; 0 when the SIMT or epilogue-only kernel would run.  The size
+ * assumes 16-byte aligned pointers (alpha != 0); with an unaligned mat1 the
+ * call also needs the mat1 copy, and a workspace without room for it makes
+ * gemm_addmm_f32_ws run the SIMT kernel (or return IMC_ERR_ARG in a forced
+ * tensor-core mode).  Returns 0 for invalid sizes or mode. */
 size_t gemm_addmm_f32_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode);
 
 /* gemm_addmm_f32_ex with caller-provided scratch: `workspace` is a device
@@ -270,9 +276,10 @@ int conv2d_gemm_f32_ws(const float* x, const float* w, const float* bias, float*
  * mode: IMC_MODE_* (not IMC_MODE_DIRECT), optionally | IMC_ACT_RELU.  The
  * weight is already K-major, so the tensor-core path needs scratch only for
  * its TF32 lo part (N*K*4 bytes, 3xTF32) and any split-K partial sums;
- * linear_f32 takes it from the stream-ordered pool, linear_f32_ws from the
- * caller (rules as gemm_addmm_f32_ws).  Tensor-core path: K % 4 == 0 and
- * 16-byte aligned x and w; otherwise SIMT.
+ * when K % 4 != 0 (or w / x is not 16-byte aligned) the weight (hi and lo)
+ * and x are copied there with rows of K rounded up to 4 floats.  linear_f32
+ * takes the scratch from the stream-ordered pool, linear_f32_ws from the
+ * caller (rules as gemm_addmm_f32_ws).  Tiny problems take the SIMT kernel.
  */
 int linear_f32(const float* x, const float* w, const float* bias, float* out, int64_t M,
                int64_t N, int64_t K, int mode, void* stream);

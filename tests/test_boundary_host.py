@@ -145,7 +145,13 @@ def test_workspace_size_query(lib):
     assert q(1024, 3072, 768, 2) == 0                   # SIMT needs none
     assert q(64, 80, 96, 0) == 0                        # tiny: SIMT
     assert q(64, 80, 96, 3) == 2 * 80 * 96 * 4          # forced tensor-core kernel
-    assert q(1024, 3072, 770, 0) == 0                   # K % 4 != 0: SIMT
+    # K % 4 != 0: the tensor-core path with rows of 772 floats -- mat2^T hi and
+    # lo, then a copy of mat1 -- so that every row the TMA reads is aligned
+    assert q(1024, 3072, 770, 0) == 2 * 3072 * 772 * 4 + 1024 * 772 * 4
+    assert q(1024, 3072, 770, 1) == 3072 * 772 * 4 + 1024 * 772 * 4
+    # linear with K % 4 != 0: the weight copied too (hi and lo), then mat1
+    assert binding.linear_f32_workspace_bytes(1024, 3072, 770, 0) == \
+        2 * 3072 * 772 * 4 + 1024 * 772 * 4
     assert q(0, 8, 8, 0) == 0 and q(8, 8, -1, 0) == 0 and q(8, 8, 8, 9) == 0
 
 
@@ -282,7 +288,6 @@ def test_host_buffer_entry_points_check_before_any_cuda_call(lib):
     assert H(P1, 2, P2, P3, P4, 8, 8, 8, 1.0, 1.0, 0, None) == binding.IMC_ERR_ARG
     assert H(P1, 0, P2, P3, P4, 8, 8, 8, 1.0, 1.0, 9, None) == binding.IMC_ERR_ARG
     assert H(P1, 0, P2, P3, P2 + 16, 8, 8, 8, 1.0, 1.0, 0, None) == binding.IMC_ERR_ALIAS
-    assert H(P1, 0, P2, P3, P4, 8, 8, 10, 1.0, 1.0, 3, None) == binding.IMC_ERR_SHAPE  # K % 4
     assert H(P1, 0, P2, P3, P4, 0, 8, 8, 1.0, 1.0, 0, None) == binding.IMC_OK  # empty: no work
     C = binding.conv2d_gemm_f32_host
     conv = [P1, P2, P3, P4, 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 1, 0, None]
@@ -291,6 +296,10 @@ def test_host_buffer_entry_points_check_before_any_cuda_call(lib):
     bad = list(conv)
     bad[11] = 0  # stride 0
     assert C(*bad) == binding.IMC_ERR_SHAPE
+    # a forced tensor-core mode takes K % 4 != 0 (operand rows are padded in
+    # the scratch); the call then needs a GPU
+    assert without_gpu([["gemm_addmm_f32_host", [P1, 0, P2, P3, P4, 8, 8, 10, 1.0, 1.0, 3,
+                                                 None]]]) == [binding.IMC_ERR_DEVICE]
     got = without_gpu([["gemm_addmm_f32_host", [P1, 0, P2, P3, P4, 8, 8, 8, 1.0, 1.0, 0, None]],
                        ["conv2d_gemm_f32_host", conv]])
     assert got == [binding.IMC_ERR_DEVICE] * 2

@@ -61,14 +61,20 @@ def test_linear_matches_oracle(mode, mnk):
         within(out.cpu().numpy(), ref, S, TOL[mode], f"linear {mnk} {mode} bias={bias is not None}")
 
 
-def test_linear_k_not_multiple_of_4_takes_simt():
-    M, N, K = 70, 40, 33
-    x = synth.uniform(synth.stream_key(0, 650, 1), M * K, -1, 1).reshape(M, K)
-    w = synth.uniform(synth.stream_key(0, 650, 2), N * K, -1, 1).reshape(N, K)
-    out = binding.linear(dev(x), dev(w), None)
-    assert binding.last_kernel() == "simt"
-    ref, S = oracle.addmm(None, x, np.ascontiguousarray(w.T), beta=0.0)
-    within(out.cpu().numpy(), ref, S, 1e-5, "linear K=33")
+@pytest.mark.parametrize("mode", ["default", "force_tc3", "force_tc1"])
+def test_linear_k_not_multiple_of_4_on_tensor_cores(mode):
+    # weight rows of K % 4 != 0 floats: the weight (hi and lo) and x are
+    # copied to rows of K rounded up to 4 in the scratch
+    for M, N, K in [(70, 40, 33), (1024, 768, 770), (300, 257, 3)]:
+        x = synth.uniform(synth.stream_key(0, 650 + K, 1), M * K, -1, 1).reshape(M, K)
+        w = synth.uniform(synth.stream_key(0, 650 + K, 2), N * K, -1, 1).reshape(N, K)
+        b = synth.normal(synth.stream_key(0, 650 + K, 3), N, 0.0, 0.02)
+        out = binding.linear(dev(x), dev(w), dev(b), mode=mode)
+        torch.cuda.synchronize()
+        tiny = M * N * K < (1 << 22)
+        assert binding.last_kernel() == EXPECT.get(mode, "simt" if tiny else "tc3")
+        ref, S = oracle.addmm(b, x, np.ascontiguousarray(w.T))
+        within(out.cpu().numpy(), ref, S, TOL[mode], f"linear {M}x{N}x{K} {mode}")
 
 
 def test_linear_integer_inputs_are_bit_exact():

@@ -138,14 +138,85 @@ def test_addmm_ragged_partial_last_wave(mode):
     assert np.array_equal(got.astype(np.float64), ref), mode
 
 
-def test_addmm_k_not_multiple_of_4_takes_simt():
-    for M, N, K in [(70, 40, 33), (5, 7, 3), (300, 260, 130)]:
-        s, a, b = synth.addmm_inputs(M, N, K, self_2d=False, workload=5)
-        got, ref, S, kern = run_addmm(s, a, b, 1.0, 1.0, "default")
-        assert kern == "simt"
-        within(got, ref, S, 1e-5, f"{M}x{N}x{K}")
-        with pytest.raises(binding.ImcError):
-            binding.addmm(dev(s), dev(a), dev(b), mode="force_tc3")
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1"])
+def test_addmm_k_not_multiple_of_4_on_tensor_cores(mode):
+    # rows of K % 4 != 0 floats are not 16-byte aligned: mat1 is copied to
+    # rows of K rounded up to 4 and mat2^T written with that row length; the
+    # TMA reads zeros past K
+    for M, N, K, self_2d in [(70, 40, 33, False), (5, 7, 3, True), (300, 260, 130, False),
+                             (129, 65, 1, True), (256, 96, 2, False), (200, 300, 259, True)]:
+        s, a, b = synth.addmm_inputs(M, N, K, self_2d=self_2d, workload=5 + K)
+        # alpha = 1 for 1xTF32: with K of 1 to 3 nothing averages the product's
+        # truncation error (up to 2^-9 of |a*b|), and the bound 2e-3*S does not
+        # scale with alpha
+        alpha = 1.5 if mode == "force_tc3" else 1.0
+        got, ref, S, kern = run_addmm(s, a, b, 0.5, alpha, mode)
+        assert kern == EXPECT[mode]
+        within(got, ref, S, TOL[mode], f"{mode} {M}x{N}x{K}")
+    spec = ("I", -4, 4)
+    s, a, b = synth.addmm_inputs(300, 260, 130, self_2d=True, workload=7, mat1=spec, mat2=spec,
+                                 self_=spec)
+    got, ref, _, _ = run_addmm(s, a, b, 1.0, 1.0, mode)
+    assert np.array_equal(got.astype(np.float64), ref)
+
+
+def test_addmm_ragged_k_workloads():
+    # the default mode takes the tensor cores for K % 4 != 0: a ragged
+    # transformer-sized shape in full, and 8192x4096x4095 on 256 seeded rows
+    M, N, K = 577, 770, 767
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=False, workload=81, mat1=("N", 0.0, 1.0),
+                                 mat2=("U", -1 / np.sqrt(K), 1 / np.sqrt(K)),
+                                 self_=("N", 0.0, 0.02))
+    for mode in ("default", "tf32"):
+        got, ref, S, kern = run_addmm(s, a, b, 1.0, 1.0, mode)
+        assert kern == ("tc3" if mode == "default" else "tc1")
+        within(got, ref, S, TOL[mode], f"577x770x767 {mode}")
+    M, N, K = 8192, 4096, 4095
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=False, workload=82, mat1=("N", 0.0, 1 / 64),
+                                 mat2=("N", 0.0, 1 / 64), self_=("N", 0.0, 1.0))
+    rows = synth.sample_rows(synth.stream_key(0, 82, 99), M, 256)
+    ref, S = oracle.addmm(s, a, b, rows=rows, self_2d=False)
+    for mode in ("default", "tf32"):
+        out = binding.addmm(dev(s), dev(a), dev(b), mode=mode)
+        torch.cuda.synchronize()
+        assert binding.last_kernel() == ("tc3" if mode == "default" else "tc1")
+        within(out.cpu().numpy()[rows], ref, S, TOL[mode], f"8192x4096x4095 {mode}")
+        del out
+
+
+def test_addmm_unaligned_mat1():
+    # mat1 starting 4 bytes past a 16-byte boundary: the library pool path
+    # copies it to aligned rows (tensor cores); a caller workspace with room
+    # for the mat2 copies alone (what an aligned mat1 needs at least) runs the
+    # SIMT kernel
+    M, N, K = 300, 260, 132
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=False, workload=83)
+    base = torch.zeros(M * K + 1, device="cuda")
+    base[1:] = torch.from_numpy(a.ravel()).cuda()
+    A = base[1:].view(M, K)
+    assert A.data_ptr() % 16 == 4
+    S, B = dev(s), dev(b)
+    stream = torch.cuda.current_stream().cuda_stream
+    out = torch.empty((M, N), device="cuda")
+    rc = binding.gemm_addmm_f32_ex(S.data_ptr(), 0, A.data_ptr(), B.data_ptr(), out.data_ptr(),
+                                   M, N, K, 1.0, 1.0, 0, stream)
+    assert rc == binding.IMC_OK and binding.last_kernel() == "tc3"
+    torch.cuda.synchronize()
+    ref, Sr = oracle.addmm(s, a, b)
+    within(out.cpu().numpy(), ref, Sr, 1e-5, "unaligned mat1, pool")
+    least = 2 * N * K * 4
+    ws = torch.empty(least, dtype=torch.uint8, device="cuda")
+    got = torch.empty((M, N), device="cuda")
+    rc = binding.gemm_addmm_f32_ws(S.data_ptr(), 0, A.data_ptr(), B.data_ptr(), got.data_ptr(),
+                                   M, N, K, 1.0, 1.0, 0, ws.data_ptr(), least, stream)
+    assert rc == binding.IMC_OK and binding.last_kernel() == "simt"
+    torch.cuda.synchronize()
+    within(got.cpu().numpy(), ref, Sr, 1e-5, "unaligned mat1, small workspace")
+    # with the size the query gives (room for split-K partial sums) it fits
+    got = binding.addmm(S, A, B)
+    torch.cuda.synchronize()
+    assert binding.last_kernel() in ("tc3", "simt")
+    within(got.cpu().numpy(), ref, Sr, 1e-5, "unaligned mat1, query-sized workspace")
 
 
 @pytest.mark.parametrize("mode", ["force_tc3", "force_tc1"])
