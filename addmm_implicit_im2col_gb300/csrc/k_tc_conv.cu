@@ -26,9 +26,10 @@
 //               and, for 3xTF32, lo part -- so that its tiles can be
 //               TMA-loaded whatever K is
 //   warps 0-7   im2col gather: warp w fills TMEM lanes 32*(w%4) .. +31 (32
-//               positions) with k = 8*(w/4) .. +7 of every k-block of 16; the
-//               values of the next two k-blocks are in flight while one is
-//               split into TF32 hi / lo and written to its stage (tcgen05.st)
+//               positions) with all 16 k of every other k-block (those whose
+//               index has parity w/4); the values of its next two k-blocks are
+//               in flight while one is split into TF32 hi / lo and written to
+//               its stage (tcgen05.st)
 //   warp 8      TMA producer of the weight tiles (BN x 16 fp32, 64B swizzle)
 //   warp 9      TMEM owner + MMA issuer, A from TMEM and B from shared memory:
 //               A_lo*B_hi + A_hi*B_lo + A_hi*B_hi per k-step of 8, or A*B
@@ -161,23 +162,19 @@ __global__ void __launch_bounds__(256) k_prep_w(const float* __restrict__ w, int
   }
 }
 
-// Three register buffers of gathered values, rotated by unrolling (copying a
-// buffer whose loads are in flight would wait for them): the values of k-blocks
-// i+1 and i+2 are in flight while k-block i is stored.
+// Two register buffers of gathered values, alternated by unrolling (copying a
+// buffer whose loads are in flight would wait for them): the 16 values of a
+// warp's next k-block are in flight while one k-block is stored.
 template <class Gather, class Store>
-__device__ __forceinline__ bool rotate3(int nkb, Gather& gather, Store& store) {
-  float va[8], vb[8], vc[8];
+__device__ __forceinline__ bool rotate2(int nkb, Gather& gather, Store& store) {
+  float va[BK], vb[BK];
   gather(va);
-  if (nkb > 1) gather(vb);
-  for (int i = 0; i < nkb; i += 3) {
-    if (i + 2 < nkb) gather(vc);
+  for (int i = 0; i < nkb; i += 2) {
+    if (i + 1 < nkb) gather(vb);
     if (!store(va)) return false;
     if (i + 1 >= nkb) break;
-    if (i + 3 < nkb) gather(va);
+    if (i + 2 < nkb) gather(va);
     if (!store(vb)) return false;
-    if (i + 2 >= nkb) break;
-    if (i + 4 < nkb) gather(vb);
-    if (!store(vc)) return false;
   }
   return true;
 }
@@ -203,8 +200,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int kh = r / c.KW, kw = r - kh * c.KW;
     tab[r] = make_int2(kh * c.dH, kw * c.dW);
   }
-  // full: the 8 gather warps + the weight TMA
-  if (threadIdx.x == 0) init_barriers(ctl, q.stages, GATHER_WARPS + 1, 1);
+  // full: the 4 gather warps of the stage's k-block parity + the weight TMA
+  if (threadIdx.x == 0) init_barriers(ctl, q.stages, GATHER_WARPS / 2 + 1, 1);
   ptx::griddep_launch();  // the slice-sum kernel may launch (it waits for this one)
   if (warp == TMA_WARP && lane == 0) {
     ptx::tma_prefetch_desc(&tmWh);
@@ -222,40 +219,56 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp < GATHER_WARPS) {
     // ------------------------------------------------------ im2col gather
-    const int quarter = warp & 3, half = warp >> 2;
+    // Warp w fills TMEM lanes 32*(w%4) .. +31 with all 16 k of the k-blocks
+    // whose index in this CTA's sequence has parity w/4: each warp hands over
+    // one k-block in two, so the store-and-signal latency of one k-block
+    // overlaps the gather of the next in the other warp.
+    const int quarter = warp & 3, par = warp >> 2;
     const int HW = c.H * c.W, ICHW = c.IC * HW, P = c.OH * c.OW;
-    const uint32_t trow =
-        tmem + ((uint32_t)(quarter * 32) << 16) + A_COL0 + (uint32_t)(half * 8);
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + A_COL0;
     int s = 0;
     uint32_t ph = 0;
+    int64_t g0 = 0;  // index of the unit's first k-block in this CTA's sequence
     bool ok = true;
-    // Splits the 8 values of a k-block into TF32 hi / lo and writes them to
-    // the stage's TMEM columns; then arrives on the stage's full barrier.
-    auto put = [&](const float (&v)[8]) {
+    // Splits the 16 values of a k-block into TF32 hi / lo and writes them to
+    // the stage's TMEM columns; then arrives on the stage's full barrier and
+    // moves to this warp's next stage (two k-blocks on).
+    auto put = [&](const float (&v)[BK]) {
       const uint32_t ta = trow + (uint32_t)s * A_STAGE_COLS;
       if (THREE) {
-        float hi[8], lo[8];
+        float hi[BK], lo[BK];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < BK; ++j) {
           hi[j] = tf32_hi(v[j]);
           lo[j] = tf32_lo(v[j]);
         }
-        ptx::tmem_st8(ta, hi);
-        ptx::tmem_st8(ta + 16, lo);
+        ptx::tmem_st16(ta, hi);
+        ptx::tmem_st16(ta + 16, lo);
       } else {
-        ptx::tmem_st8(ta, v);  // the tensor core reads it as TF32
+        ptx::tmem_st16(ta, v);  // the tensor core reads it as TF32
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&ctl->full[s]);
-      if (++s == q.stages) {
-        s = 0;
+      s += 2;
+      if (s >= q.stages) {
+        s -= q.stages;
         ph ^= 1u;
       }
     };
     for (int u = blockIdx.x; u < q.units && ok; u += gridDim.x) {
       const Unit un = decode(q, u);
+      const int nkb_unit = un.kb1 - un.kb0;
+      const int i0 = (int)((par ^ g0) & 1);  // this warp's first k-block of the unit
+      const int nkb = nkb_unit > i0 ? (nkb_unit - i0 + 1) / 2 : 0;
+      {
+        const int64_t g = g0 + i0;
+        s = (int)(g % q.stages);
+        ph = (uint32_t)((g / q.stages) & 1);
+      }
+      g0 += nkb_unit;
+      if (nkb == 0) continue;
       const TilePos tp = tile_pos(c, q, un.pt);
       const int64_t p = tp.p0 + quarter * 32 + lane;
       const bool pok = quarter * 32 + lane < tp.count;
@@ -268,9 +281,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         iw0 = ow * c.sW - c.pW;
       }
       const float* xb = c.x + (int64_t)b * ICHW;
-      const int k0 = un.kb0 * BK + half * 8;
-      const int nkb = un.kb1 - un.kb0;
-      auto store = [&](const float (&v)[8]) -> bool {
+      const int k0 = (un.kb0 + i0) * BK;
+      auto store = [&](const float (&v)[BK]) -> bool {
         if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) return false;
         ptx::tc_fence_after();
         put(v);
@@ -292,11 +304,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         };
         set_tap();
-        // The 8 values of one k-block (0 past K, outside the image, or past
-        // the last position), then skip the other half's 8.
-        auto gather = [&](float (&v)[8]) {
+        // The 16 values of one k-block (0 past K, outside the image, or past
+        // the last position), then skip the other warp's k-block.
+        auto gather = [&](float (&v)[BK]) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < BK; ++j) {
             v[j] = tap_in ? __ldg(xb + (ic_hw + tap_off)) : 0.0f;
             ic_hw += HW;
             if (++ic == c.IC) {
@@ -306,43 +318,43 @@ __global__ void __launch_bounds__(THREADS, 1)
               set_tap();
             }
           }
-          ic += 8;
-          ic_hw += 8 * HW;
+          ic += BK;
           if (ic >= c.IC) {
             while (ic >= c.IC) {
               ic -= c.IC;
               ++tap;
             }
-            ic_hw = ic * HW;
             set_tap();
           }
+          ic_hw = ic * HW;
         };
         if (c.IC % BK == 0) {
-          // a k-block lies in one tap: one bounds check per k-block, then 8
+          // a k-block lies in one tap: one bounds check per k-block, then 16
           // loads at the channel-plane stride (ic, tap: this warp's next k)
-          auto gather16 = [&](float (&v)[8]) {
+          auto gather16 = [&](float (&v)[BK]) {
             const float* src = xb + (ic_hw + tap_off);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = tap_in ? __ldg(src + j * HW) : 0.0f;
-            ic += BK;
-            ic_hw += BK * HW;
-            if (ic >= c.IC) {  // next tap: ic comes back to 0 or 8 (this warp's half)
-              ic -= c.IC;
-              ic_hw = ic * HW;
-              ++tap;
+            for (int j = 0; j < BK; ++j) v[j] = tap_in ? __ldg(src + j * HW) : 0.0f;
+            ic += 2 * BK;
+            if (ic >= c.IC) {  // a later tap: ic stays a multiple of 16
+              while (ic >= c.IC) {
+                ic -= c.IC;
+                ++tap;
+              }
               set_tap();
             }
+            ic_hw = ic * HW;
           };
-          ok = rotate3(nkb, gather16, store);
+          ok = rotate2(nkb, gather16, store);
         } else {
-          ok = rotate3(nkb, gather, store);
+          ok = rotate2(nkb, gather, store);
         }
       } else {
         // running (ic, r) of this warp's next k = ic*taps + r
         int ic_hw = (k0 / taps) * HW, r = k0 - (k0 / taps) * taps;
-        auto gather = [&](float (&v)[8]) {
+        auto gather = [&](float (&v)[BK]) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < BK; ++j) {
             const int2 d = tab[r];
             const int ih = ih0 + d.x, iw = iw0 + d.y;
             const bool in = pok && ic_hw < ICHW && (unsigned)ih < (unsigned)c.H &&
@@ -353,13 +365,13 @@ __global__ void __launch_bounds__(THREADS, 1)
               ic_hw += HW;
             }
           }
-          r += 8;
+          r += BK;
           while (r >= taps) {
             r -= taps;
             ic_hw += HW;
           }
         };
-        ok = rotate3(nkb, gather, store);
+        ok = rotate2(nkb, gather, store);
       }
     }
   } else if (warp == TMA_WARP) {
@@ -777,8 +789,9 @@ bool tc_conv_shape_ok(const ConvArgs& c) {
   if ((int64_t)(c.KH - 1) * c.dH >= lim30 || (int64_t)(c.KW - 1) * c.dW >= lim30) return false;
   if ((int64_t)c.H + 2 * (int64_t)c.pH >= lim30 || (int64_t)c.W + 2 * (int64_t)c.pW >= lim30)
     return false;
-  // the running input-channel offset may pass IC by up to 17 planes
-  if (((int64_t)c.IC + 17) * c.H * c.W > lim31) return false;
+  // the running input-channel offset may pass IC by up to 33 planes (one
+  // k-block and the skipped one after the last)
+  if (((int64_t)c.IC + 33) * c.H * c.W > lim31) return false;
   // position tiles are at most one per 128 positions plus one per image
   const int64_t tiles = ((c.N + BM - 1) / BM + c.B) * ((c.M + BN_MAX - 1) / BN_MAX);
   return tiles < lim31;
