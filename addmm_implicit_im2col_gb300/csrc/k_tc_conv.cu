@@ -63,7 +63,16 @@ constexpr int BK = 16;           // fp32 per k-block: one 64-byte swizzle row
 constexpr int KSTEPS = BK / UK;  // 2
 constexpr int BN_MAX = 256;
 constexpr int GATHER_WARPS = 8;
-constexpr int TMA_WARP = 8, MMA_WARP = 9, EPI_WARP0 = 10, THREADS = 14 * 32;
+constexpr int TMA_WARP = 8, MMA_WARP = 9, EPI_WARP0 = 10, SLAB_WARP = 14;
+// gather forms (kernel template argument)
+constexpr int GM_PAGES = 0;  // K order (ic, kh, kw), reads from global memory
+constexpr int GM_ICF = 1;    // K order (kh, kw, ic), reads from global memory
+constexpr int GM_SLAB = 2;   // K order (ic, kh, kw), reads an input slab in shared memory
+// threads of a CTA: 14 warps, 15 with the slab producer
+constexpr int threads_of(int gm) { return (gm == GM_SLAB ? 15 : 14) * 32; }
+constexpr int SLAB_ROWS = 4, SLAB_COLS = 32;  // 2-D position tile of the slab form
+constexpr int kSlabMaxBytes = 48 * 1024;      // one slab buffer (two are resident)
+constexpr int kSlabMaxK = 2048;               // k offset table of the slab form (8 KB)
 constexpr uint32_t A_COL0 = 256, A_STAGE_COLS = 32;
 constexpr int MAX_TAPS = 1024;  // KH*KW entries of the per-CTA tap table
 constexpr int EPI_CHUNK_FLOATS = 32 * BM;  // one 32-channel chunk of a tile
@@ -84,6 +93,11 @@ struct Sched {
   int tab_bytes;            // tap table
   int tma_out;              // whole tiles inside one image leave by TMA store
   int tpi;                  // position tiles per image (0: tiles run across images)
+  // slab form: a position tile is SLAB_ROWS output rows x SLAB_COLS output
+  // columns (tw tiles across a row); its input window [IC][srows][sbw] (first
+  // column soff floats before the first tap) comes in by one TMA box
+  int slab, tw, sbw, srows, soff;
+  int slab_tx, slab_stride;  // bytes of one box, bytes between the two buffers
   float* part;              // tail partial sums [units - full][bn][128]
 };
 
@@ -130,6 +144,19 @@ __device__ __forceinline__ TilePos tile_pos(const ConvArgs& c, const Sched& q, i
     t.p0 = (int64_t)pt * BM;
     t.count = c.N - t.p0 < BM ? (int)(c.N - t.p0) : BM;
   }
+  return t;
+}
+
+// Slab form: image and top-left output position of position tile pt.
+struct Tile2 {
+  int b, oh0, ow0;
+};
+__device__ __forceinline__ Tile2 tile2d(const Sched& q, int pt) {
+  Tile2 t;
+  t.b = pt / q.tpi;
+  const int r = pt - t.b * q.tpi, rt = r / q.tw;
+  t.oh0 = rt * SLAB_ROWS;
+  t.ow0 = (r - rt * q.tw) * SLAB_COLS;
   return t;
 }
 
@@ -180,28 +207,66 @@ __device__ __forceinline__ bool rotate2(int nkb, Gather& gather, Store& store) {
 }
 
 // ------------------------------------------------------------ main kernel
-template <bool THREE, bool ICF>
-__global__ void __launch_bounds__(THREADS, 1)
+template <bool THREE, int GM>
+__global__ void __launch_bounds__(threads_of(GM), 1)
     k_tc_conv(const __grid_constant__ CUtensorMap tmWh, const __grid_constant__ CUtensorMap tmWl,
-              const __grid_constant__ CUtensorMap tmO, const ConvArgs c, const Sched q) {
+              const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmX,
+              const ConvArgs c, const Sched q) {
+  constexpr bool ICF = GM == GM_ICF, SLAB = GM == GM_SLAB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
   const int b_tile = q.bn * BK * 4;  // one weight tile (hi or lo)
-  // [weight stages][tap table][epilogue staging][barriers]
-  int2* tab = reinterpret_cast<int2*>(smem + q.stages * q.w_bytes);
+  // [weight stages][2 input slabs (slab form)][tap table][epilogue staging]
+  // [barriers][slab barriers: full 0, 1, empty 0, 1]
+  float* slab = reinterpret_cast<float*>(smem + q.stages * q.w_bytes);
+  int2* tab = reinterpret_cast<int2*>(reinterpret_cast<uint8_t*>(slab) +
+                                      (SLAB ? 2 * q.slab_stride : 0));
   float* epi_stage = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tab) + q.tab_bytes);
   Ctl* ctl = reinterpret_cast<Ctl*>(reinterpret_cast<uint8_t*>(epi_stage) + EPI_STAGE_BYTES);
+  uint64_t* sbar = reinterpret_cast<uint64_t*>(ctl + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int taps = c.KH * c.KW;
   int* wd = &g_watchdog_conv;
 
-  // tap table: r = kh*KW + kw -> (kh*dH, kw*dW)
-  for (int r = threadIdx.x; r < taps; r += blockDim.x) {
-    const int kh = r / c.KW, kw = r - kh * c.KW;
-    tab[r] = make_int2(kh * c.dH, kw * c.dW);
+  if constexpr (SLAB) {
+    // k offset table: k = ic*taps + kh*KW + kw -> ic*srows*sbw + kh*dH*sbw +
+    // kw*dW, the value's place in a slab relative to its position's first
+    // tap (0 for k >= K, masked by the gather)
+    int* koff = reinterpret_cast<int*>(tab);
+    for (int k = threadIdx.x; k < q.kb * BK; k += blockDim.x) {
+      int o = 0;
+      if (k < c.K) {
+        const int ic = k / taps, r = k - ic * taps, kh = r / c.KW, kw = r - kh * c.KW;
+        o = (ic * q.srows + kh * c.dH) * q.sbw + kw * c.dW;
+      }
+      koff[k] = o;
+    }
+  } else {
+    // tap table: r = kh*KW + kw -> (kh*dH, kw*dW)
+    for (int r = threadIdx.x; r < taps; r += blockDim.x) {
+      const int kh = r / c.KW, kw = r - kh * c.KW;
+      tab[r] = make_int2(kh * c.dH, kw * c.dW);
+    }
   }
   // full: the 4 gather warps of the stage's k-block parity + the weight TMA
   if (threadIdx.x == 0) init_barriers(ctl, q.stages, GATHER_WARPS / 2 + 1, 1);
+  // Slab form: the producer sets up its own barriers and sends the first
+  // box before the CTA's set-up barrier (the input does not come from the
+  // pre-pass), so that its memory latency overlaps the set-up.
+  auto slab_load = [&](int u, int sb) {
+    const Tile2 t = tile2d(q, decode(q, u).pt);
+    ptx::mbar_arrive_expect_tx(&sbar[sb], (uint32_t)q.slab_tx);
+    ptx::tma_load_4d(slab + sb * (q.slab_stride / 4), &tmX, &sbar[sb],
+                     t.ow0 * c.sW - c.pW - q.soff, t.oh0 * c.sH - c.pH, 0, t.b);
+  };
+  if (SLAB && warp == SLAB_WARP && lane == 0) {
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&sbar[i], 1);                 // the producer's expect-tx
+      ptx::mbar_init(&sbar[2 + i], GATHER_WARPS);  // every gather warp is done with it
+    }
+    ptx::fence_mbar_init();
+    if ((int)blockIdx.x < q.units) slab_load((int)blockIdx.x, 0);
+  }
   ptx::griddep_launch();  // the slice-sum kernel may launch (it waits for this one)
   if (warp == TMA_WARP && lane == 0) {
     ptx::tma_prefetch_desc(&tmWh);
@@ -233,7 +298,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // Splits the 16 values of a k-block into TF32 hi / lo and writes them to
     // the stage's TMEM columns; then arrives on the stage's full barrier and
     // moves to this warp's next stage (two k-blocks on).
-    auto put = [&](const float (&v)[BK]) {
+    auto put_issue = [&](const float (&v)[BK]) {
       const uint32_t ta = trow + (uint32_t)s * A_STAGE_COLS;
       if (THREE) {
         float hi[BK], lo[BK];
@@ -247,6 +312,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       } else {
         ptx::tmem_st16(ta, v);  // the tensor core reads it as TF32
       }
+    };
+    auto put_commit = [&]() {
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
@@ -257,7 +324,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         ph ^= 1u;
       }
     };
-    for (int u = blockIdx.x; u < q.units && ok; u += gridDim.x) {
+    auto put = [&](const float (&v)[BK]) {
+      put_issue(v);
+      put_commit();
+    };
+    auto store = [&](const float (&v)[BK]) -> bool {
+      if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) return false;
+      ptx::tc_fence_after();
+      put(v);
+      return true;
+    };
+    int ul = 0;  // units of this CTA so far
+    for (int u = blockIdx.x; u < q.units && ok; u += gridDim.x, ++ul) {
       const Unit un = decode(q, u);
       const int nkb_unit = un.kb1 - un.kb0;
       const int i0 = (int)((par ^ g0) & 1);  // this warp's first k-block of the unit
@@ -268,6 +346,69 @@ __global__ void __launch_bounds__(THREADS, 1)
         ph = (uint32_t)((g / q.stages) & 1);
       }
       g0 += nkb_unit;
+      const int k0 = (un.kb0 + i0) * BK;
+      if constexpr (SLAB) {
+        // Every gather warp waits for the unit's slab (so that its arrival
+        // below counts toward this use of the buffer), reads it, and hands
+        // the buffer back.  Lane = output column ow0 + lane, quarter = output
+        // row oh0 + quarter; the slab holds input rows oh0*sH - pH .. and
+        // columns ow0*sW - pW - soff .., zeros outside the image.
+        const int sb = ul & 1;
+        if (!warp_wait_bar(&sbar[sb], (uint32_t)(ul >> 1) & 1u, abort, kSiteSlabFull, wd)) {
+          ok = false;
+          break;
+        }
+        if (nkb > 0) {
+          const float* sl = slab + sb * (q.slab_stride / 4) + quarter * c.sH * q.sbw +
+                            lane * c.sW + q.soff;
+          const int* koff = reinterpret_cast<const int*>(tab);
+          int kk = k0;  // first k of this warp's next k-block
+          // 16 offsets by four broadcast loads, then 16 independent loads
+          // (an offset past K is 0, inside the slab; the value is masked)
+          auto gather = [&](float (&v)[BK]) {
+            int o[BK];
+#pragma unroll
+            for (int j = 0; j < BK; j += 4) {
+              const int4 t = *reinterpret_cast<const int4*>(koff + kk + j);
+              o[j] = t.x;
+              o[j + 1] = t.y;
+              o[j + 2] = t.z;
+              o[j + 3] = t.w;
+            }
+#pragma unroll
+            for (int j = 0; j < BK; ++j) {
+              const float xv = sl[o[j]];
+              v[j] = kk + j < c.K ? xv : 0.0f;
+            }
+            kk += 2 * BK;
+          };
+          // the TMEM stores of one k-block complete while the next is gathered
+          float va[BK], vb[BK];
+          gather(va);
+          for (int i = 0; i < nkb; i += 2) {
+            if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            put_issue(va);
+            if (i + 1 < nkb) gather(vb);
+            put_commit();
+            if (i + 1 >= nkb) break;
+            if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            put_issue(vb);
+            if (i + 2 < nkb) gather(va);
+            put_commit();
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sbar[2 + sb]);
+        continue;
+      }
       if (nkb == 0) continue;
       const TilePos tp = tile_pos(c, q, un.pt);
       const int64_t p = tp.p0 + quarter * 32 + lane;
@@ -281,13 +422,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         iw0 = ow * c.sW - c.pW;
       }
       const float* xb = c.x + (int64_t)b * ICHW;
-      const int k0 = (un.kb0 + i0) * BK;
-      auto store = [&](const float (&v)[BK]) -> bool {
-        if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) return false;
-        ptx::tc_fence_after();
-        put(v);
-        return true;
-      };
       if constexpr (ICF) {
         // running position of this warp's next k = tap*IC + ic: the tap's
         // validity and in-plane offset, and the channel plane offset ic*H*W
@@ -447,6 +581,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       drain_wait(&ctl->drain, 0);
     }
     __syncwarp();
+  } else if (warp == SLAB_WARP) {
+    // ------------------------------------- input slab producer (slab form)
+    // One TMA box [IC][srows][sbw] per unit, into buffer (unit & 1) once the
+    // gather warps have handed it back; the box may start before the image
+    // (column a multiple of 4, zeros there) and run past its end.
+    if (SLAB && lane == 0) {
+      int ul = (int)blockIdx.x < q.units ? 1 : 0;  // the first box went out before set-up
+      for (int u = blockIdx.x + ul * gridDim.x; u < q.units && !*abort; u += gridDim.x, ++ul) {
+        const int sb = ul & 1;
+        if (!wait_bar(&sbar[2 + sb], ((uint32_t)(ul >> 1) & 1u) ^ 1u, abort, kSiteSlabEmpty, wd))
+          break;
+        slab_load(u, sb);
+      }
+      for (int j = (ul > 2 ? ul - 2 : 0); j < ul; ++j)  // the boxes still in flight land
+        drain_wait(&sbar[j & 1], (uint32_t)(j >> 1) & 1u);
+    }
   } else {
     // ----------------------------------------------------------- epilogue
     // Per 32-channel chunk: TMEM -> registers -> a [32 channels][128
@@ -470,7 +620,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const TilePos tp = tile_pos(c, q, un.pt);
       const int64_t p0 = tp.p0, plast = tp.p0 + tp.count - 1;
       const int b0 = (int)(p0 / P);
-      const bool by_tma = q.tma_out && un.slot < 0 && plast / P == b0;
+      // slab form: every whole tile leaves by TMA (4-D box, clipped at the
+      // image's right and bottom edges); only K-slice partial sums do not
+      const bool by_tma = SLAB ? un.slot < 0 : q.tma_out && un.slot < 0 && plast / P == b0;
       // this lane's four positions in the store phase
       const int64_t pq = p0 + 4 * lane;
       const int left = tp.count - 4 * lane;
@@ -512,7 +664,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           ptx::fence_proxy_async_smem();
           epi_sync();
           if (issuer) {
-            ptx::tma_store_3d(&tmO, blk, (int)(p0 - (int64_t)b0 * P), oc0 + cc, b0);
+            if constexpr (SLAB) {
+              const Tile2 t = tile2d(q, un.pt);
+              ptx::tma_store_4d(&tmO, blk, t.ow0, t.oh0, oc0 + cc, t.b);
+            } else {
+              ptx::tma_store_3d(&tmO, blk, (int)(p0 - (int64_t)b0 * P), oc0 + cc, b0);
+            }
             ptx::bulk_commit();
           }
           continue;
@@ -576,9 +733,19 @@ __global__ void __launch_bounds__(256) k_conv_tail(const ConvArgs c, const Sched
   const int col = (int)(rest % q.bn), tt = (int)(rest / q.bn);
   if (tt >= tail) return;
   const int t = q.full + tt, pt = t / q.n_oc, ot = t - pt * q.n_oc;
-  const TilePos tp = tile_pos(c, q, pt);
   const int r0 = 4 * quad, oc = ot * q.bn + col;
-  if (r0 >= tp.count || oc >= c.OC) return;
+  if (oc >= c.OC) return;
+  int64_t obase = -1;  // slab form: out offset of (b, oc, oh, ow), -1 if off the image
+  TilePos tp{0, BM};
+  if (q.slab) {  // row r0 of the tile is output (oh0 + r0/32, ow0 + r0%32 ..+3), OW % 4 == 0
+    const Tile2 t2 = tile2d(q, pt);
+    const int oh = t2.oh0 + (r0 >> 5), ow = t2.ow0 + (r0 & 31);
+    if (oh >= c.OH || ow >= c.OW) return;
+    obase = (((int64_t)t2.b * c.OC + oc) * c.OH + oh) * c.OW + ow;
+  } else {
+    tp = tile_pos(c, q, pt);
+    if (r0 >= tp.count) return;
+  }
   const int64_t per = (int64_t)q.bn * BM;
   const float4* src =
       reinterpret_cast<const float4*>(q.part + ((int64_t)tt * q.slices * q.bn + col) * BM + r0);
@@ -595,6 +762,10 @@ __global__ void __launch_bounds__(256) k_conv_tail(const ConvArgs c, const Sched
   if (c.relu) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) o[k] = fmaxf(o[k], 0.0f);
+  }
+  if (obase >= 0) {
+    *reinterpret_cast<float4*>(c.out + obase) = make_float4(o[0], o[1], o[2], o[3]);
+    return;
   }
   const int64_t P = (int64_t)c.OH * c.OW, p = tp.p0 + r0, b = p / P;
   if (c.vec_out && r0 + 3 < tp.count) {  // P % 4 == 0: p .. p+3 are in one image
@@ -657,8 +828,54 @@ struct Plan {
   int smem;         // dynamic shared memory of the main kernel
 };
 
+// Input channel fastest in the kernel's K order (see the file comment).
+bool ic_fastest(const ConvArgs& c) { return c.IC >= 8; }
+
+// Shared memory of the main kernel besides the weight stages.
+int fixed_smem(const Sched& q) {
+  return 1024 + (q.slab ? 2 * q.slab_stride : 0) + q.tab_bytes + EPI_STAGE_BYTES +
+         (int)sizeof(Ctl) + 4 * (int)sizeof(uint64_t);
+}
+
+// Slab form, for few input channels (the pages' K order): position tiles of
+// SLAB_ROWS x SLAB_COLS outputs, each tile's input window brought into shared
+// memory by one 4-D TMA box and the im2col values read from there.  Applies
+// when the box fits the TMA limits (each extent <= 256, x and its rows
+// 16-byte aligned: W % 4 == 0), both buffers fit beside four weight stages,
+// the output takes 4-D TMA stores (OW % 4 == 0, aligned out), K is at most
+// kSlabMaxK (the k offset table), and at least 3/4 of the tiles' positions are
+// real outputs.
+bool slab_geometry(const ConvArgs& c, Sched& q, int w_bytes) {
+  if (ic_fastest(c) || c.W % 4 != 0 || c.OW % 4 != 0 || !c.vec_out ||
+      reinterpret_cast<uintptr_t>(c.x) % 16 != 0 || (int64_t)q.kb * BK > kSlabMaxK)
+    return false;
+  const int64_t off = (4 - c.pW % 4) % 4;  // box column start a multiple of 4
+  const int64_t bw =
+      (off + (SLAB_COLS - 1) * (int64_t)c.sW + (int64_t)(c.KW - 1) * c.dW + 1 + 3) / 4 * 4;
+  const int64_t rows = (SLAB_ROWS - 1) * (int64_t)c.sH + (int64_t)(c.KH - 1) * c.dH + 1;
+  if (bw > 256 || rows > 256 || c.IC > 256) return false;
+  const int64_t bytes = (int64_t)c.IC * rows * bw * 4;
+  if (bytes > kSlabMaxBytes) return false;
+  const int64_t tw = (c.OW + SLAB_COLS - 1) / SLAB_COLS, th = (c.OH + SLAB_ROWS - 1) / SLAB_ROWS;
+  if (4 * (int64_t)c.OW * c.OH < 3 * tw * SLAB_COLS * th * SLAB_ROWS) return false;
+  if ((int64_t)c.B * tw * th * q.n_oc >= (int64_t(1) << 30)) return false;  // tile indices fit an int
+  Sched t = q;
+  t.slab = 1;
+  t.tw = (int)tw;
+  t.tpi = (int)(tw * th);
+  t.sbw = (int)bw;
+  t.srows = (int)rows;
+  t.soff = (int)off;
+  t.slab_tx = (int)bytes;
+  t.slab_stride = (int)((bytes + 1023) / 1024 * 1024);
+  t.tab_bytes = (t.kb * BK * 4 + 1023) / 1024 * 1024;  // k offset table
+  if (fixed_smem(t) + 4 * w_bytes > SMEM_LIMIT) return false;
+  q = t;
+  return true;
+}
+
 // Channel tiles of at most 256 (as even as possible, multiples of 16);
-// 128-position tiles; K-slices for the tail tiles when they shorten the
+// 128-position tiles (SLAB_ROWS x SLAB_COLS in the slab form); K-slices for the tail tiles when they shorten the
 // longest CTA's work and the partial sums fit in `limit` bytes of workspace.
 // Cost in k-block times of one CTA: whole-tile waves, the sliced wave(s), the
 // fix-up launch, and the partial sums' write + read at HBM speed (one k-block
@@ -671,10 +888,15 @@ Plan make_plan(const ConvArgs& c, bool three, size_t limit) {
   q.n_oc = (int)((OC + BN_MAX - 1) / BN_MAX);
   q.bn = (int)(((OC + q.n_oc - 1) / q.n_oc + 15) / 16 * 16);
   q.kb = (int)((K + BK - 1) / BK);
-  // per-image tiles when that adds at most 1/16 empty positions
-  const int64_t tpi = (P + BM - 1) / BM;
-  q.tpi = (P >= BM && (tpi * BM - P) * 16 <= P) ? (int)tpi : 0;
-  const int64_t ptiles = q.tpi > 0 ? (int64_t)c.B * q.tpi : (Npix + BM - 1) / BM;
+  int64_t ptiles;
+  if (slab_geometry(c, q, (three ? 2 : 1) * q.bn * BK * 4)) {
+    ptiles = (int64_t)c.B * q.tpi;
+  } else {
+    // per-image tiles when that adds at most 1/16 empty positions
+    const int64_t tpi = (P + BM - 1) / BM;
+    q.tpi = (P >= BM && (tpi * BM - P) * 16 <= P) ? (int)tpi : 0;
+    ptiles = q.tpi > 0 ? (int64_t)c.B * q.tpi : (Npix + BM - 1) / BM;
+  }
   const int64_t tiles = ptiles * q.n_oc;
   const size_t w_bytes = (three ? 2u : 1u) * (size_t)OC * (size_t)padded_k(K) * sizeof(float);
   pl.part_off = (w_bytes + 255) / 256 * 256;
@@ -710,10 +932,13 @@ Plan make_plan(const ConvArgs& c, bool three, size_t limit) {
 bool layout(Plan& pl, const ConvArgs& c, bool three) {
   Sched& q = pl.q;
   q.w_bytes = (three ? 2 : 1) * q.bn * BK * 4;
-  q.tab_bytes = (c.KH * c.KW * 8 + 1023) / 1024 * 1024;  // keeps the epilogue blocks 1 KB-aligned
-  const int avail = SMEM_LIMIT - 1024 - q.tab_bytes - EPI_STAGE_BYTES - (int)sizeof(Ctl);
+  // tap table, or the k offset table of the slab form; a multiple of 1 KB
+  // keeps the epilogue blocks 1 KB-aligned
+  q.tab_bytes = q.slab ? (q.kb * BK * 4 + 1023) / 1024 * 1024
+                       : (c.KH * c.KW * 8 + 1023) / 1024 * 1024;
+  const int avail = SMEM_LIMIT - fixed_smem(q);
   q.stages = avail / q.w_bytes < MAX_STAGES ? avail / q.w_bytes : MAX_STAGES;
-  pl.smem = 1024 + q.stages * q.w_bytes + q.tab_bytes + EPI_STAGE_BYTES + (int)sizeof(Ctl);
+  pl.smem = fixed_smem(q) + q.stages * q.w_bytes;
   return q.stages >= 3;
 }
 
@@ -733,16 +958,46 @@ bool encode_out(CUtensorMap* m, const ConvArgs& c) {
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Input channel fastest in the kernel's K order (see the file comment).
-bool ic_fastest(const ConvArgs& c) { return c.IC >= 8; }
+// Slab form: out viewed as [B][OC][OH][OW] -> tensor map, box {SLAB_COLS,
+// SLAB_ROWS, 32 channels, 1 image}; the parts past OW, OH or OC are not
+// written.  Needs OW % 4 == 0 and a 16-byte aligned out.
+bool encode_out_2d(CUtensorMap* m, const ConvArgs& c) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t OW = (cuuint64_t)c.OW, OH = (cuuint64_t)c.OH, OC = (cuuint64_t)c.OC;
+  const cuuint64_t dims[4] = {OW, OH, OC, (cuuint64_t)c.B};
+  const cuuint64_t strides[3] = {OW * 4, OH * OW * 4, OC * OH * OW * 4};
+  const cuuint32_t box[4] = {(cuuint32_t)SLAB_COLS, (cuuint32_t)SLAB_ROWS, 32, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, c.out, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Slab form: x viewed as [B][IC][H][W] -> tensor map, box {sbw, srows, IC,
+// 1 image}, unswizzled ([IC][srows][sbw] in shared memory); outside the
+// image reads as zero.  Needs W % 4 == 0 and a 16-byte aligned x.
+bool encode_x_slab(CUtensorMap* m, const ConvArgs& c, const Sched& q) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t W = (cuuint64_t)c.W, H = (cuuint64_t)c.H, IC = (cuuint64_t)c.IC;
+  const cuuint64_t dims[4] = {W, H, IC, (cuuint64_t)c.B};
+  const cuuint64_t strides[3] = {W * 4, H * W * 4, IC * H * W * 4};
+  const cuuint32_t box[4] = {(cuuint32_t)q.sbw, (cuuint32_t)q.srows, (cuuint32_t)c.IC, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(c.x), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 constexpr int kMaxDev = 64;
 
-template <bool THREE, bool ICF>
+template <bool THREE, int GM>
 cudaError_t launch_main(const ConvArgs& c, const Plan& pl, const CUtensorMap& th,
-                        const CUtensorMap& tl, const CUtensorMap& to, int grid, cudaStream_t s) {
+                        const CUtensorMap& tl, const CUtensorMap& to, const CUtensorMap& tx,
+                        int grid, cudaStream_t s) {
   static std::atomic<bool> ready[kMaxDev];  // per device: the attribute is set (calls may race)
-  auto k = k_tc_conv<THREE, ICF>;
+  auto k = k_tc_conv<THREE, GM>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -751,8 +1006,8 @@ cudaError_t launch_main(const ConvArgs& c, const Plan& pl, const CUtensorMap& th
     if (e != cudaSuccess) return e;
     if (dev < kMaxDev) ready[dev].store(true, std::memory_order_release);
   }
-  return launch_after_previous(k, dim3(grid), dim3(THREADS), (size_t)pl.smem, s, th, tl, to, c,
-                               pl.q);
+  return launch_after_previous(k, dim3(grid), dim3(threads_of(GM)), (size_t)pl.smem, s, th, tl, to, tx,
+                               c, pl.q);
 }
 
 template <bool THREE>
@@ -763,16 +1018,27 @@ cudaError_t run(const ConvArgs& c, Plan pl, const float* w_hi, const float* w_lo
       !encode_w(&tl, THREE ? w_lo : w_hi, (uint64_t)Kp, (uint64_t)c.OC, pl.q.bn))
     return cudaErrorInvalidValue;
   if (!layout(pl, c, THREE)) return cudaErrorInvalidValue;
-  CUtensorMap to;
-  pl.q.tma_out = c.vec_out && encode_out(&to, c) ? 1 : 0;  // vec_out: P % 4 == 0, aligned out
-  if (!pl.q.tma_out) to = th;                                // not read
+  CUtensorMap to, tx = th;  // tx: read in the slab form only
+  if (pl.q.slab) {
+    if (!encode_out_2d(&to, c) || !encode_x_slab(&tx, c, pl.q)) return cudaErrorInvalidValue;
+    pl.q.tma_out = 1;
+  } else {
+    pl.q.tma_out = c.vec_out && encode_out(&to, c) ? 1 : 0;  // vec_out: P % 4 == 0, aligned out
+    if (!pl.q.tma_out) to = th;                                // not read
+  }
   pl.q.part = part;
   const int sms = device_sm_count();
   const int grid = pl.q.units < sms ? pl.q.units : sms;
-  cudaError_t e = ic_fastest(c) ? launch_main<THREE, true>(c, pl, th, tl, to, grid, s)
-                                : launch_main<THREE, false>(c, pl, th, tl, to, grid, s);
+  cudaError_t e;
+  if (pl.q.slab)
+    e = launch_main<THREE, GM_SLAB>(c, pl, th, tl, to, tx, grid, s);
+  else if (ic_fastest(c))
+    e = launch_main<THREE, GM_ICF>(c, pl, th, tl, to, tx, grid, s);
+  else
+    e = launch_main<THREE, GM_PAGES>(c, pl, th, tl, to, tx, grid, s);
   note_launch();
-  note_kernel_name(THREE ? "k_tc_conv<3xtf32>" : "k_tc_conv<1xtf32>");
+  note_kernel_name(pl.q.slab ? (THREE ? "k_tc_conv<3xtf32,slab>" : "k_tc_conv<1xtf32,slab>")
+                             : (THREE ? "k_tc_conv<3xtf32>" : "k_tc_conv<1xtf32>"));
   if (e != cudaSuccess || pl.tail == 0) return e;
   const int64_t threads = (int64_t)pl.tail * pl.q.bn * 32;
   e = launch_after_previous(k_conv_tail, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0,

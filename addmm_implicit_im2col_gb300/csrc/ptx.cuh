@@ -104,6 +104,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_
       : "memory");
 }
 
+// 4-D tiled bulk tensor load global -> shared, completion counted in bytes on
+// bar; c0 is the innermost coordinate (a negative or out-of-range coordinate
+// reads zeros, c0 * element size a multiple of 16 bytes).
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, uint64_t* bar, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(tmap), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // 3-D tiled bulk tensor store shared -> global (x innermost), tracked by the
 // issuing thread's bulk async-groups.  Elements outside the tensor are not
 // written.
@@ -113,6 +125,16 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, 
       "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
           tmap),
       "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+// 4-D tiled bulk tensor store shared -> global (c0 innermost), likewise;
+// the parts of the box past the tensor's end are not written.
+__device__ __forceinline__ void tma_store_4d(const void* tmap, const void* src, int32_t c0,
+                                             int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::
+          "l"(tmap),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
 // 2-D tiled bulk tensor store shared -> global (x innermost), likewise.

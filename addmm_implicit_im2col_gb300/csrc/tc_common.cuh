@@ -27,6 +27,8 @@ enum WaitSite {
   kSiteMmaOperands = 4,
   kSiteEpilogueAccFull = 5,
   kSiteSelfTest = 6,  // imc_selftest_wait_timeout: a wait nothing completes
+  kSiteSlabFull = 7,   // conv gather waiting for its input slab
+  kSiteSlabEmpty = 8,  // conv slab producer waiting for a free slab buffer
 };
 
 struct Ctl {

@@ -489,6 +489,94 @@ def test_conv_workloads(name):
         within(got, ref, S, TOL[mode], f"{name} {mode}")
 
 
+# Few input channels (IC < 8) with W % 4 == 0 and OW % 4 == 0: the slab form
+# (position tiles of 4 output rows x 32 output columns; each tile's input
+# window comes into shared memory by one TMA box, the im2col values are read
+# from there; whole tiles leave by 4-D TMA stores clipped at the image edges).
+SLAB_CONV = [  # B, IC, H, W, OC, KH, KW, stride, pad, dil, channels checked (None: all)
+    # ragged right and bottom edges (OW 120 = 3.75 column tiles, OH 102), pad 1
+    (2, 3, 102, 120, 64, 3, 3, 1, 1, 1, None),
+    # pad 0 (box starts on the window), 5x5
+    (1, 4, 40, 68, 32, 5, 5, 1, 0, 1, None),
+    # stride 2, dilation 2, pad 2, OH 33
+    (2, 2, 66, 128, 48, 3, 3, 2, 2, 2, None),
+    # per-axis stride / pad / dilation, OH 29
+    (2, 5, 31, 64, 40, 3, 5, (1, 2), (1, 2), (2, 1), None),
+    # 160 tiles: one wave, then 8 tiles in K-slices (K = 343)
+    (1, 7, 80, 256, 32, 7, 7, 1, 3, 1, None),
+    # K = 9: one k-block per tile, so one warp group gathers nothing
+    (2, 1, 64, 64, 16, 3, 3, 1, 1, 1, None),
+    # OC 300: two channel tiles of 160, stride 2
+    (1, 3, 64, 128, 300, 5, 5, 2, 2, 1, np.arange(0, 300, 7)),
+    # the stem shape at 96x96: OW = OH = 24, three quarters of each tile used
+    (1, 3, 96, 96, 128, 7, 7, 4, 3, 1, None),
+]
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1", "default"])
+@pytest.mark.parametrize("idx", range(len(SLAB_CONV)))
+def test_conv_slab_form(mode, idx):
+    t = SLAB_CONV[idx]
+    x, w, b, s, p, d = _conv_case(t[:10], 520 + idx)
+    got, ref, S, kern = run_conv(x, w, b, s, p, d, mode, channels=t[10])
+    if mode in EXPECT:
+        assert kern == EXPECT[mode]
+    if kern != "simt":  # the default mode may take SIMT for the smallest shapes
+        assert ",slab>" in binding.last_kernel_name(), binding.last_kernel_name()
+    within(got, ref, S, TOL[mode], f"{mode} slab conv #{idx}")
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1"])
+@pytest.mark.parametrize("idx", [0, 3, 4, 6])
+def test_conv_slab_integer_bit_exact(mode, idx):
+    t = SLAB_CONV[idx]
+    x, w, b, s, p, d = _conv_case(t[:10], 540 + idx, spec=("I", -3, 3))
+    got, ref, _, _ = run_conv(x, w, b, s, p, d, mode, channels=t[10])
+    assert ",slab>" in binding.last_kernel_name()
+    assert np.array_equal(got.astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1"])
+def test_conv_slab_relu_no_bias(mode):
+    t = SLAB_CONV[0]
+    x, w, _, s, p, d = _conv_case(t[:10], 560)
+    out = binding.conv2d(dev(x), dev(w), None, s, p, d, mode=mode, relu=True)
+    torch.cuda.synchronize()
+    assert ",slab>" in binding.last_kernel_name()
+    ref, S = oracle.conv2d(x, w, None, s, p, d)
+    within(out.cpu().numpy(), np.maximum(ref, 0.0), S, TOL[mode], f"slab relu {mode}")
+
+
+def test_conv_slab_reads_only_the_taps():
+    # 2x2 taps at stride 4: input columns 4j+2 and 4j+3 belong to no output's
+    # window.  The slab holds them; a NaN there must not reach any output.
+    B, IC, H, W, OC = 1, 3, 32, 128, 24
+    x, w, b = synth.conv_inputs(B, IC, H, W, OC, 2, 2, workload=561)
+    x = x.copy()
+    x[:, :, :, 2::4] = np.nan
+    x[:, :, :, 3::4] = np.inf
+    got, ref, S, _ = run_conv(x, w, b, 4, 0, 1, "force_tc3")
+    assert ",slab>" in binding.last_kernel_name()
+    assert np.isfinite(ref).all()
+    within(got, ref, S, 1e-5, "slab conv, NaN outside the taps")
+
+
+def test_conv_slab_shape_with_unaligned_input_takes_the_global_gather():
+    # same shape as a slab case, x one float off a 16-byte boundary: no TMA
+    # box can start there, so the gather reads global memory instead
+    t = SLAB_CONV[0]
+    x, w, b, s, p, d = _conv_case(t[:10], 562)
+    buf = torch.empty(x.size + 1, dtype=torch.float32, device="cuda")
+    xv = buf[1:].view(x.shape)
+    xv.copy_(torch.from_numpy(x))
+    assert xv.data_ptr() % 16 != 0
+    out = binding.conv2d(xv, dev(w), dev(b), s, p, d, mode="force_tc3")
+    torch.cuda.synchronize()
+    assert binding.last_kernel_name() == "k_tc_conv<3xtf32>"
+    ref, S = oracle.conv2d(x, w, b, s, p, d)
+    within(out.cpu().numpy(), ref, S, 1e-5, "unaligned x")
+
+
 def test_launch_counter_and_watchdog():
     n0 = binding.launch_count()
     s, a, b = synth.addmm_inputs(256, 256, 64, self_2d=False, workload=3)
