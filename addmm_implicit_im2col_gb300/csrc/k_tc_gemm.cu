@@ -204,13 +204,14 @@ struct Store {
   const GemmArgs& g;
   int64_t m0, n0;
   const float* srow;  // beta * self[n0 + c] in shared memory (vector self), else nullptr
+  int64_t nlim;       // min(N, n0 + tile width): the columns from there on are not this tile's
   // beta * self for the segment (row r, columns c .. c+3 of the tile), read
   // before any output of the block is written (out may be self: each element
   // is read before its own write).
   __device__ __forceinline__ float4 load(int r, int c) const {
     const int64_t m = m0 + r, n = n0 + c;
     float4 sv = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (!g.read_self || m >= g.M || n >= g.N) return sv;
+    if (!g.read_self || m >= g.M || n >= nlim) return sv;
     if (srow) return *reinterpret_cast<const float4*>(srow + c);
     const float* sp = g.self + (g.self_2d ? m * g.N : 0) + n;
     if (g.vec_out) {
@@ -225,7 +226,7 @@ struct Store {
   }
   __device__ __forceinline__ void operator()(int r, int c, float4 v, float4 bs) const {
     const int64_t m = m0 + r, n = n0 + c;
-    if (m >= g.M || n >= g.N) return;
+    if (m >= g.M || n >= nlim) return;
     float* o = g.out + m * g.N + n;
     float4 o4 = make_float4(fmaf(g.alpha, v.x, bs.x), fmaf(g.alpha, v.y, bs.y),
                             fmaf(g.alpha, v.z, bs.z), fmaf(g.alpha, v.w, bs.w));
@@ -245,15 +246,30 @@ struct Store {
 // memory in the 128-byte swizzled layout (row r, 16-byte unit u at
 // r*128 + ((u ^ (r % 8)) * 16)), and lane 0 stores the 32 x 32 block with one
 // 2-D tensor store.  `srow` holds beta * self of the tile's columns (nullptr:
-// no self).  The accumulator is released after its last TMEM load.
+// no self).  The accumulator is released after its last TMEM load.  A tile
+// width of 16 mod 32 ends on a half chunk: a 32-column box would overwrite the
+// next tile's columns, so each lane stores its row's 16 values itself.
 __device__ __forceinline__ void drain_tma(uint32_t tmem, int q, int bn, uint8_t* blk,
                                           const CUtensorMap* tm_out, const GemmArgs& g,
                                           int64_t m0, int64_t n0, const float* srow,
                                           uint64_t* release) {
   const int lane = threadIdx.x & 31;
   const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+  // alpha*acc + beta*self (+ ReLU) of 4 columns from c + 4u
+  auto value = [&](const uint32_t (&v)[32], int c, int u) {
+    const float4 s4 = srow ? *reinterpret_cast<const float4*>(srow + c + 4 * u)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 o = make_float4(fmaf(g.alpha, __uint_as_float(v[4 * u]), s4.x),
+                           fmaf(g.alpha, __uint_as_float(v[4 * u + 1]), s4.y),
+                           fmaf(g.alpha, __uint_as_float(v[4 * u + 2]), s4.z),
+                           fmaf(g.alpha, __uint_as_float(v[4 * u + 3]), s4.w));
+    if (g.relu)
+      o = make_float4(fmaxf(o.x, 0.f), fmaxf(o.y, 0.f), fmaxf(o.z, 0.f), fmaxf(o.w, 0.f));
+    return o;
+  };
+  int c = 0;
 #pragma unroll 1
-  for (int c = 0; c < bn; c += 32) {
+  for (; c + 32 <= bn; c += 32) {
     uint32_t v[32];
     ptx::tmem_ld32(tbase + (uint32_t)c, v);
     ptx::tmem_ld_wait();
@@ -264,22 +280,30 @@ __device__ __forceinline__ void drain_tma(uint32_t tmem, int q, int bn, uint8_t*
     if (lane == 0) ptx::bulk_wait_read0();  // the previous chunk's store has read the block
     __syncwarp();
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float4 s4 = srow ? *reinterpret_cast<const float4*>(srow + c + 4 * u)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-      float4 o = make_float4(fmaf(g.alpha, __uint_as_float(v[4 * u]), s4.x),
-                             fmaf(g.alpha, __uint_as_float(v[4 * u + 1]), s4.y),
-                             fmaf(g.alpha, __uint_as_float(v[4 * u + 2]), s4.z),
-                             fmaf(g.alpha, __uint_as_float(v[4 * u + 3]), s4.w));
-      if (g.relu)
-        o = make_float4(fmaxf(o.x, 0.f), fmaxf(o.y, 0.f), fmaxf(o.z, 0.f), fmaxf(o.w, 0.f));
-      *reinterpret_cast<float4*>(blk + lane * 128 + ((u ^ (lane & 7)) << 4)) = o;
-    }
+    for (int u = 0; u < 8; ++u)
+      *reinterpret_cast<float4*>(blk + lane * 128 + ((u ^ (lane & 7)) << 4)) = value(v, c, u);
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
       ptx::tma_store_2d(tm_out, blk, (int)(n0 + c), (int)(m0 + q * 32));
       ptx::bulk_commit();
+    }
+  }
+  if (c < bn) {  // half chunk: each lane stores its row's 16 values itself
+    uint32_t v[32];
+    ptx::tmem_ld32(tbase + (uint32_t)c, v);
+    ptx::tmem_ld_wait();
+    if (release) {
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(release);
+    }
+    const int64_t m = m0 + q * 32 + lane;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t n = n0 + c + 4 * u;
+      const float4 o = value(v, c, u);
+      if (m < g.M && n < g.N)  // N % 4 == 0: the whole float4 is inside
+        *reinterpret_cast<float4*>(g.out + m * g.N + n) = o;
     }
   }
 }
@@ -288,10 +312,11 @@ __device__ __forceinline__ void drain_tma(uint32_t tmem, int q, int bn, uint8_t*
 struct PartStore {
   float* p;
   int64_t M, N, m0, n0;
+  int64_t nlim;  // min(N, n0 + tile width)
   __device__ __forceinline__ float4 load(int, int) const { return make_float4(0.f, 0.f, 0.f, 0.f); }
   __device__ __forceinline__ void operator()(int r, int c, float4 v, float4) const {
     const int64_t m = m0 + r, n = n0 + c;
-    if (m >= M || n >= N) return;
+    if (m >= M || n >= nlim) return;
     float* o = p + m * N + n;
     if (N % 4 == 0) {
       *reinterpret_cast<float4*>(o) = v;
@@ -503,12 +528,14 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
                   &tmOut, g, (int64_t)mt * BM, (int64_t)nt * bn, vec_self ? srow : nullptr, early);
       else if (splits == 1)
         drain_accumulator(tmem, q, (uint32_t)buf * ACC_STRIDE, bn, stage,
-                          Store{g, (int64_t)mt * BM, (int64_t)nt * bn, vec_self ? srow : nullptr},
+                          Store{g, (int64_t)mt * BM, (int64_t)nt * bn, vec_self ? srow : nullptr,
+                                min(g.N, (int64_t)(nt + 1) * bn)},
                           early);
       else
         drain_accumulator(tmem, q, (uint32_t)buf * ACC_STRIDE, bn, stage,
                           PartStore{part + (int64_t)(u / num_tiles) * g.M * g.N, g.M, g.N,
-                                    (int64_t)mt * BM, (int64_t)nt * bn},
+                                    (int64_t)mt * BM, (int64_t)nt * bn,
+                                    min(g.N, (int64_t)(nt + 1) * bn)},
                           early);
       if (!TS) {
         ptx::tc_fence_before();
@@ -691,7 +718,8 @@ struct Plan {
   int64_t part_offset;  // byte offset of the split-K partials in the scratch
 };
 
-// Picks the tile width BN (multiple of 32) and the number of K-slices by an
+// Picks the tile width BN (a multiple of 32, or of 16 from 112 up for an
+// unsplit K) and the number of K-slices by an
 // estimate of the last SM's time in MMA column-k-blocks: waves * kps * (BN +
 // 32), plus, when split, the slice-sum pass ((splits + 1) * M*N*4 bytes at
 // HBM speed, ~1.5 ns per unit).  Ties go to wider tiles and fewer slices.
@@ -713,9 +741,10 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bool three, bool b_kmajor, bool 
   const int64_t a_bytes = pad_a ? M * ld * (int64_t)sizeof(float) : 0;
   const int64_t part_offset = (a_offset + a_bytes + 255) / 256 * 256;
   double best_cost = 1e300;
-  for (int bn = BN_MAX; bn >= 32; bn -= 32) {
+  for (int bn = BN_MAX; bn >= 32; bn -= 16) {
+    if (bn % 32 != 0 && bn < 112) continue;  // narrow tiles: steps of 32
     const int64_t tiles = best.num_m * ((N + bn - 1) / bn);
-    for (int sp = 1; sp <= 16; ++sp) {
+    for (int sp = 1; sp <= (bn % 32 != 0 ? 1 : 16); ++sp) {  // half steps: unsplit tiles only
       const int64_t kps = (num_kb + sp - 1) / sp;
       const int64_t eff = (num_kb + kps - 1) / kps;  // non-empty slices
       if (sp > 1 && (kps < 4 || eff != sp)) continue;

@@ -167,7 +167,7 @@ __device__ __forceinline__ uint8_t* smem_align1024(uint8_t* smem_raw) {
   return smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
 }
 
-// Reads `ncols` (a multiple of 32) accumulator columns of the 32 rows this
+// Reads `ncols` (a multiple of 16) accumulator columns of the 32 rows this
 // warp owns (TMEM lanes 32q .. 32q+31, starting at column `col`), transposes
 // each 32x32 block through the warp's staging area and hands 16-byte row
 // segments to the store functor: first store.load(row, col) for all eight
@@ -176,6 +176,9 @@ __device__ __forceinline__ uint8_t* smem_align1024(uint8_t* smem_raw) {
 // With `release` given, the thread arrives on it (after a tcgen05 fence) as
 // soon as its last columns are in registers, so the MMA can reuse the
 // accumulator while the stores finish; otherwise the caller arrives after.
+// When ncols ends halfway through a 32-column block, the block's last load
+// reads 16 columns past the tile (inside the TMEM allocation) and the store
+// functor, which bounds its columns by the tile's end, drops them.
 template <class StoreFn>
 __device__ __forceinline__ void drain_accumulator(uint32_t tmem, int q, uint32_t col, int ncols,
                                                   float* stage, const StoreFn& store,

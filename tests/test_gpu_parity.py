@@ -184,6 +184,37 @@ def test_addmm_ragged_k_workloads():
         del out
 
 
+# Tile widths of 16 mod 32 (the planner takes them from 112 up when they fill
+# the 152 SMs better): the last 32-column chunk of such a tile is half inside
+# it, and neither epilogue may write the next tile's columns.  Plans (3xTF32):
+# 1024x3072x768 -> BN 176, one wave of 144 tiles (A from TMEM, TMA-store
+# epilogue; with an [M,N] self the shared-memory form and the generic store);
+# 577x768x768 -> BN 112 in 4 K-slices; 600x3070x768 -> BN 112 with N % 4 != 0
+# (generic store); 1100x2200x640 -> BN 144, ragged M and N.
+HALF_CHUNK = [  # M, N, K, self_2d
+    (1024, 3072, 768, False), (1024, 3072, 768, True), (577, 768, 768, False),
+    (600, 3070, 768, False), (1100, 2200, 640, False),
+]
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1"])
+@pytest.mark.parametrize("idx", range(len(HALF_CHUNK)))
+def test_addmm_half_chunk_tile_widths(mode, idx):
+    M, N, K, s2 = HALF_CHUNK[idx]
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=s2, workload=700 + idx)
+    out = binding.addmm(dev(s), dev(a), dev(b), beta=0.75, alpha=1.25, mode=mode)
+    torch.cuda.synchronize()
+    assert binding.last_kernel() == EXPECT[mode]
+    ref, S = oracle.addmm(s, a, b, beta=0.75, alpha=1.25)
+    within(out.cpu().numpy(), ref, S, TOL[mode], f"{mode} {M}x{N}x{K} self_2d={s2}")
+    if idx in (0, 3):  # integer inputs: bit-exact, and a ReLU on the way out
+        si, ai, bi = synth.addmm_inputs(M, N, K, self_2d=s2, workload=720 + idx,
+                                        mat1=("I", -3, 3), mat2=("I", -3, 3), self_=("I", -9, 9))
+        got = binding.addmm(dev(si), dev(ai), dev(bi), mode=mode, relu=True).cpu().numpy()
+        ref, _ = oracle.addmm(si, ai, bi)
+        assert np.array_equal(got.astype(np.float64), np.maximum(ref, 0.0))
+
+
 def test_addmm_unaligned_mat1():
     # mat1 starting 4 bytes past a 16-byte boundary: the library pool path
     # copies it to aligned rows (tensor cores); a caller workspace with room
