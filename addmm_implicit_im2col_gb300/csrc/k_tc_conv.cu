@@ -17,7 +17,7 @@
 //   K order     with IC >= 8, k runs over (kh, kw, ic) inside the kernel --
 //               input channel fastest -- instead of the pages' (ic, kh, kw):
 //               a sum does not depend on the order of its terms up to
-//               rounding, and this way the 8 k a thread gathers per k-block
+//               rounding, and this way the 16 k a thread gathers per k-block
 //               usually share one spatial tap (one bounds check, then reads
 //               at a fixed channel-plane stride).  Few channels keep the pages'
 //               order, where consecutive k reuse the same input rows.
@@ -27,9 +27,9 @@
 //               TMA-loaded whatever K is
 //   warps 0-7   im2col gather: warp w fills TMEM lanes 32*(w%4) .. +31 (32
 //               positions) with all 16 k of every other k-block (those whose
-//               index has parity w/4); the values of its next two k-blocks are
-//               in flight while one is split into TF32 hi / lo and written to
-//               its stage (tcgen05.st)
+//               index has parity w/4); the values of its next k-block are in
+//               flight while one is split into TF32 hi / lo and written to its
+//               stage (tcgen05.st)
 //   warp 8      TMA producer of the weight tiles (BN x 16 fp32, 64B swizzle)
 //   warp 9      TMEM owner + MMA issuer, A from TMEM and B from shared memory:
 //               A_lo*B_hi + A_hi*B_lo + A_hi*B_hi per k-step of 8, or A*B
@@ -38,6 +38,13 @@
 //               leaves by one 3-D TMA store per 32-channel chunk, other tiles
 //               (and K-slice partial sums) as 512-byte runs of positions per
 //               channel
+//   warp 14     slab form only (few input channels, see slab_geometry): the
+//               position tile is 4 output rows x 32 output columns, and this
+//               warp brings each tile's input window [IC][rows][columns] into
+//               one of two shared-memory slabs by one 4-D TMA box (zeros
+//               outside the image); the gather warps then read the im2col
+//               values from the slab through a k offset table, and whole
+//               tiles leave by 4-D TMA stores clipped at the image edges
 // TMEM columns 0-255 hold the accumulator (two of 128 when BN <= 128, so the
 // epilogue of one tile overlaps the next), columns 256-511 the A stages (32
 // columns each: hi 0-15, lo 16-31).
