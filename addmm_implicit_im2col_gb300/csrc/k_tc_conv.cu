@@ -67,7 +67,7 @@ namespace {
 using namespace tc;
 
 constexpr int BK = 16;           // fp32 per k-block: one 64-byte swizzle row
-constexpr int KSTEPS = BK / UK;  // 2
+static_assert(BK == 2 * UK, "a k-block is two MMA k-steps");
 constexpr int BN_MAX = 256;
 constexpr int GATHER_WARPS = 8;
 constexpr int TMA_WARP = 8, MMA_WARP = 9, EPI_WARP0 = 10, SLAB_WARP = 14;
@@ -543,6 +543,16 @@ __global__ void __launch_bounds__(threads_of(GM), 1)
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = ptx::idesc_tf32(BM, (uint32_t)q.bn, false, false);
+      // Operand addresses advance by constants (the issuing thread's few
+      // instructions between MMAs are on the pipeline's critical path):
+      // B descriptors of stage s at k-step 0 = b0 + s * (w_bytes >> 4) (a
+      // descriptor holds the address >> 4 in its low 14 bits); k-step 1 adds
+      // 32 bytes (2), the lo tile b_tile bytes; the A stage's TMEM columns.
+      const uint64_t b0 = sw64_desc(ptx::smem_addr(smem), 0);
+      const uint64_t b_step = (uint64_t)(q.w_bytes >> 4), lo = (uint64_t)(b_tile >> 4);
+      const uint32_t a0 = tmem + A_COL0;
+      uint64_t bs = b0;
+      uint32_t as = a0;
       int s = 0, ul = 0;
       uint32_t ph = 0;
       for (int u = blockIdx.x; u < q.units; u += gridDim.x, ++ul) {
@@ -559,26 +569,27 @@ __global__ void __launch_bounds__(threads_of(GM), 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t bst = ptx::smem_addr(smem + s * q.w_bytes);
-          const uint32_t a = tmem + A_COL0 + (uint32_t)s * A_STAGE_COLS;
-#pragma unroll
-          for (int ks = 0; ks < KSTEPS; ++ks) {
-            const uint32_t ah = a + (uint32_t)(ks * UK);
-            const uint64_t bh = sw64_desc(bst, ks);
-            const uint32_t acc = (kb > un.kb0 || ks > 0) ? 1u : 0u;
-            if (THREE) {
-              const uint64_t bl = sw64_desc(bst + (uint32_t)b_tile, ks);
-              ptx::mma_tf32_ts(d, ah + 16u, bh, idesc, acc);  // A_lo * B_hi
-              ptx::mma_tf32_ts(d, ah, bl, idesc, 1u);         // A_hi * B_lo
-              ptx::mma_tf32_ts(d, ah, bh, idesc, 1u);         // A_hi * B_hi
-            } else {
-              ptx::mma_tf32_ts(d, ah, bh, idesc, acc);
-            }
+          const uint32_t acc = kb > un.kb0 ? 1u : 0u;
+          if (THREE) {  // k-step 0, then k-step 1 (TMEM columns + UK, descriptors + 2)
+            ptx::mma_tf32_ts(d, as + 16u, bs, idesc, acc);       // A_lo * B_hi
+            ptx::mma_tf32_ts(d, as, bs + lo, idesc, 1u);         // A_hi * B_lo
+            ptx::mma_tf32_ts(d, as, bs, idesc, 1u);              // A_hi * B_hi
+            ptx::mma_tf32_ts(d, as + 16u + UK, bs + 2, idesc, 1u);
+            ptx::mma_tf32_ts(d, as + UK, bs + lo + 2, idesc, 1u);
+            ptx::mma_tf32_ts(d, as + UK, bs + 2, idesc, 1u);
+          } else {
+            ptx::mma_tf32_ts(d, as, bs, idesc, acc);
+            ptx::mma_tf32_ts(d, as + UK, bs + 2, idesc, 1u);
           }
           ptx::mma_commit(&ctl->empty[s]);
           if (++s == q.stages) {
             s = 0;
             ph ^= 1u;
+            bs = b0;
+            as = a0;
+          } else {
+            bs += b_step;
+            as += A_STAGE_COLS;
           }
         }
         if (!ok) break;
