@@ -55,7 +55,7 @@ namespace {
 using namespace tc;
 
 constexpr int BK = 16;           // fp32 per k-block: one 64-byte swizzle row
-constexpr int KSTEPS = BK / UK;  // 2
+static_assert(BK == 2 * UK, "a k-block is two MMA k-steps");
 constexpr int BN_MAX = 256;
 constexpr int A_BYTES = BM * BK * 4;      // 8 KB
 constexpr int B_BYTES = BN_MAX * BK * 4;  // 16 KB
@@ -438,6 +438,17 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = ptx::idesc_tf32(BM, (uint32_t)bn, false, false);
+      // Operand addresses advance by constants (the issuing thread's few
+      // instructions between MMAs are on the pipeline's critical path): a
+      // descriptor holds the shared address >> 4 in its low 14 bits, so the
+      // stage, the tile within it and k-step 1 (+32 bytes) are plain adds.
+      constexpr uint64_t kStage = (uint64_t)(L.bytes >> 4), kA = (uint64_t)(L.a >> 4),
+                         kAlo = (uint64_t)(L.a_lo >> 4), kBhi = (uint64_t)(L.b_hi >> 4),
+                         kBlo = (uint64_t)(L.b_lo >> 4), kK1 = 2;
+      const uint64_t d0 = sw64_desc(ptx::smem_addr(smem), 0);
+      const uint32_t t0 = tmem + TS_A_COL0;
+      uint64_t ds = d0;   // stage s, k-step 0
+      uint32_t ts = t0;   // stage s's A columns (A-from-TMEM form)
       int s = 0, tl = 0;
       uint32_t ph = 0;
       for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++tl) {
@@ -454,30 +465,34 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t st = ptx::smem_addr(smem + s * L.bytes);
-#pragma unroll
-          for (int ks = 0; ks < KSTEPS; ++ks) {
-            const uint64_t ah = sw64_desc(st + L.a, ks), bh = sw64_desc(st + L.b_hi, ks);
-            const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
-            if (TS) {
-              const uint32_t th = tmem + TS_A_COL0 + (uint32_t)s * TS_A_STAGE_COLS + ks * UK;
-              const uint64_t bl = sw64_desc(st + L.b_lo, ks);
-              ptx::mma_tf32_ts(d, th + 16u, bh, idesc, acc);  // A_lo * B_hi
-              ptx::mma_tf32_ts(d, th, bl, idesc, 1u);         // A_hi * B_lo
-              ptx::mma_tf32_ts(d, th, bh, idesc, 1u);         // A_hi * B_hi
-            } else if (THREE) {
-              const uint64_t al = sw64_desc(st + L.a_lo, ks), bl = sw64_desc(st + L.b_lo, ks);
-              ptx::mma_tf32(d, al, bh, idesc, acc);  // small terms first
-              ptx::mma_tf32(d, ah, bl, idesc, 1u);
-              ptx::mma_tf32(d, ah, bh, idesc, 1u);
-            } else {
-              ptx::mma_tf32(d, ah, bh, idesc, acc);
-            }
+          const uint32_t acc = kb > kb0 ? 1u : 0u;
+          if (TS) {  // k-step 0, then k-step 1 (TMEM columns + UK, descriptors + 2)
+            ptx::mma_tf32_ts(d, ts + 16u, ds + kBhi, idesc, acc);  // A_lo * B_hi
+            ptx::mma_tf32_ts(d, ts, ds + kBlo, idesc, 1u);         // A_hi * B_lo
+            ptx::mma_tf32_ts(d, ts, ds + kBhi, idesc, 1u);         // A_hi * B_hi
+            ptx::mma_tf32_ts(d, ts + 16u + UK, ds + kBhi + kK1, idesc, 1u);
+            ptx::mma_tf32_ts(d, ts + UK, ds + kBlo + kK1, idesc, 1u);
+            ptx::mma_tf32_ts(d, ts + UK, ds + kBhi + kK1, idesc, 1u);
+          } else if (THREE) {  // small terms first
+            ptx::mma_tf32(d, ds + kAlo, ds + kBhi, idesc, acc);
+            ptx::mma_tf32(d, ds + kA, ds + kBlo, idesc, 1u);
+            ptx::mma_tf32(d, ds + kA, ds + kBhi, idesc, 1u);
+            ptx::mma_tf32(d, ds + kAlo + kK1, ds + kBhi + kK1, idesc, 1u);
+            ptx::mma_tf32(d, ds + kA + kK1, ds + kBlo + kK1, idesc, 1u);
+            ptx::mma_tf32(d, ds + kA + kK1, ds + kBhi + kK1, idesc, 1u);
+          } else {
+            ptx::mma_tf32(d, ds + kA, ds + kBhi, idesc, acc);
+            ptx::mma_tf32(d, ds + kA + kK1, ds + kBhi + kK1, idesc, 1u);
           }
           ptx::mma_commit(&ctl->empty[s]);
           if (++s == L.stages) {
             s = 0;
             ph ^= 1u;
+            ds = d0;
+            ts = t0;
+          } else {
+            ds += kStage;
+            ts += TS_A_STAGE_COLS;
           }
         }
         if (!ok) break;
