@@ -170,27 +170,36 @@ __device__ __forceinline__ Tile2 tile2d(const Sched& q, int pt) {
 // ------------------------------------------------------- weight pre-pass
 // Column k of row oc takes w[oc, ic, kh, kw]: k = ic*taps + tap (the pages'
 // order) or, with icf, k = tap*IC + ic (tap = kh*KW + kw).  w_hi gets its TF32
-// part (0 for k >= K), w_lo the rest.  Block (x, y) covers columns of rows
-// y, y + gridDim.y, ...
+// part (0 for k >= K), w_lo the rest.  Thread = column k (grid-stride in x),
+// rows 4 at a time (loads first) from 4*blockIdx.y in steps of 4*gridDim.y.
+// The grid is sized to be resident at once beside the main kernel's CTAs, so
+// that the main kernel (launched as its dependent) starts without waiting for
+// pre-pass blocks to drain.
 __global__ void __launch_bounds__(256) k_prep_w(const float* __restrict__ w, int OC, int K, int Kp,
                                                 int IC, int taps, int icf, float* __restrict__ w_hi,
                                                 float* __restrict__ w_lo) {
   ptx::griddep_launch();  // the main kernel may start its prologue and gathers
-  for (int oc = blockIdx.y; oc < OC; oc += gridDim.y) {
-    const float* wr = w + (int64_t)oc * K;
-    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < Kp; k += gridDim.x * blockDim.x) {
-      int src = k;
-      if (icf) {
-        const int tap = k / IC;
-        src = (k - tap * IC) * taps + tap;
-      }
-      const float v = k < K ? __ldg(wr + src) : 0.0f;
-      const int64_t e = (int64_t)oc * Kp + k;
-      if (w_lo) {
-        w_hi[e] = tf32_hi(v);
-        w_lo[e] = tf32_lo(v);
-      } else {
-        w_hi[e] = v;
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < Kp; k += gridDim.x * blockDim.x) {
+    int src = k;
+    if (icf) {
+      const int tap = k / IC;
+      src = (k - tap * IC) * taps + tap;
+    }
+    for (int oc0 = 4 * (int)blockIdx.y; oc0 < OC; oc0 += 4 * (int)gridDim.y) {
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        v[i] = (oc0 + i < OC && k < K) ? __ldg(w + (int64_t)(oc0 + i) * K + src) : 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (oc0 + i >= OC) break;
+        const int64_t e = (int64_t)(oc0 + i) * Kp + k;
+        if (w_lo) {
+          w_hi[e] = tf32_hi(v[i]);
+          w_lo[e] = tf32_lo(v[i]);
+        } else {
+          w_hi[e] = v[i];
+        }
       }
     }
   }
@@ -1096,8 +1105,10 @@ cudaError_t launch_tc_conv(const ConvArgs& c, bool three_pass, void* workspace,
   float* w_hi = static_cast<float*>(workspace);
   float* w_lo = three_pass ? w_hi + c.OC * Kp : nullptr;
   float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.part_off);
+  // at most two pre-pass blocks per SM (see k_prep_w)
   const int gx = (int)((Kp + 255) / 256 < 64 ? (Kp + 255) / 256 : 64);
-  const int gy = (int)(c.OC < 1024 ? c.OC : 1024);
+  const int gy_cap = 2 * device_sm_count() / gx > 1 ? 2 * device_sm_count() / gx : 1;
+  const int gy = std::max(1, (int)((c.OC + 3) / 4 < gy_cap ? (c.OC + 3) / 4 : gy_cap));
   k_prep_w<<<dim3(gx, gy), 256, 0, s>>>(c.w, c.OC, (int)c.K, (int)Kp, c.IC, c.KH * c.KW,
                                         ic_fastest(c) ? 1 : 0, w_hi, w_lo);
   note_launch();
