@@ -170,12 +170,22 @@ __global__ void __launch_bounds__(256) k_prep_b4(const float* __restrict__ mat2,
 
 // linear: the weight w[N,K] is already K-major and serves as B_hi as it is
 // (the tensor core truncates to TF32); 3xTF32 needs only w_lo = w - tf32(w).
-__global__ void __launch_bounds__(256) k_prep_blo(const float* __restrict__ w, int64_t total,
-                                                  float* __restrict__ w_lo) {
+// 16-byte elements, four in flight per thread; the grid (at most two blocks
+// per SM) stays resident beside the main kernel's CTAs, so the main kernel,
+// launched as its dependent, starts without waiting for pre-pass blocks.
+__global__ void __launch_bounds__(256) k_prep_blo(const float4* __restrict__ w, int64_t total4,
+                                                  float4* __restrict__ w_lo) {
   ptx::griddep_launch();
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x)
-    w_lo[i] = tf32_lo(__ldg(w + i));
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total4; i += 4 * stride) {
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      v[j] = i + j * stride < total4 ? __ldg(w + i + j * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (i + j * stride < total4) w_lo[i + j * stride] = tf32_lo4(v[j]);
+  }
 }
 
 // A [rows, K] operand whose rows are not 16-byte aligned (K % 4 != 0 or an
@@ -899,8 +909,11 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
     b_lo = three_pass ? ws : nullptr;
     ldb = g.K;  // == ld: K % 4 == 0 here
     if (three_pass) {
-      const int64_t total = g.N * g.K, blocks = (total + 255) / 256;
-      k_prep_blo<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(g.mat2, total, ws);
+      // K % 4 == 0 and 16-byte aligned rows here: whole float4s
+      const int64_t total4 = g.N * g.K / 4, blocks = (total4 + 255) / 256;
+      const int64_t cap2 = 2 * (int64_t)device_sm_count();
+      k_prep_blo<<<(unsigned)(blocks < cap2 ? blocks : cap2), 256, 0, s>>>(
+          reinterpret_cast<const float4*>(g.mat2), total4, reinterpret_cast<float4*>(ws));
       note_launch();
       prep = true;
     }
