@@ -591,15 +591,12 @@ __global__ void __launch_bounds__(threads_of(GM), 1)
             ptx::mma_tf32_ts(d, as + UK, bs + 2, idesc, 1u);
           }
           ptx::mma_commit(&ctl->empty[s]);
-          if (++s == q.stages) {
-            s = 0;
-            ph ^= 1u;
-            bs = b0;
-            as = a0;
-          } else {
-            bs += b_step;
-            as += A_STAGE_COLS;
-          }
+          // next stage, by selects (no branch between this k-block's MMAs and the next wait)
+          const bool wrap = ++s == q.stages;
+          s = wrap ? 0 : s;
+          ph ^= wrap ? 1u : 0u;
+          bs = wrap ? b0 : bs + b_step;
+          as = wrap ? a0 : as + A_STAGE_COLS;
         }
         if (!ok) break;
         ptx::mma_commit(&ctl->accf[buf]);
