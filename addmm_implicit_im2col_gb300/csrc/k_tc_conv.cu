@@ -13,7 +13,8 @@
 // reads only the weight tile from shared memory, and the gather never writes
 // shared memory):
 //   tile        128 output positions p (TMEM lanes) x BN output channels
-//               (BN a multiple of 16, at most 256)
+//               (BN at most 256, a multiple of 16, of 32 when OC needs
+//               several channel tiles)
 //   K order     with IC >= 8, k runs over (kh, kw, ic) inside the kernel --
 //               input channel fastest -- instead of the pages' (ic, kh, kw):
 //               a sum does not depend on the order of its terms up to
@@ -898,7 +899,8 @@ bool slab_geometry(const ConvArgs& c, Sched& q, int w_bytes) {
   return true;
 }
 
-// Channel tiles of at most 256 (as even as possible, multiples of 16);
+// Channel tiles of at most 256 (as even as possible, multiples of 16, or of
+// 32 when there are several);
 // 128-position tiles (SLAB_ROWS x SLAB_COLS in the slab form); K-slices for the tail tiles when they shorten the
 // longest CTA's work and the partial sums fit in `limit` bytes of workspace.
 // Cost in k-block times of one CTA: whole-tile waves, the sliced wave(s), the
@@ -910,7 +912,11 @@ Plan make_plan(const ConvArgs& c, bool three, size_t limit) {
   Plan pl{};
   Sched& q = pl.q;
   q.n_oc = (int)((OC + BN_MAX - 1) / BN_MAX);
-  q.bn = (int)(((OC + q.n_oc - 1) / q.n_oc + 15) / 16 * 16);
+  // The epilogue writes 32-channel blocks, and a TMA box is clipped only at
+  // OC: with several channel tiles each is a multiple of 32 wide, so that no
+  // block reaches into the next tile's channels (one tile: a multiple of 16).
+  const int64_t per_tile = (OC + q.n_oc - 1) / q.n_oc;
+  q.bn = (int)(q.n_oc > 1 ? (per_tile + 31) / 32 * 32 : (per_tile + 15) / 16 * 16);
   q.kb = (int)((K + BK - 1) / BK);
   int64_t ptiles;
   if (slab_geometry(c, q, (three ? 2 : 1) * q.bn * BK * 4)) {

@@ -608,6 +608,23 @@ def test_conv_slab_shape_with_unaligned_input_takes_the_global_gather():
     within(out.cpu().numpy(), ref, S, 1e-5, "unaligned x")
 
 
+# OC > 256 in two channel tiles whose even split is 16 mod 32 wide (275 ->
+# 138): the tiles are widened to 160 so that no 32-channel output block of one
+# tile reaches into the next; global gather and slab form, both epilogues
+# (whole tiles by TMA store, K-slice partial sums).
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1"])
+@pytest.mark.parametrize("shape", [
+    (1, 21, 6, 71, 275, 1, 6, (3, 2), (2, 2), (2, 2)),   # channel-fastest gather
+    (1, 3, 64, 128, 275, 3, 3, 1, 1, 1),                # slab form
+    (2, 40, 30, 30, 300, 3, 3, 1, 1, 1),                # K-sliced tail tiles
+])
+def test_conv_several_channel_tiles(mode, shape):
+    x, w, b, s, p, d = _conv_case(shape, 580 + shape[4] + shape[1])
+    got, ref, S, kern = run_conv(x, w, b, s, p, d, mode)
+    assert kern == EXPECT[mode]
+    within(got, ref, S, TOL[mode], f"{mode} conv {shape}")
+
+
 def test_launch_counter_and_watchdog():
     n0 = binding.launch_count()
     s, a, b = synth.addmm_inputs(256, 256, 64, self_2d=False, workload=3)

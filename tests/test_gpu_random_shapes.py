@@ -1,0 +1,112 @@
+"""GPU parity on seeded random shapes: addmm and conv2d in every mode against
+the oracle, to reach planner paths the hand-picked cases may miss (tile widths
+of 16 mod 32, K-slices, ragged edges, the conv's slab form with few input
+channels, per-axis stride / padding / dilation).
+
+Shapes come from a fixed numpy generator (the same list on every run), sized so
+that the oracle finishes each case in well under a second.  The tolerance is
+the one the other parity tests use: 1e-5 * S + 1e-6 per element for 3xTF32 and
+SIMT, 2e-3 * S + 1e-6 for 1xTF32 (S = the sum of |products| of the element).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from addmm_implicit_im2col_gb300 import binding, build, synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"default": 1e-5, "force_tc3": 1e-5, "force_tc1": 2e-3, "simt": 1e-5}
+MODES = ["default", "force_tc3", "force_tc1"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    build.build()
+    binding.load()
+
+
+def dev(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def within(got, ref, S, c, what):
+    err = np.abs(np.asarray(got, np.float64) - ref)
+    ratio = float((err / (c * S + 1e-6)).max()) if err.size else 0.0
+    assert ratio <= 1.0, f"{what}: worst |err|/tol = {ratio:.3g}"
+
+
+def _addmm_shapes(n=24, seed=2024):
+    rng = np.random.RandomState(seed)
+    out = []
+    while len(out) < n:
+        M, N, K = int(rng.randint(1, 1300)), int(rng.randint(1, 3300)), int(rng.randint(1, 1300))
+        if M * N * K > 6e8:
+            continue
+        out.append((M, N, K, bool(rng.randint(2)), float(rng.choice([1.0, 0.5, -1.25, 0.0])),
+                    float(rng.choice([1.0, 2.0, 0.75]))))
+    return out
+
+
+def _conv_shapes(n=24, seed=7):
+    rng = np.random.RandomState(seed)
+    out = []
+    while len(out) < n:
+        B, IC, OC = int(rng.randint(1, 4)), int(rng.randint(1, 40)), int(rng.randint(1, 300))
+        KH, KW = int(rng.randint(1, 8)), int(rng.randint(1, 8))
+        s = (int(rng.randint(1, 5)), int(rng.randint(1, 5)))
+        p = (int(rng.randint(0, 4)), int(rng.randint(0, 4)))
+        d = (int(rng.randint(1, 3)), int(rng.randint(1, 3)))
+        H = int(rng.randint(1, 90))
+        kind = len(out) % 3
+        if kind == 0:
+            W = int(rng.randint(1, 130))
+        else:
+            # few input channels, W and OW multiples of 4 (kind 1), or OW a
+            # multiple of 32 and OH of 4 (kind 2): the slab form's territory
+            IC = int(rng.randint(1, 8 if kind == 1 else 5))
+            OW = 4 * int(rng.randint(2, 48)) if kind == 1 else 32 * int(rng.randint(1, 5))
+            w_min = (OW - 1) * s[1] + d[1] * (KW - 1) + 1 - 2 * p[1]
+            W = (max(w_min, 4) + 3) // 4 * 4
+            if kind == 2:
+                OH = 4 * int(rng.randint(1, 12))
+                H = max(1, (OH - 1) * s[0] + d[0] * (KH - 1) + 1 - 2 * p[0])
+        OH = (H + 2 * p[0] - d[0] * (KH - 1) - 1) // s[0] + 1
+        OW = (W + 2 * p[1] - d[1] * (KW - 1) - 1) // s[1] + 1
+        if OH < 1 or OW < 1 or B * OC * OH * OW * IC * KH * KW > 2.5e8:
+            continue
+        out.append((B, IC, H, W, OC, KH, KW, s, p, d))
+    return out
+
+
+ADDMM = _addmm_shapes()
+CONV = _conv_shapes()
+
+
+@pytest.mark.parametrize("idx", range(len(ADDMM)))
+def test_random_addmm(idx):
+    M, N, K, s2, beta, alpha = ADDMM[idx]
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=s2, workload=1000 + idx)
+    ref, S = oracle.addmm(s, a, b, beta=beta, alpha=alpha)
+    for mode in MODES:
+        out = binding.addmm(dev(s), dev(a), dev(b), beta=beta, alpha=alpha, mode=mode)
+        torch.cuda.synchronize()
+        within(out.cpu().numpy(), ref, S, TOL[mode],
+               f"addmm {M}x{N}x{K} self_2d={s2} beta={beta} alpha={alpha} {mode} "
+               f"({binding.last_kernel_name()})")
+
+
+@pytest.mark.parametrize("idx", range(len(CONV)))
+def test_random_conv(idx):
+    B, IC, H, W, OC, KH, KW, st, pd, dl = CONV[idx]
+    x, w, bias = synth.conv_inputs(B, IC, H, W, OC, KH, KW, workload=1100 + idx)
+    ref, S = oracle.conv2d(x, w, bias, st, pd, dl)
+    for mode in MODES:
+        out = binding.conv2d(dev(x), dev(w), dev(bias), st, pd, dl, mode=mode)
+        torch.cuda.synchronize()
+        within(out.cpu().numpy(), ref, S, TOL[mode],
+               f"conv {B}x{IC}x{H}x{W}->{OC} {KH}x{KW} s{st} p{pd} d{dl} {mode} "
+               f"({binding.last_kernel_name()})")
