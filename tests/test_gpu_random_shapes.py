@@ -1,4 +1,4 @@
-"""GPU parity on seeded random shapes: addmm and conv2d in every mode against
+"""GPU parity on seeded random shapes: addmm, linear and conv2d in every mode against
 the oracle, to reach planner paths the hand-picked cases may miss (tile widths
 of 16 mod 32, K-slices, ragged edges, the conv's slab form with few input
 channels, per-axis stride / padding / dilation).
@@ -39,7 +39,7 @@ def within(got, ref, S, c, what):
     assert ratio <= 1.0, f"{what}: worst |err|/tol = {ratio:.3g}"
 
 
-def _addmm_shapes(n=24, seed=2024):
+def _addmm_shapes(n=60, seed=2024):
     rng = np.random.RandomState(seed)
     out = []
     while len(out) < n:
@@ -51,7 +51,7 @@ def _addmm_shapes(n=24, seed=2024):
     return out
 
 
-def _conv_shapes(n=24, seed=7):
+def _conv_shapes(n=60, seed=7):
     rng = np.random.RandomState(seed)
     out = []
     while len(out) < n:
@@ -82,8 +82,20 @@ def _conv_shapes(n=24, seed=7):
     return out
 
 
+def _linear_shapes(n=24, seed=99):
+    rng = np.random.RandomState(seed)
+    out = []
+    while len(out) < n:
+        M, N, K = int(rng.randint(1, 1500)), int(rng.randint(1, 3300)), int(rng.randint(1, 3300))
+        if M * N * K > 6e8:
+            continue
+        out.append((M, N, K, bool(rng.randint(2)), bool(rng.randint(2))))
+    return out
+
+
 ADDMM = _addmm_shapes()
 CONV = _conv_shapes()
+LINEAR = _linear_shapes()
 
 
 @pytest.mark.parametrize("idx", range(len(ADDMM)))
@@ -91,8 +103,11 @@ def test_random_addmm(idx):
     M, N, K, s2, beta, alpha = ADDMM[idx]
     s, a, b = synth.addmm_inputs(M, N, K, self_2d=s2, workload=1000 + idx)
     ref, S = oracle.addmm(s, a, b, beta=beta, alpha=alpha)
+    relu = idx % 3 == 1
+    if relu:
+        ref = np.maximum(ref, 0.0)
     for mode in MODES:
-        out = binding.addmm(dev(s), dev(a), dev(b), beta=beta, alpha=alpha, mode=mode)
+        out = binding.addmm(dev(s), dev(a), dev(b), beta=beta, alpha=alpha, mode=mode, relu=relu)
         torch.cuda.synchronize()
         within(out.cpu().numpy(), ref, S, TOL[mode],
                f"addmm {M}x{N}x{K} self_2d={s2} beta={beta} alpha={alpha} {mode} "
@@ -104,9 +119,31 @@ def test_random_conv(idx):
     B, IC, H, W, OC, KH, KW, st, pd, dl = CONV[idx]
     x, w, bias = synth.conv_inputs(B, IC, H, W, OC, KH, KW, workload=1100 + idx)
     ref, S = oracle.conv2d(x, w, bias, st, pd, dl)
+    relu = idx % 3 == 1
+    if relu:
+        ref = np.maximum(ref, 0.0)
     for mode in MODES:
-        out = binding.conv2d(dev(x), dev(w), dev(bias), st, pd, dl, mode=mode)
+        out = binding.conv2d(dev(x), dev(w), dev(bias), st, pd, dl, mode=mode, relu=relu)
         torch.cuda.synchronize()
         within(out.cpu().numpy(), ref, S, TOL[mode],
                f"conv {B}x{IC}x{H}x{W}->{OC} {KH}x{KW} s{st} p{pd} d{dl} {mode} "
+               f"({binding.last_kernel_name()})")
+
+
+@pytest.mark.parametrize("idx", range(len(LINEAR)))
+def test_random_linear(idx):
+    M, N, K, with_bias, relu = LINEAR[idx]
+    x = synth.normal(synth.stream_key(0, 1200 + idx, 1), M * K).reshape(M, K)
+    sc = 1.0 / np.sqrt(K)
+    w = synth.uniform(synth.stream_key(0, 1200 + idx, 2), N * K, -sc, sc).reshape(N, K)
+    b = synth.normal(synth.stream_key(0, 1200 + idx, 3), N, 0.0, 0.02) if with_bias else None
+    ref, S = oracle.addmm(b, x, np.ascontiguousarray(w.T), beta=1.0 if b is not None else 0.0,
+                          alpha=1.0, self_2d=False)
+    if relu:
+        ref = np.maximum(ref, 0.0)
+    for mode in MODES:
+        out = binding.linear(dev(x), dev(w), dev(b), mode=mode, relu=relu)
+        torch.cuda.synchronize()
+        within(out.cpu().numpy(), ref, S, TOL[mode],
+               f"linear {M}x({K}->{N}) bias={with_bias} relu={relu} {mode} "
                f"({binding.last_kernel_name()})")
