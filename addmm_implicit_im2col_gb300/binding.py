@@ -251,6 +251,10 @@ def _addmm_dims(self, mat1, mat2, host):
     return M, N, K, self_2d
 
 
+def _aligned16(t):
+    return t.data_ptr() % 16 == 0
+
+
 def addmm(self, mat1, mat2, *, beta=1.0, alpha=1.0, mode="default", relu=False, out=None):
     """out = beta*self + alpha*(mat1 @ mat2) on the GPU (aten.addmm semantics).
 
@@ -264,8 +268,12 @@ def addmm(self, mat1, mat2, *, beta=1.0, alpha=1.0, mode="default", relu=False, 
         out = torch.empty((M, N), dtype=torch.float32, device=mat1.device)
     else:
         _check_tensor(out, "out", (2,))
-    # scratch for the transposed mat2 comes from torch's allocator
+    # scratch for the transposed mat2 comes from torch's allocator; the size
+    # query assumes 16-byte aligned operands, and imc.h documents the extra
+    # mat1 copy (M * Kp * 4 bytes) an unaligned mat1 needs
     nbytes = gemm_addmm_f32_workspace_bytes(M, N, K, MODES[mode])
+    if nbytes and K % 4 == 0 and not _aligned16(mat1):
+        nbytes += M * K * 4 + 256
     ws = torch.empty(nbytes, dtype=torch.uint8, device=mat1.device) if nbytes else None
     rc = gemm_addmm_f32_ws(_ptr(self), self_2d, _ptr(mat1), _ptr(mat2), _ptr(out), M, N, K,
                            float(beta), float(alpha), _mode(mode, relu), _ptr(ws), nbytes,
@@ -295,6 +303,14 @@ def linear(x, w, bias=None, *, mode="default", relu=False, out=None):
     else:
         _check_tensor(out, "out", (2,))
     nbytes = linear_f32_workspace_bytes(M, N, K, MODES[mode])
+    if MODES[mode] != MODES["simt"] and K % 4 == 0:
+        # the size query assumes 16-byte aligned operands; imc.h documents the
+        # copies an unaligned x (M * Kp * 4) or weight (hi and lo, 2 * N * Kp * 4)
+        # needs
+        if not _aligned16(x):
+            nbytes += M * K * 4 + 256
+        if not _aligned16(w):
+            nbytes += 2 * N * K * 4 + 256
     ws = torch.empty(nbytes, dtype=torch.uint8, device=x.device) if nbytes else None
     rc = linear_f32_ws(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), M, N, K, _mode(mode, relu),
                        _ptr(ws), nbytes, _stream_ptr(x.device))

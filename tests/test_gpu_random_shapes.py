@@ -147,3 +147,69 @@ def test_random_linear(idx):
         within(out.cpu().numpy(), ref, S, TOL[mode],
                f"linear {M}x({K}->{N}) bias={with_bias} relu={relu} {mode} "
                f"({binding.last_kernel_name()})")
+
+
+def _offset(a):
+    """a on the device one float past a 16-byte boundary (same values)."""
+    a = np.ascontiguousarray(a)
+    buf = torch.empty(a.size + 1, dtype=torch.float32, device="cuda")
+    v = buf[1:].view(a.shape)
+    v.copy_(torch.from_numpy(a))
+    return v
+
+
+@pytest.mark.parametrize("idx", range(0, len(ADDMM), 4))
+def test_random_addmm_integer_and_unaligned(idx):
+    # integer inputs: every product and partial sum is exact in fp32 and TF32,
+    # so each path must match the oracle bit for bit; then the same with every
+    # operand and the output one float off a 16-byte boundary
+    M, N, K, s2, beta, alpha = ADDMM[idx]
+    spec = ("I", -3, 3)
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=s2, workload=1300 + idx, mat1=spec, mat2=spec,
+                                 self_=spec)
+    beta, alpha = (1.0, 1.0) if beta != 0.0 else (0.0, 1.0)
+    ref, _ = oracle.addmm(s, a, b, beta=beta, alpha=alpha)
+    for mode in MODES + ["simt"]:
+        got = binding.addmm(dev(s), dev(a), dev(b), beta=beta, alpha=alpha, mode=mode)
+        assert np.array_equal(got.cpu().numpy().astype(np.float64), ref), \
+            f"addmm {M}x{N}x{K} {mode} ({binding.last_kernel_name()})"
+        out = _offset(np.zeros((M, N), np.float32))
+        got = binding.addmm(_offset(s), _offset(a), _offset(b), beta=beta, alpha=alpha, mode=mode,
+                            out=out)
+        assert np.array_equal(got.cpu().numpy().astype(np.float64), ref), \
+            f"unaligned addmm {M}x{N}x{K} {mode} ({binding.last_kernel_name()})"
+
+
+@pytest.mark.parametrize("idx", range(0, len(CONV), 4))
+def test_random_conv_integer_and_unaligned(idx):
+    B, IC, H, W, OC, KH, KW, st, pd, dl = CONV[idx]
+    spec = ("I", -3, 3)
+    x, w, bias = synth.conv_inputs(B, IC, H, W, OC, KH, KW, workload=1400 + idx, x=spec, w=spec,
+                                   bias=spec)
+    ref, _ = oracle.conv2d(x, w, bias, st, pd, dl)
+    for mode in MODES + ["simt"]:
+        got = binding.conv2d(dev(x), dev(w), dev(bias), st, pd, dl, mode=mode)
+        assert np.array_equal(got.cpu().numpy().astype(np.float64), ref), \
+            f"conv {CONV[idx]} {mode} ({binding.last_kernel_name()})"
+        out = _offset(np.zeros(ref.shape, np.float32))
+        got = binding.conv2d(_offset(x), _offset(w), _offset(bias), st, pd, dl, mode=mode, out=out)
+        assert np.array_equal(got.cpu().numpy().astype(np.float64), ref), \
+            f"unaligned conv {CONV[idx]} {mode} ({binding.last_kernel_name()})"
+
+
+@pytest.mark.parametrize("idx", range(0, len(LINEAR), 4))
+def test_random_linear_unaligned(idx):
+    M, N, K, with_bias, _ = LINEAR[idx]
+    spec = ("I", -3, 3)
+    from addmm_implicit_im2col_gb300.synth import _draw  # the seeded integer draws
+    x = _draw(spec, synth.stream_key(0, 1500 + idx, 1), M * K).reshape(M, K)
+    w = _draw(spec, synth.stream_key(0, 1500 + idx, 2), N * K).reshape(N, K)
+    b = _draw(spec, synth.stream_key(0, 1500 + idx, 3), N) if with_bias else None
+    ref, _ = oracle.addmm(b, x, np.ascontiguousarray(w.T), beta=1.0 if b is not None else 0.0,
+                          alpha=1.0, self_2d=False)
+    for mode in MODES + ["simt"]:
+        out = _offset(np.zeros((M, N), np.float32))
+        got = binding.linear(_offset(x), _offset(w), None if b is None else _offset(b), mode=mode,
+                             out=out)
+        assert np.array_equal(got.cpu().numpy().astype(np.float64), ref), \
+            f"unaligned linear {M}x({K}->{N}) {mode} ({binding.last_kernel_name()})"
