@@ -676,3 +676,49 @@ def test_a_wait_that_runs_out_is_reported_and_the_context_stays_usable():
     got, ref, S, kern = run_addmm(s, a, b, 0.5, 1.5, "default")
     assert kern == "tc3"
     within(got, ref, S, 1e-5, "after a timeout")
+
+
+def test_pool_backed_calls_on_four_streams():
+    """The exact boundary signatures take their scratch from the library's
+    stream-ordered pool: calls interleaved on four streams (each call's scratch
+    freed on its own stream while other streams keep allocating) must each give
+    their own oracle result."""
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    jobs = []
+    for i in range(12):
+        M, N, K = 300 + 37 * i, 520 + 24 * (i % 5), 388 + 16 * (i % 3)
+        s, a, b = synth.addmm_inputs(M, N, K, self_2d=bool(i % 2), workload=760 + i)
+        jobs.append(("addmm", (s, a, b), [dev(s), dev(a), dev(b)], (M, N, K, i % 2)))
+    for i in range(8):
+        shape = (2, 16 + 8 * (i % 3), 24, 24, 96 + 32 * (i % 4), 3, 3)
+        x, w, bias = synth.conv_inputs(*shape, workload=780 + i)
+        jobs.append(("conv", (x, w, bias), [dev(x), dev(w), dev(bias)], shape))
+    outs = []
+    for j, (kind, host, devs, dims) in enumerate(jobs):
+        st = streams[j % 4]
+        st.wait_stream(torch.cuda.current_stream())  # the inputs were written on it
+        with torch.cuda.stream(st):
+            if kind == "addmm":
+                M, N, K, s2 = dims
+                out = torch.full((M, N), float("nan"), device="cuda")
+                rc = binding.gemm_addmm_f32(devs[0].data_ptr(), s2, devs[1].data_ptr(),
+                                            devs[2].data_ptr(), out.data_ptr(), M, N, K, 1.0, 1.0,
+                                            st.cuda_stream)
+            else:
+                B, IC, H, W, OC, KH, KW = dims
+                out = torch.full((B, OC, H, W), float("nan"), device="cuda")
+                rc = binding.conv2d_gemm_f32(devs[0].data_ptr(), devs[1].data_ptr(),
+                                             devs[2].data_ptr(), out.data_ptr(), B, IC, H, W, OC,
+                                             KH, KW, 1, 1, 1, st.cuda_stream)
+            assert rc == binding.IMC_OK, binding.status_string(rc)
+            for t in devs:
+                t.record_stream(st)
+        outs.append(out)
+    torch.cuda.synchronize()
+    for (kind, host, _, dims), out in zip(jobs, outs):
+        if kind == "addmm":
+            ref, S = oracle.addmm(*host)
+        else:
+            ref, S = oracle.conv2d(host[0], host[1], host[2], 1, 1, 1)
+        within(out.cpu().numpy(), ref, S, 1e-5, f"{kind} {dims} on a side stream")
+    assert binding.check_device_error(None) == binding.IMC_OK
