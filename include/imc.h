@@ -36,7 +36,10 @@
  *    keeps fp32 accuracy: each product is split into TF32 pieces
  *    (3xTF32) on the tensor cores, or computed with fp32 FMA on the SIMT
  *    fallback.  IMC_MODE_TF32 is an explicitly requested faster mode with
- *    single TF32 products (about 3 fewer decimal digits).
+ *    single TF32 products (about 3 fewer decimal digits): the tensor core
+ *    truncates both operands to TF32, so a product may be off by up to
+ *    ~1.95e-3 of its magnitude (the error of out[i,j] is then bounded by
+ *    about 1.95e-3 * |alpha| * sum_k |mat1[i,k] * mat2[k,j]|).
  */
 #ifndef IMC_H
 #define IMC_H
