@@ -40,6 +40,13 @@
  *    truncates both operands to TF32, so a product may be off by up to
  *    ~1.95e-3 of its magnitude (the error of out[i,j] is then bounded by
  *    about 1.95e-3 * |alpha| * sum_k |mat1[i,k] * mat2[k,j]|).
+ *  - Non-finite inputs: the SIMT kernels follow IEEE arithmetic.  On the
+ *    tensor cores an output whose exact value is NaN comes out non-finite
+ *    (the tensor core reads a NaN whose payload lies only in the 13 low
+ *    mantissa bits as an infinity), an output whose exact value is +inf or
+ *    -inf comes out as that infinity -- or as NaN in the 3xTF32 mode, whose
+ *    cross products can multiply an infinity by a zero low part -- and
+ *    outputs no non-finite input reaches are unaffected.
  */
 #ifndef IMC_H
 #define IMC_H

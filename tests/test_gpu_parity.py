@@ -722,3 +722,72 @@ def test_pool_backed_calls_on_four_streams():
             ref, S = oracle.conv2d(host[0], host[1], host[2], 1, 1, 1)
         within(out.cpu().numpy(), ref, S, 1e-5, f"{kind} {dims} on a side stream")
     assert binding.check_device_error(None) == binding.IMC_OK
+
+
+def _plant_non_finite(a, spots):
+    """a with the given (index, kind) entries replaced: kind 'inf', '-inf',
+    'nan' (canonical quiet NaN) or 'nan_low' (a NaN whose payload lies only in
+    the 13 low mantissa bits, which a TF32 truncation would clear)."""
+    a = a.copy()
+    bits = a.view(np.uint32)
+    for idx, kind in spots:
+        if kind == "nan_low":
+            bits[idx] = np.uint32(0x7F800001)
+        else:
+            a[idx] = {"inf": np.inf, "-inf": -np.inf, "nan": np.nan}[kind]
+    return a
+
+
+def _same_non_finite(got, ref, S, tol, mode, what):
+    """The contract for non-finite inputs (imc.h): SIMT follows IEEE
+    arithmetic, so its NaN / +inf / -inf pattern equals the reference's.  On
+    the tensor cores an output the reference has as NaN is non-finite (a NaN
+    whose payload lies only in the 13 low mantissa bits reads as an infinity
+    there), one it has as +inf or -inf is that infinity (or NaN in 3xTF32,
+    whose cross products can multiply an infinity by a zero low part), and
+    every output the reference has finite is finite and within tolerance."""
+    got = np.asarray(got, np.float64)
+    if mode == "simt":
+        assert np.array_equal(np.isnan(got), np.isnan(ref)), f"{what}: NaN positions differ"
+    else:
+        assert np.all(~np.isfinite(got[np.isnan(ref)])), f"{what}: a NaN output came out finite"
+    for sign, pos in ((np.isposinf, "+inf"), (np.isneginf, "-inf")):
+        r = sign(ref)
+        ok = sign(got[r]) | (np.isnan(got[r]) if mode == "force_tc3" else False)
+        assert np.all(ok), f"{what}: a {pos} output came out as something else"
+    fin = np.isfinite(ref)
+    assert np.all(np.isfinite(got[fin])), f"{what}: a finite output came out non-finite"
+    within(got[fin], ref[fin], S[fin], tol, what + " (finite outputs)")
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1", "simt"])
+def test_addmm_non_finite_inputs_propagate(mode):
+    M, N, K = 200, 300, 132
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=False, workload=790)
+    a = _plant_non_finite(a, [((3, 5), "inf"), ((7, 9), "-inf"), ((11, 2), "nan"),
+                              ((13, 4), "nan_low")])
+    b = _plant_non_finite(b, [((6, 40), "inf"), ((8, 41), "nan_low"), ((9, 42), "-inf")])
+    b[5, 7] = 0.0  # row 3 of mat1 holds inf at k = 5: inf * 0 is NaN in column 7
+    ref, S = oracle.addmm(s, a, b)
+    out = binding.addmm(dev(s), dev(a), dev(b), mode=mode)
+    torch.cuda.synchronize()
+    assert binding.last_kernel() == {"force_tc3": "tc3", "force_tc1": "tc1", "simt": "simt"}[mode]
+    _same_non_finite(out.cpu().numpy(), ref, S, TOL[mode], mode, f"addmm {mode} non-finite")
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1", "simt"])
+@pytest.mark.parametrize("ic", [3, 32])  # slab form / channel-fastest gather
+def test_conv_non_finite_inputs_propagate(mode, ic):
+    B, H, W, OC = 1, 32, 64, 40
+    x, w, bias = synth.conv_inputs(B, ic, H, W, OC, 3, 3, workload=791 + ic)
+    x = _plant_non_finite(x, [((0, 1, 5, 7), "inf"), ((0, 2, 20, 30), "nan_low"),
+                              ((0, 0, 10, 50), "-inf"), ((0, 1, 25, 12), "nan")])
+    w = _plant_non_finite(w, [((17, 0, 1, 1), "nan_low"), ((30, 2, 0, 2), "inf")])
+    # padding taps read 0 and are multiplied like any other (an infinite
+    # weight times a padding zero is NaN): the reference is the oracle on the
+    # explicitly zero-padded input, which equals the padded form for finite data
+    xp = np.pad(x, ((0, 0), (0, 0), (1, 1), (1, 1)))
+    ref, S = oracle.conv2d(xp, w, bias, 1, 0, 1)
+    out = binding.conv2d(dev(x), dev(w), dev(bias), 1, 1, 1, mode=mode)
+    torch.cuda.synchronize()
+    _same_non_finite(out.cpu().numpy(), ref, S, TOL[mode], mode, f"conv IC={ic} {mode} non-finite")
