@@ -40,8 +40,11 @@
 //               memory and 16-byte row-segment stores
 //
 // One persistent CTA per SM walks 128 x BN tiles in a grouped raster; BN (32
-// to 256) is picked per problem to fill the SMs with few waves.  Every
-// barrier wait is bounded (see tc_common.cuh).
+// to 256: a multiple of 32, or of 16 from 112 up when K is not split) is
+// picked per problem to fill the SMs with few waves.  The MMA issuer keeps
+// its operand descriptors as running values (a few instructions per k-block
+// in the issuing thread are on the pipeline's critical path).  Every barrier
+// wait is bounded (see tc_common.cuh).
 #include <atomic>
 #include <mutex>
 
