@@ -79,6 +79,19 @@ def integers(key: int, n: int, lo: int, hi: int) -> np.ndarray:
     return (lo + (r % span).astype(np.int64)).astype(np.float32)
 
 
+def log_uniform(key: int, n: int, lo_exp: float, hi_exp: float) -> np.ndarray:
+    """n fp32 values +-10^e, e uniform in [lo_exp, hi_exp), the sign from the
+    stream's lowest bit (a wide dynamic range)."""
+    out = np.empty(n, dtype=np.float32)
+    for s in range(0, n, _CHUNK):
+        c = min(_CHUNK, n - s)
+        r = raw_u64(key, s, c)
+        u = (r >> np.uint64(40)).astype(np.float64) * (1.0 / (1 << 24))
+        sign = np.where((r & np.uint64(1)) == 0, 1.0, -1.0)
+        out[s:s + c] = (sign * 10.0 ** (lo_exp + (hi_exp - lo_exp) * u)).astype(np.float32)
+    return out
+
+
 def sample_rows(key: int, total: int, count: int) -> np.ndarray:
     """``count`` distinct sorted indices in [0, total), chosen by the stream."""
     if count >= total:
@@ -99,6 +112,8 @@ def _draw(spec, key, n):
         return normal(key, n, spec[1], spec[2])
     if kind == "I":
         return integers(key, n, spec[1], spec[2])
+    if kind == "L":
+        return log_uniform(key, n, spec[1], spec[2])
     raise ValueError(kind)
 
 

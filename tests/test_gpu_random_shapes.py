@@ -217,3 +217,45 @@ def test_random_linear_unaligned(idx):
                              out=out)
         assert np.array_equal(got.cpu().numpy().astype(np.float64), ref), \
             f"unaligned linear {M}x({K}->{N}) {mode} ({binding.last_kernel_name()})"
+
+
+# Wide dynamic range: every operand +-10^e with e uniform in [-15, 15).  The
+# bound as the other tests write it, 1e-5 * S with S = sum_k |a*b|, leaves out
+# beta*self (the conv's bias): where that term is many orders larger than the
+# products, rounding the result to fp32 alone exceeds 1e-5 * S, for SIMT FFMA
+# as for any fp32 arithmetic.  These cases therefore measure the error
+# against S' = |alpha| * S + |beta * self| (conv: S + |bias|), the magnitudes
+# of every term of the expression (reading R18).
+WIDE = ("L", -15.0, 15.0)
+
+
+@pytest.mark.parametrize("idx", range(8))
+def test_wide_dynamic_range_addmm(idx):
+    rng = np.random.RandomState(300 + idx)
+    M, N, K = int(rng.randint(1, 900)), int(rng.randint(1, 1500)), int(rng.randint(1, 900))
+    s2 = bool(idx % 2)
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=s2, workload=1600 + idx, mat1=WIDE, mat2=WIDE,
+                                 self_=WIDE)
+    ref, S = oracle.addmm(s, a, b)
+    Sx = S + np.abs(np.broadcast_to(s.astype(np.float64), ref.shape))
+    for mode in MODES + ["simt"]:
+        out = binding.addmm(dev(s), dev(a), dev(b), mode=mode)
+        torch.cuda.synchronize()
+        within(out.cpu().numpy(), ref, Sx, TOL[mode],
+               f"wide-range addmm {M}x{N}x{K} {mode} ({binding.last_kernel_name()})")
+
+
+@pytest.mark.parametrize("idx", range(8))
+def test_wide_dynamic_range_conv(idx):
+    rng = np.random.RandomState(400 + idx)
+    IC, H, W = int(rng.randint(1, 40)), int(rng.randint(3, 60)), int(rng.randint(3, 90))
+    OC = int(rng.randint(1, 200))
+    x, w, bias = synth.conv_inputs(1, IC, H, W, OC, 3, 3, workload=1700 + idx, x=WIDE, w=WIDE,
+                                   bias=WIDE)
+    ref, S = oracle.conv2d(x, w, bias, 1, 1, 1)
+    Sx = S + np.abs(bias.astype(np.float64))[None, :, None, None]
+    for mode in MODES + ["simt"]:
+        out = binding.conv2d(dev(x), dev(w), dev(bias), 1, 1, 1, mode=mode)
+        torch.cuda.synchronize()
+        within(out.cpu().numpy(), ref, Sx, TOL[mode],
+               f"wide-range conv {IC}x{H}x{W}->{OC} {mode} ({binding.last_kernel_name()})")
