@@ -4,7 +4,9 @@ of 16 mod 32, K-slices, ragged edges, the conv's slab form with few input
 channels, per-axis stride / padding / dilation).
 
 Shapes come from a fixed numpy generator (the same list on every run), sized so
-that the oracle finishes each case in well under a second.  The tolerance is
+that the oracle finishes each case in about a second at most; a few extreme
+addmm shapes (a handful of rows or columns, K up to 20000 with a small output)
+stand beside the general ones.  The tolerance is
 the one the other parity tests use: 1e-5 * S + 1e-6 per element for 3xTF32 and
 SIMT, 2e-3 * S + 1e-6 for 1xTF32 (S = the sum of |products| of the element).
 """
@@ -51,6 +53,25 @@ def _addmm_shapes(n=60, seed=2024):
     return out
 
 
+def _addmm_extreme_shapes(n=16, seed=4242):
+    """Few rows with long rows, long K with a small output (many K-slices), and
+    one to eight columns."""
+    rng = np.random.RandomState(seed)
+    out = []
+    while len(out) < n:
+        kind = len(out) % 3
+        if kind == 0:
+            M, N, K = int(rng.randint(1, 17)), int(rng.randint(1, 9000)), int(rng.randint(1, 9000))
+        elif kind == 1:
+            M, N, K = int(rng.randint(1, 400)), int(rng.randint(1, 400)), int(rng.randint(2000, 20000))
+        else:
+            M, N, K = int(rng.randint(1, 9000)), int(rng.randint(1, 9)), int(rng.randint(1, 4000))
+        if M * N * K > 3e8:
+            continue
+        out.append((M, N, K, bool(rng.randint(2))))
+    return out
+
+
 def _conv_shapes(n=60, seed=7):
     rng = np.random.RandomState(seed)
     out = []
@@ -94,6 +115,7 @@ def _linear_shapes(n=24, seed=99):
 
 
 ADDMM = _addmm_shapes()
+ADDMM_EXTREME = _addmm_extreme_shapes()
 CONV = _conv_shapes()
 LINEAR = _linear_shapes()
 
@@ -116,6 +138,18 @@ def test_random_addmm(idx):
         within(out.cpu().numpy(), ref, S, TOL[mode],
                f"addmm {M}x{N}x{K} self_2d={s2} beta={beta} alpha={al} {mode} "
                f"({binding.last_kernel_name()})")
+
+
+@pytest.mark.parametrize("idx", range(len(ADDMM_EXTREME)))
+def test_random_addmm_extreme_shapes(idx):
+    M, N, K, s2 = ADDMM_EXTREME[idx]
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=s2, workload=1800 + idx)
+    ref, S = oracle.addmm(s, a, b)
+    for mode in MODES:
+        out = binding.addmm(dev(s), dev(a), dev(b), mode=mode)
+        torch.cuda.synchronize()
+        within(out.cpu().numpy(), ref, S, TOL[mode],
+               f"addmm {M}x{N}x{K} self_2d={s2} {mode} ({binding.last_kernel_name()})")
 
 
 @pytest.mark.parametrize("idx", range(len(CONV)))
