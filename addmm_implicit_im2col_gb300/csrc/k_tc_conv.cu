@@ -746,6 +746,249 @@ __global__ void __launch_bounds__(threads_of(GM), 1)
   }
 }
 
+// ------------------------------------------ transposed slab form (k_tc_conv_t)
+// For few input channels, at most 128 output channels and at most one
+// 256-position tile per CTA, the product is taken the other way round:
+// D[oc, p] = sum_k w[oc, k] * im2col[p, k], 128 channels (M, TMEM lanes) x 256
+// positions (N, TMEM columns) per MMA, both operands in shared memory.  A
+// position tile is ST_ROWS x ST_COLS outputs of one image.
+//   warps 0-7   gather: warp r, lane j -> output position (oh0 + r, ow0 + j),
+//               row n = 32r + j of the B tiles; per k-block the position's 16
+//               im2col values are read from the input slab through the k
+//               offset table, split into TF32 hi / lo and stored as its
+//               64-byte row (K-major, 64-byte swizzle), then fenced for the
+//               tensor core
+//   warp 8      TMA producer of the weight tiles (128 x 16 fp32, rows past OC
+//               read as zero)
+//   warp 9      TMEM owner + MMA issuer: W_lo*B_hi + W_hi*B_lo + W_hi*B_hi per
+//               k-step of 8, or W*B
+//   warps 10-13 epilogue: one tcgen05.ld gives a thread one channel's 32
+//               positions of an output row (+ bias, + ReLU); warp q stages its
+//               32 channels x 32 positions (128-byte swizzle) in the input
+//               slab's space, free once the last k-block is gathered, and
+//               stores them with one 4-D TMA box {32 columns, 1 row, 32
+//               channels, 1 image} clipped at the output's edges
+//   warp 14     the CTA's input slab [IC][srows][sbw]: one 4-D TMA box
+// Stage: W_hi | W_lo | B_hi | B_lo (3xTF32) or W | B.
+constexpr int ST_ROWS = 8, ST_COLS = 32, ST_POS = ST_ROWS * ST_COLS;
+constexpr int ST_W_TILE = BM * BK * 4;      // 8 KB: 128 channels x 16 k
+constexpr int ST_B_TILE = ST_POS * BK * 4;  // 16 KB: 256 positions x 16 k
+constexpr int ST_THREADS = 15 * 32;
+constexpr int kStSlabMaxBytes = 64 * 1024;
+constexpr int kStEpiBytes = 4 * 2 * 4096;  // epilogue: two 4 KB blocks per warp
+
+template <bool THREE>
+__global__ void __launch_bounds__(ST_THREADS, 1)
+    k_tc_conv_t(const __grid_constant__ CUtensorMap tmWh, const __grid_constant__ CUtensorMap tmWl,
+                const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmO,
+                const ConvArgs c, const Sched q) {
+  constexpr int B_OFF = THREE ? 2 * ST_W_TILE : ST_W_TILE;  // B tiles within a stage
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_align1024(smem_raw);
+  // [stages][input slab][k offset table][barriers][slab barrier]
+  float* slab = reinterpret_cast<float*>(smem + q.stages * q.w_bytes);
+  int* koff = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(slab) + q.slab_stride);
+  Ctl* ctl = reinterpret_cast<Ctl*>(reinterpret_cast<uint8_t*>(koff) + q.tab_bytes);
+  uint64_t* sbar = reinterpret_cast<uint64_t*>(ctl + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int taps = c.KH * c.KW;
+  int* wd = &g_watchdog_conv;
+  // this CTA's position tile: image b, output rows oh0.., columns ow0..
+  const int b = (int)blockIdx.x / q.tpi, r = (int)blockIdx.x - b * q.tpi, rt = r / q.tw;
+  const int oh0 = rt * ST_ROWS, ow0 = (r - rt * q.tw) * ST_COLS;
+
+  // k = ic*taps + kh*KW + kw -> ic*srows*sbw + kh*dH*sbw + kw*dW (0 past K)
+  for (int k = threadIdx.x; k < q.kb * BK; k += blockDim.x) {
+    int o = 0;
+    if (k < c.K) {
+      const int ic = k / taps, rr = k - ic * taps, kh = rr / c.KW, kw = rr - kh * c.KW;
+      o = (ic * q.srows + kh * c.dH) * q.sbw + kw * c.dW;
+    }
+    koff[k] = o;
+  }
+  // full: the 8 gather warps + the weight TMA
+  if (threadIdx.x == 0) init_barriers(ctl, q.stages, GATHER_WARPS + 1, 1);
+  if (warp == SLAB_WARP && lane == 0) {  // the input box goes out before the set-up barrier
+    ptx::mbar_init(sbar, 1);
+    ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(sbar, (uint32_t)q.slab_tx);
+    ptx::tma_load_4d(slab, &tmX, sbar, ow0 * c.sW - c.pW - q.soff, oh0 * c.sH - c.pH, 0, b);
+  }
+  if (warp == TMA_WARP && lane == 0) {
+    ptx::tma_prefetch_desc(&tmWh);
+    if (THREE) ptx::tma_prefetch_desc(&tmWl);
+  }
+  if (warp == MMA_WARP) {
+    ptx::tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  volatile int* abort = &ctl->abort;
+
+  if (warp < GATHER_WARPS) {
+    // ------------------------------------------------------ im2col gather
+    const int n = warp * 32 + lane;  // row of the B tiles
+    const int row_off = sw64_row_base(n);
+    if (warp_wait_bar(sbar, 0, abort, kSiteSlabFull, wd)) {
+      const float* sl = slab + warp * c.sH * q.sbw + lane * c.sW + q.soff;
+      int kk = 0;  // first k of the next k-block to gather
+      auto gather = [&](float (&v)[BK]) {
+        int o[BK];
+#pragma unroll
+        for (int j = 0; j < BK; j += 4) {
+          const int4 t = *reinterpret_cast<const int4*>(koff + kk + j);
+          o[j] = t.x;
+          o[j + 1] = t.y;
+          o[j + 2] = t.z;
+          o[j + 3] = t.w;
+        }
+#pragma unroll
+        for (int j = 0; j < BK; ++j) {
+          const float xv = sl[o[j]];
+          v[j] = kk + j < c.K ? xv : 0.0f;
+        }
+        kk += BK;
+      };
+      int s = 0;
+      uint32_t ph = 0;
+      auto store = [&](const float (&v)[BK]) -> bool {
+        if (!warp_wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) return false;
+        uint8_t* row = smem + s * q.w_bytes + B_OFF + row_off;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float4 x4 = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+          if (THREE) {
+            *reinterpret_cast<float4*>(row + sw64_unit(n, u)) = tf32_hi4(x4);
+            *reinterpret_cast<float4*>(row + ST_B_TILE + sw64_unit(n, u)) = tf32_lo4(x4);
+          } else {
+            *reinterpret_cast<float4*>(row + sw64_unit(n, u)) = x4;  // read as TF32
+          }
+        }
+        ptx::fence_proxy_async_smem();  // the tensor core reads what was just stored
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ctl->full[s]);
+        if (++s == q.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
+        return true;
+      };
+      rotate2(q.kb, gather, store);
+    }
+  } else if (warp == TMA_WARP) {
+    // ------------------------------------------------ weight TMA producer
+    if (lane == 0) {
+      ptx::griddep_wait();  // the weight planes come from the pre-pass
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      for (int kb = 0; kb < q.kb && !*abort; ++kb) {
+        if (!wait_bar(&ctl->empty[s], ph ^ 1u, abort, kSiteProducerEmpty, wd)) break;
+        uint8_t* st = smem + s * q.w_bytes;
+        ptx::mbar_arrive_expect_tx(&ctl->full[s], (uint32_t)(THREE ? 2 * ST_W_TILE : ST_W_TILE));
+        ptx::tma_load_2d(st, &tmWh, &ctl->full[s], kb * BK, 0);
+        if (THREE) ptx::tma_load_2d(st + ST_W_TILE, &tmWl, &ctl->full[s], kb * BK, 0);
+        ++issued;
+        if (++s == q.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      for (int j = (issued > q.stages ? issued - q.stages : 0); j < issued; ++j)
+        drain_wait(&ctl->full[j % q.stages], (uint32_t)((j / q.stages) & 1));
+    }
+  } else if (warp == MMA_WARP) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_tf32(BM, ST_POS, false, false);
+      // descriptors as running values: stage s at k-step 0 = d0 + s * (w_bytes
+      // >> 4); the W_lo / B tiles at fixed offsets; k-step 1 adds 32 bytes (2)
+      const uint64_t d0 = sw64_desc(ptx::smem_addr(smem), 0);
+      const uint64_t step = (uint64_t)(q.w_bytes >> 4);
+      constexpr uint64_t kWlo = ST_W_TILE >> 4, kB = B_OFF >> 4,
+                         kBlo = (B_OFF + ST_B_TILE) >> 4, kK1 = 2;
+      uint64_t ds = d0;
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int kb = 0; kb < q.kb; ++kb) {
+        if (!wait_bar(&ctl->full[s], ph, abort, kSiteMmaOperands, wd)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t acc = kb > 0 ? 1u : 0u;
+        if (THREE) {
+          ptx::mma_tf32(tmem, ds + kWlo, ds + kB, idesc, acc);        // W_lo * B_hi
+          ptx::mma_tf32(tmem, ds, ds + kBlo, idesc, 1u);              // W_hi * B_lo
+          ptx::mma_tf32(tmem, ds, ds + kB, idesc, 1u);                // W_hi * B_hi
+          ptx::mma_tf32(tmem, ds + kWlo + kK1, ds + kB + kK1, idesc, 1u);
+          ptx::mma_tf32(tmem, ds + kK1, ds + kBlo + kK1, idesc, 1u);
+          ptx::mma_tf32(tmem, ds + kK1, ds + kB + kK1, idesc, 1u);
+        } else {
+          ptx::mma_tf32(tmem, ds, ds + kB, idesc, acc);
+          ptx::mma_tf32(tmem, ds + kK1, ds + kB + kK1, idesc, 1u);
+        }
+        ptx::mma_commit(&ctl->empty[s]);
+        const bool wrap = ++s == q.stages;
+        s = wrap ? 0 : s;
+        ph ^= wrap ? 1u : 0u;
+        ds = wrap ? d0 : ds + step;
+      }
+      if (ok) ptx::mma_commit(&ctl->accf[0]);
+      ptx::mma_commit(&ctl->drain);
+      drain_wait(&ctl->drain, 0);
+    }
+    __syncwarp();
+  } else if (warp == SLAB_WARP) {
+    if (lane == 0) drain_wait(sbar, 0);  // the box has landed before the CTA ends
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int quarter = warp & 3, oc = quarter * 32 + lane;
+    const float bias = (c.bias && oc < c.OC) ? __ldg(c.bias + oc) : 0.0f;
+    if (warp_wait_bar(&ctl->accf[0], 0, abort, kSiteEpilogueAccFull, wd)) {
+      // every k-block has been gathered and consumed: the slab's space is free
+      ptx::tc_fence_after();
+      const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+      uint8_t* stage = reinterpret_cast<uint8_t*>(slab) + quarter * 8192;  // two 4 KB blocks
+#pragma unroll 1
+      for (int rr = 0; rr < ST_ROWS; ++rr) {
+        uint32_t v[32];
+        __syncwarp();  // converged for the warp-wide TMEM load
+        ptx::tmem_ld32(trow + (uint32_t)(rr * ST_COLS), v);
+        ptx::tmem_ld_wait();
+        uint8_t* blk = stage + (rr & 1) * 4096;
+        if (lane == 0) ptx::bulk_wait_read1();  // the store from this block two rows ago
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          float4 o = make_float4(__uint_as_float(v[4 * u]) + bias, __uint_as_float(v[4 * u + 1]) + bias,
+                                 __uint_as_float(v[4 * u + 2]) + bias, __uint_as_float(v[4 * u + 3]) + bias);
+          if (c.relu)
+            o = make_float4(fmaxf(o.x, 0.f), fmaxf(o.y, 0.f), fmaxf(o.z, 0.f), fmaxf(o.w, 0.f));
+          *reinterpret_cast<float4*>(blk + lane * 128 + ((u ^ (lane & 7)) << 4)) = o;
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_4d(&tmO, blk, ow0, oh0 + rr, quarter * 32, b);
+          ptx::bulk_commit();
+        }
+      }
+      if (lane == 0) ptx::bulk_wait_all();  // every store has landed before the CTA ends
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 // Adds the K-slice partial tiles of the sliced tiles in slice order, then bias
 // (and ReLU), and writes NCHW.  Thread = (tile, channel, 4 positions); the
 // slice loads are unrolled (at most 16) so that they are all in flight.
@@ -1020,7 +1263,95 @@ bool encode_x_slab(CUtensorMap* m, const ConvArgs& c, const Sched& q) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Transposed slab form (k_tc_conv_t): few input channels (the pages' K
+// order), OC <= 128, one image's output in tiles of ST_ROWS x ST_COLS with at
+// most one tile per SM over the whole batch, W % 4 == 0 and a 16-byte aligned
+// x (the input box), OW % 4 == 0 and an aligned out (16-byte stores), K at
+// most kSlabMaxK (the k offset table), at least 3/4 of the tiles' positions
+// real outputs, and at least two stages beside the slab.
+bool st_geometry(const ConvArgs& c, bool three, Sched& q, int& smem) {
+  if (ic_fastest(c) || c.OC > BM || c.W % 4 != 0 || c.OW % 4 != 0 || !c.vec_out ||
+      reinterpret_cast<uintptr_t>(c.x) % 16 != 0)
+    return false;
+  const int64_t kb = (c.K + BK - 1) / BK;
+  if (kb * BK > kSlabMaxK) return false;
+  const int64_t off = (4 - c.pW % 4) % 4;
+  const int64_t bw =
+      (off + (ST_COLS - 1) * (int64_t)c.sW + (int64_t)(c.KW - 1) * c.dW + 1 + 3) / 4 * 4;
+  const int64_t rows = (ST_ROWS - 1) * (int64_t)c.sH + (int64_t)(c.KH - 1) * c.dH + 1;
+  if (bw > 256 || rows > 256 || c.IC > 256) return false;
+  const int64_t bytes = (int64_t)c.IC * rows * bw * 4;
+  if (bytes > kStSlabMaxBytes) return false;
+  const int64_t tw = (c.OW + ST_COLS - 1) / ST_COLS, th = (c.OH + ST_ROWS - 1) / ST_ROWS;
+  const int64_t slab_space = std::max<int64_t>((bytes + 1023) / 1024 * 1024, kStEpiBytes);
+  if ((int64_t)c.B * tw * th > kPlanSMs) return false;
+  if (4 * (int64_t)c.OW * c.OH < 3 * tw * ST_COLS * th * ST_ROWS) return false;
+  Sched t{};
+  t.kb = (int)kb;
+  t.slab = 1;
+  t.tw = (int)tw;
+  t.tpi = (int)(tw * th);
+  t.units = (int)(c.B * tw * th);
+  t.sbw = (int)bw;
+  t.srows = (int)rows;
+  t.soff = (int)off;
+  t.slab_tx = (int)bytes;
+  t.slab_stride = (int)slab_space;  // the slab, then the epilogue's staging blocks
+  t.tab_bytes = (int)((kb * BK * 4 + 1023) / 1024 * 1024);
+  t.w_bytes = (three ? 2 : 1) * (ST_W_TILE + ST_B_TILE);
+  const int fixed = 1024 + t.slab_stride + t.tab_bytes + (int)sizeof(Ctl) + (int)sizeof(uint64_t);
+  const int st = (SMEM_LIMIT - fixed) / t.w_bytes;
+  t.stages = st < MAX_STAGES ? st : MAX_STAGES;
+  if (t.stages < 2) return false;
+  t.bn = BM;
+  t.n_oc = 1;
+  t.nacc = 1;
+  q = t;
+  smem = fixed + t.stages * t.w_bytes;
+  return true;
+}
+
 constexpr int kMaxDev = 64;
+
+// Transposed slab form: out viewed as [B][OC][OH][OW] -> tensor map, box {32
+// columns, 1 row, 32 channels, 1 image}, 128-byte swizzle (a staged block is
+// 32 channel rows of 128 bytes); the parts past OW, OH or OC are not written.
+bool encode_out_t(CUtensorMap* m, const ConvArgs& c) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t OW = (cuuint64_t)c.OW, OH = (cuuint64_t)c.OH, OC = (cuuint64_t)c.OC;
+  const cuuint64_t dims[4] = {OW, OH, OC, (cuuint64_t)c.B};
+  const cuuint64_t strides[3] = {OW * 4, OH * OW * 4, OC * OH * OW * 4};
+  const cuuint32_t box[4] = {(cuuint32_t)ST_COLS, 1, 32, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, c.out, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool THREE>
+cudaError_t run_t(const ConvArgs& c, const Sched& q, int smem, const float* w_hi,
+                  const float* w_lo, int64_t Kp, cudaStream_t s) {
+  CUtensorMap th, tl, tx, to;
+  if (!encode_w(&th, w_hi, (uint64_t)Kp, (uint64_t)c.OC, BM) ||
+      !encode_w(&tl, THREE ? w_lo : w_hi, (uint64_t)Kp, (uint64_t)c.OC, BM) ||
+      !encode_x_slab(&tx, c, q) || !encode_out_t(&to, c))
+    return cudaErrorInvalidValue;
+  static std::atomic<bool> ready[kMaxDev];  // per device: the attribute is set (calls may race)
+  auto k = k_tc_conv_t<THREE>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= kMaxDev || !ready[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+    if (e != cudaSuccess) return e;
+    if (dev < kMaxDev) ready[dev].store(true, std::memory_order_release);
+  }
+  e = launch_after_previous(k, dim3(q.units), dim3(ST_THREADS), (size_t)smem, s, th, tl, tx, to, c, q);
+  note_launch();
+  note_kernel_name(THREE ? "k_tc_conv<3xtf32,slab_t>" : "k_tc_conv<1xtf32,slab_t>");
+  return e;
+}
 
 template <bool THREE, int GM>
 cudaError_t launch_main(const ConvArgs& c, const Plan& pl, const CUtensorMap& th,
@@ -1117,6 +1448,11 @@ cudaError_t launch_tc_conv(const ConvArgs& c, bool three_pass, void* workspace,
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  Sched qt;
+  int smem_t = 0;
+  if (st_geometry(c, three_pass, qt, smem_t))
+    return three_pass ? run_t<true>(c, qt, smem_t, w_hi, w_lo, Kp, s)
+                      : run_t<false>(c, qt, smem_t, w_hi, nullptr, Kp, s);
   return three_pass ? run<true>(c, pl, w_hi, w_lo, Kp, part, s)
                     : run<false>(c, pl, w_hi, nullptr, Kp, part, s);
 }

@@ -187,7 +187,10 @@ int gemm_addmm_f32_ws(const float* self, int self_2d, const float* mat1, const f
  * no alignment rule on x or w; tiny problems take the SIMT kernel.  With
  * fewer than 8 input channels, W and OW multiples of 4 and x, out 16-byte
  * aligned, it reads each tile's input window from shared memory, brought in
- * by one TMA box per tile ("k_tc_conv<3xtf32,slab>").
+ * by one TMA box per tile ("k_tc_conv<3xtf32,slab>"); when moreover OC <= 128
+ * and the output fits one tile of 8 rows x 32 columns per SM, the product is
+ * taken with the channels as the MMA's M and 256 positions as its N
+ * ("k_tc_conv<3xtf32,slab_t>").
  */
 int conv2d_gemm_f32(const float* x, const float* w, const float* bias, float* out, int64_t B,
                     int64_t IC, int64_t H, int64_t W, int64_t OC, int64_t KH, int64_t KW,
@@ -341,7 +344,8 @@ int imc_last_kernel(void);
 
 /* Name of the main kernel the calling host thread's last successful call
  * launched, with its form, e.g. "k_tc_gemm<3xtf32,a_tmem>",
- * "k_tc_conv<3xtf32>", "k_tc_conv<1xtf32,slab>", "k_simt_small"; "none"
+ * "k_tc_conv<3xtf32>", "k_tc_conv<1xtf32,slab>", "k_tc_conv<3xtf32,slab_t>",
+ * "k_simt_small"; "none"
  * when nothing ran.  A static string, never NULL. */
 const char* imc_last_kernel_name(void);
 

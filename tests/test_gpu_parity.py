@@ -544,6 +544,12 @@ SLAB_CONV = [  # B, IC, H, W, OC, KH, KW, stride, pad, dil, channels checked (No
 ]
 
 
+def _slab_form(name):
+    """Either slab form: 128-position tiles (",slab>") or the transposed form
+    with 256-position tiles and the channels as M (",slab_t>")."""
+    return name.endswith(",slab>") or name.endswith(",slab_t>")
+
+
 @pytest.mark.parametrize("mode", ["force_tc3", "force_tc1", "default"])
 @pytest.mark.parametrize("idx", range(len(SLAB_CONV)))
 def test_conv_slab_form(mode, idx):
@@ -553,7 +559,7 @@ def test_conv_slab_form(mode, idx):
     if mode in EXPECT:
         assert kern == EXPECT[mode]
     if kern != "simt":  # the default mode may take SIMT for the smallest shapes
-        assert ",slab>" in binding.last_kernel_name(), binding.last_kernel_name()
+        assert _slab_form(binding.last_kernel_name()), binding.last_kernel_name()
     within(got, ref, S, TOL[mode], f"{mode} slab conv #{idx}")
 
 
@@ -563,7 +569,7 @@ def test_conv_slab_integer_bit_exact(mode, idx):
     t = SLAB_CONV[idx]
     x, w, b, s, p, d = _conv_case(t[:10], 540 + idx, spec=("I", -3, 3))
     got, ref, _, _ = run_conv(x, w, b, s, p, d, mode, channels=t[10])
-    assert ",slab>" in binding.last_kernel_name()
+    assert _slab_form(binding.last_kernel_name()), binding.last_kernel_name()
     assert np.array_equal(got.astype(np.float64), ref)
 
 
@@ -573,7 +579,7 @@ def test_conv_slab_relu_no_bias(mode):
     x, w, _, s, p, d = _conv_case(t[:10], 560)
     out = binding.conv2d(dev(x), dev(w), None, s, p, d, mode=mode, relu=True)
     torch.cuda.synchronize()
-    assert ",slab>" in binding.last_kernel_name()
+    assert _slab_form(binding.last_kernel_name()), binding.last_kernel_name()
     ref, S = oracle.conv2d(x, w, None, s, p, d)
     within(out.cpu().numpy(), np.maximum(ref, 0.0), S, TOL[mode], f"slab relu {mode}")
 
@@ -587,9 +593,77 @@ def test_conv_slab_reads_only_the_taps():
     x[:, :, :, 2::4] = np.nan
     x[:, :, :, 3::4] = np.inf
     got, ref, S, _ = run_conv(x, w, b, 4, 0, 1, "force_tc3")
-    assert ",slab>" in binding.last_kernel_name()
+    assert _slab_form(binding.last_kernel_name()), binding.last_kernel_name()
     assert np.isfinite(ref).all()
     within(got, ref, S, 1e-5, "slab conv, NaN outside the taps")
+
+
+# The transposed slab form (OC <= 128, one 256-position tile of 8 output rows x
+# 32 columns per SM at most): channels are the MMA's M, positions its N.
+SLAB_T_CONV = [  # B, IC, H, W, OC, KH, KW, stride, pad, dil, channels checked (None: all)
+    # the stem: 3 -> 128 channels, 768x768, 7x7 stride 4 (144 tiles)
+    (1, 3, 768, 768, 128, 7, 7, 4, 3, 1, np.arange(0, 128, 9)),
+    # ragged: OH 50 (7 row tiles, the last 2 rows used), OW 108 (4 column tiles), OC 40
+    (1, 3, 100, 216, 40, 5, 5, 2, 2, 1, None),
+    # 3x3 stride 1, two images, OC 128
+    (2, 3, 64, 64, 128, 3, 3, 1, 1, 1, None),
+    # K = 9: a single k-block
+    (1, 1, 64, 96, 64, 3, 3, 1, 1, 1, None),
+    # per-axis stride / pad / dilation
+    (1, 5, 40, 64, 24, 3, 5, (1, 2), (1, 2), (2, 1), None),
+    # K = 343: 22 k-blocks through 3 or 7 stages
+    (1, 7, 48, 128, 64, 7, 7, 1, 3, 1, None),
+]
+
+# Slab-form shapes past the transposed form's reach: more tiles than SMs, or OC > 128.
+SLAB_WIDE_CONV = [
+    (4, 3, 256, 256, 64, 7, 7, 2, 3, 1, np.arange(0, 64, 5)),  # 256 tiles of 256 positions
+    (1, 3, 64, 128, 160, 5, 5, 2, 2, 1, None),                  # OC 160
+]
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1", "default"])
+@pytest.mark.parametrize("idx", range(len(SLAB_T_CONV)))
+def test_conv_slab_transposed_form(mode, idx):
+    t = SLAB_T_CONV[idx]
+    x, w, b, s, p, d = _conv_case(t[:10], 570 + idx)
+    got, ref, S, kern = run_conv(x, w, b, s, p, d, mode, channels=t[10])
+    if mode in EXPECT:
+        assert kern == EXPECT[mode]
+    if kern != "simt":
+        assert binding.last_kernel_name().endswith(",slab_t>"), binding.last_kernel_name()
+    within(got, ref, S, TOL[mode], f"{mode} transposed slab conv #{idx}")
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1"])
+@pytest.mark.parametrize("idx", range(len(SLAB_WIDE_CONV)))
+def test_conv_slab_form_past_the_transposed_reach(mode, idx):
+    t = SLAB_WIDE_CONV[idx]
+    x, w, b, s, p, d = _conv_case(t[:10], 580 + idx)
+    got, ref, S, _ = run_conv(x, w, b, s, p, d, mode, channels=t[10])
+    assert binding.last_kernel_name().endswith(",slab>"), binding.last_kernel_name()
+    within(got, ref, S, TOL[mode], f"{mode} slab conv (wide) #{idx}")
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1"])
+@pytest.mark.parametrize("idx", [1, 3, 4, 5])
+def test_conv_slab_transposed_integer_bit_exact(mode, idx):
+    t = SLAB_T_CONV[idx]
+    x, w, b, s, p, d = _conv_case(t[:10], 590 + idx, spec=("I", -3, 3))
+    got, ref, _, _ = run_conv(x, w, b, s, p, d, mode, channels=t[10])
+    assert binding.last_kernel_name().endswith(",slab_t>")
+    assert np.array_equal(got.astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("mode", ["force_tc3", "force_tc1"])
+def test_conv_slab_transposed_relu_no_bias(mode):
+    t = SLAB_T_CONV[1]
+    x, w, _, s, p, d = _conv_case(t[:10], 596)
+    out = binding.conv2d(dev(x), dev(w), None, s, p, d, mode=mode, relu=True)
+    torch.cuda.synchronize()
+    assert binding.last_kernel_name().endswith(",slab_t>")
+    ref, S = oracle.conv2d(x, w, None, s, p, d)
+    within(out.cpu().numpy(), np.maximum(ref, 0.0), S, TOL[mode], f"transposed slab relu {mode}")
 
 
 def test_conv_slab_shape_with_unaligned_input_takes_the_global_gather():
