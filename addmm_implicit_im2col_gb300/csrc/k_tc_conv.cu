@@ -49,6 +49,9 @@
 // TMEM columns 0-255 hold the accumulator (two of 128 when BN <= 128, so the
 // epilogue of one tile overlaps the next), columns 256-511 the A stages (32
 // columns each: hi 0-15, lo 16-31).
+// A second kernel, k_tc_conv_t (the transposed slab form, further down), takes
+// the stem-like convs (IC < 8, OC <= 128, one 256-position tile per SM) the
+// other way round: channels as the MMA's M, positions as N.
 // Scheduling: persistent CTAs take whole tiles first.  When the last wave
 // would leave SMs idle, its tiles are cut into S K-slices; a slice writes its
 // partial sums to scratch and k_conv_tail adds the S partial tiles in slice
