@@ -738,6 +738,39 @@ def test_calls_captured_in_a_cuda_graph():
         within(y.cpu().numpy(), ref, Sc, 1e-5, f"graph replay {rep} conv")
 
 
+def test_stem_like_conv_captured_in_a_cuda_graph():
+    # the transposed slab form (input window by TMA, output by TMA boxes) replayed
+    # from a graph on new inputs, beside a slab-form conv past its reach
+    shapes = [(1, 3, 64, 128, 64, 7, 7, 2, 3, 1), (2, 3, 64, 128, 160, 5, 5, 2, 2, 1)]
+    bufs, outs = [], []
+    for i, (B_, IC, H, W, OC, KH, KW, st, pd, dl) in enumerate(shapes):
+        x0, w0, b0 = synth.conv_inputs(B_, IC, H, W, OC, KH, KW, workload=600 + i)
+        bufs.append((dev(x0), dev(w0), dev(b0)))
+        binding.conv2d(*bufs[-1], st, pd, dl)  # attributes set outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for (X, W, Bias), t in zip(bufs, shapes):
+            outs.append(binding.conv2d(X, W, Bias, t[7], t[8], t[9]))
+    for rep in range(2):
+        new = []
+        for i, ((X, W, Bias), t) in enumerate(zip(bufs, shapes)):
+            x, w, b = synth.conv_inputs(*t[:7], workload=610 + 2 * i + rep)
+            for dst, v in ((X, x), (W, w), (Bias, b)):
+                dst.copy_(torch.from_numpy(v))
+            new.append((x, w, b))
+        graph.replay()
+        torch.cuda.synchronize()
+        for (x, w, b), t, y in zip(new, shapes, outs):
+            ref, S = oracle.conv2d(x, w, b, t[7], t[8], t[9])
+            within(y.cpu().numpy(), ref, S, 1e-5, f"graph replay {rep} conv {t}")
+    # the two shapes take the two slab forms
+    binding.conv2d(*bufs[0], 2, 3, 1)
+    assert binding.last_kernel_name().endswith(",slab_t>"), binding.last_kernel_name()
+    binding.conv2d(*bufs[1], 2, 2, 1)
+    assert binding.last_kernel_name().endswith(",slab>"), binding.last_kernel_name()
+
+
 def test_a_wait_that_runs_out_is_reported_and_the_context_stays_usable():
     # failure path of the bounded barrier waits, without a fault: a kernel
     # waits on a barrier nothing completes, gives up after 20 ms, and the host
