@@ -750,8 +750,9 @@ __global__ void __launch_bounds__(threads_of(GM), 1)
 }
 
 // ------------------------------------------ transposed slab form (k_tc_conv_t)
-// For few input channels, at most 128 output channels and at most one
-// 256-position tile per CTA, the product is taken the other way round:
+// For few input channels, at most 128 output channels and one 256-position
+// tile per CTA over 3/4 of the SMs or more, the product is taken the other
+// way round:
 // D[oc, p] = sum_k w[oc, k] * im2col[p, k], 128 channels (M, TMEM lanes) x 256
 // positions (N, TMEM columns) per MMA, both operands in shared memory.  A
 // position tile is ST_ROWS x ST_COLS outputs of one image.
@@ -1267,8 +1268,8 @@ bool encode_x_slab(CUtensorMap* m, const ConvArgs& c, const Sched& q) {
 }
 
 // Transposed slab form (k_tc_conv_t): few input channels (the pages' K
-// order), OC <= 128, one image's output in tiles of ST_ROWS x ST_COLS with at
-// most one tile per SM over the whole batch, W % 4 == 0 and a 16-byte aligned
+// order), OC <= 128, the output in tiles of ST_ROWS x ST_COLS, between 3/4 of
+// a tile and one tile per SM over the whole batch, W % 4 == 0 and a 16-byte aligned
 // x (the input box), OW % 4 == 0 and an aligned out (16-byte stores), K at
 // most kSlabMaxK (the k offset table), at least 3/4 of the tiles' positions
 // real outputs, and at least two stages beside the slab.
@@ -1287,7 +1288,11 @@ bool st_geometry(const ConvArgs& c, bool three, Sched& q, int& smem) {
   if (bytes > kStSlabMaxBytes) return false;
   const int64_t tw = (c.OW + ST_COLS - 1) / ST_COLS, th = (c.OH + ST_ROWS - 1) / ST_ROWS;
   const int64_t slab_space = std::max<int64_t>((bytes + 1023) / 1024 * 1024, kStEpiBytes);
-  if ((int64_t)c.B * tw * th > kPlanSMs) return false;
+  // one tile per SM, and enough tiles to fill 3/4 of them: with fewer, the
+  // 128-position form cuts K across the idle SMs and measured faster (64
+  // tiles of K = 147: 12.5 against 14.5 us; 24 tiles of K = 343: 16.5 against
+  // 20.6 us)
+  if ((int64_t)c.B * tw * th > kPlanSMs || 4 * (int64_t)c.B * tw * th < 3 * kPlanSMs) return false;
   if (4 * (int64_t)c.OW * c.OH < 3 * tw * ST_COLS * th * ST_ROWS) return false;
   Sched t{};
   t.kb = (int)kb;

@@ -188,7 +188,8 @@ int gemm_addmm_f32_ws(const float* self, int self_2d, const float* mat1, const f
  * fewer than 8 input channels, W and OW multiples of 4 and x, out 16-byte
  * aligned, it reads each tile's input window from shared memory, brought in
  * by one TMA box per tile ("k_tc_conv<3xtf32,slab>"); when moreover OC <= 128
- * and the output fits one tile of 8 rows x 32 columns per SM, the product is
+ * and the output's tiles of 8 rows x 32 columns fill between 3/4 of the SMs
+ * and all of them (one tile each), the product is
  * taken with the channels as the MMA's M and 256 positions as its N
  * ("k_tc_conv<3xtf32,slab_t>").
  */

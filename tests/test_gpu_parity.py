@@ -603,21 +603,23 @@ def test_conv_slab_reads_only_the_taps():
 SLAB_T_CONV = [  # B, IC, H, W, OC, KH, KW, stride, pad, dil, channels checked (None: all)
     # the stem: 3 -> 128 channels, 768x768, 7x7 stride 4 (144 tiles)
     (1, 3, 768, 768, 128, 7, 7, 4, 3, 1, np.arange(0, 128, 9)),
-    # ragged: OH 50 (7 row tiles, the last 2 rows used), OW 108 (4 column tiles), OC 40
-    (1, 3, 100, 216, 40, 5, 5, 2, 2, 1, None),
-    # 3x3 stride 1, two images, OC 128
-    (2, 3, 64, 64, 128, 3, 3, 1, 1, 1, None),
-    # K = 9: a single k-block
-    (1, 1, 64, 96, 64, 3, 3, 1, 1, 1, None),
-    # per-axis stride / pad / dilation
-    (1, 5, 40, 64, 24, 3, 5, (1, 2), (1, 2), (2, 1), None),
-    # K = 343: 22 k-blocks through 3 or 7 stages
-    (1, 7, 48, 128, 64, 7, 7, 1, 3, 1, None),
+    # ragged: OH 50 (7 row tiles, the last 2 rows used), OW 108 (4 column tiles), OC 40; 140 tiles
+    (5, 3, 100, 216, 40, 5, 5, 2, 2, 1, None),
+    # 3x3 stride 1, OC 128, 128 tiles
+    (8, 3, 64, 64, 128, 3, 3, 1, 1, 1, np.arange(0, 128, 3)),
+    # K = 9: a single k-block; 144 tiles
+    (6, 1, 64, 96, 64, 3, 3, 1, 1, 1, None),
+    # per-axis stride / pad / dilation, OH 38, OW 32; 120 tiles
+    (24, 5, 40, 64, 24, 3, 5, (1, 2), (1, 2), (2, 1), None),
+    # K = 343: 22 k-blocks through 3 or 7 stages; 120 tiles
+    (5, 7, 48, 128, 64, 7, 7, 1, 3, 1, np.arange(0, 64, 5)),
 ]
 
-# Slab-form shapes past the transposed form's reach: more tiles than SMs, or OC > 128.
+# Slab-form shapes past the transposed form's reach: more tiles than SMs, fewer
+# than 3/4 of them, or OC > 128.
 SLAB_WIDE_CONV = [
     (4, 3, 256, 256, 64, 7, 7, 2, 3, 1, np.arange(0, 64, 5)),  # 256 tiles of 256 positions
+    (1, 3, 256, 256, 64, 7, 7, 2, 3, 1, None),                  # 64 tiles
     (1, 3, 64, 128, 160, 5, 5, 2, 2, 1, None),                  # OC 160
 ]
 
@@ -741,7 +743,7 @@ def test_calls_captured_in_a_cuda_graph():
 def test_stem_like_conv_captured_in_a_cuda_graph():
     # the transposed slab form (input window by TMA, output by TMA boxes) replayed
     # from a graph on new inputs, beside a slab-form conv past its reach
-    shapes = [(1, 3, 64, 128, 64, 7, 7, 2, 3, 1), (2, 3, 64, 128, 160, 5, 5, 2, 2, 1)]
+    shapes = [(3, 3, 320, 512, 32, 7, 7, 4, 3, 1), (2, 3, 64, 128, 160, 5, 5, 2, 2, 1)]
     bufs, outs = [], []
     for i, (B_, IC, H, W, OC, KH, KW, st, pd, dl) in enumerate(shapes):
         x0, w0, b0 = synth.conv_inputs(B_, IC, H, W, OC, KH, KW, workload=600 + i)
@@ -765,7 +767,7 @@ def test_stem_like_conv_captured_in_a_cuda_graph():
             ref, S = oracle.conv2d(x, w, b, t[7], t[8], t[9])
             within(y.cpu().numpy(), ref, S, 1e-5, f"graph replay {rep} conv {t}")
     # the two shapes take the two slab forms
-    binding.conv2d(*bufs[0], 2, 3, 1)
+    binding.conv2d(*bufs[0], 4, 3, 1)
     assert binding.last_kernel_name().endswith(",slab_t>"), binding.last_kernel_name()
     binding.conv2d(*bufs[1], 2, 2, 1)
     assert binding.last_kernel_name().endswith(",slab>"), binding.last_kernel_name()
