@@ -952,13 +952,15 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
     // ----------------------------------------------------------- epilogue
     const int quarter = warp & 3, oc = quarter * 32 + lane;
     const float bias = (c.bias && oc < c.OC) ? __ldg(c.bias + oc) : 0.0f;
-    if (warp_wait_bar(&ctl->accf[0], 0, abort, kSiteEpilogueAccFull, wd)) {
+    // a warp whose 32 channels all lie past OC has nothing to store
+    if (quarter * 32 < c.OC && warp_wait_bar(&ctl->accf[0], 0, abort, kSiteEpilogueAccFull, wd)) {
       // every k-block has been gathered and consumed: the slab's space is free
       ptx::tc_fence_after();
       const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
       uint8_t* stage = reinterpret_cast<uint8_t*>(slab) + quarter * 8192;  // two 4 KB blocks
+      const int rows = c.OH - oh0 < ST_ROWS ? c.OH - oh0 : ST_ROWS;  // output rows of the tile
 #pragma unroll 1
-      for (int rr = 0; rr < ST_ROWS; ++rr) {
+      for (int rr = 0; rr < rows; ++rr) {
         uint32_t v[32];
         __syncwarp();  // converged for the warp-wide TMEM load
         ptx::tmem_ld32(trow + (uint32_t)(rr * ST_COLS), v);
