@@ -1,6 +1,6 @@
 """GPU parity on seeded random shapes: addmm, linear and conv2d in every mode against
 the oracle, to reach planner paths the hand-picked cases may miss (tile widths
-of 16 mod 32, K-slices, ragged edges, the conv's slab form with few input
+of 16 mod 32, K-slices, ragged edges, the conv's two slab forms with few input
 channels, per-axis stride / padding / dilation).
 
 Shapes come from a fixed numpy generator (the same list on every run), sized so
@@ -103,6 +103,42 @@ def _conv_shapes(n=60, seed=7):
     return out
 
 
+def _conv_t_shapes(n=16, seed=31):
+    """Stem-like convs the transposed slab form takes: IC < 8, OC <= 128, W and
+    OW multiples of 4, 114 to 152 tiles of 8 output rows x 32 columns over the
+    batch, at least 3/4 of the tiles' positions real, the input window of a
+    tile at most 64 KB and K at most 2048."""
+    rng = np.random.RandomState(seed)
+    out = []
+    while len(out) < n:
+        IC, OC = int(rng.randint(1, 8)), int(rng.randint(1, 129))
+        KH, KW = int(rng.randint(1, 8)), int(rng.randint(1, 8))
+        s = (int(rng.randint(1, 5)), int(rng.randint(1, 5)))
+        p = (int(rng.randint(0, 4)), int(rng.randint(0, 4)))
+        d = (int(rng.randint(1, 3)), int(rng.randint(1, 3)))
+        OW = 4 * int(rng.randint(6, 64))
+        OH = int(rng.randint(8, 120))
+        w_min = (OW - 1) * s[1] + d[1] * (KW - 1) + 1 - 2 * p[1]
+        W = (max(w_min, 4) + 3) // 4 * 4
+        H = max(1, (OH - 1) * s[0] + d[0] * (KH - 1) + 1 - 2 * p[0])
+        OH = (H + 2 * p[0] - d[0] * (KH - 1) - 1) // s[0] + 1
+        OW = (W + 2 * p[1] - d[1] * (KW - 1) - 1) // s[1] + 1
+        if OH < 1 or OW < 1 or OW % 4:
+            continue
+        tw, th = -(-OW // 32), -(-OH // 8)
+        B = max(1, round(133 / (tw * th)))
+        tiles = B * tw * th
+        off = (4 - p[1] % 4) % 4
+        bw = (off + 31 * s[1] + (KW - 1) * d[1] + 1 + 3) // 4 * 4
+        rows = 7 * s[0] + (KH - 1) * d[0] + 1
+        if not (114 <= tiles <= 152) or 4 * OW * OH < 3 * tw * 32 * th * 8:
+            continue
+        if bw > 256 or rows > 256 or IC * rows * bw * 4 > 65536 or IC * KH * KW > 2048:
+            continue
+        out.append((B, IC, H, W, OC, KH, KW, s, p, d))
+    return out
+
+
 def _linear_shapes(n=24, seed=99):
     rng = np.random.RandomState(seed)
     out = []
@@ -117,6 +153,7 @@ def _linear_shapes(n=24, seed=99):
 ADDMM = _addmm_shapes()
 ADDMM_EXTREME = _addmm_extreme_shapes()
 CONV = _conv_shapes()
+CONV_T = _conv_t_shapes()
 LINEAR = _linear_shapes()
 
 
@@ -233,6 +270,19 @@ def test_random_conv_integer_and_unaligned(idx):
         got = binding.conv2d(_offset(x), _offset(w), _offset(bias), st, pd, dl, mode=mode, out=out)
         assert np.array_equal(got.cpu().numpy().astype(np.float64), ref), \
             f"unaligned conv {CONV[idx]} {mode} ({binding.last_kernel_name()})"
+
+
+@pytest.mark.parametrize("idx", range(len(CONV_T)))
+def test_random_conv_transposed_form(idx):
+    B, IC, H, W, OC, KH, KW, st, pd, dl = CONV_T[idx]
+    x, w, bias = synth.conv_inputs(B, IC, H, W, OC, KH, KW, workload=1600 + idx)
+    channels = np.arange(idx % min(5, OC), OC, 9)  # every 9th channel keeps the oracle quick
+    ref, S = oracle.conv2d(x, w, bias, st, pd, dl, channels=channels)
+    for mode in MODES:
+        got = binding.conv2d(dev(x), dev(w), dev(bias), st, pd, dl, mode=mode).cpu().numpy()
+        if binding.last_kernel() != "simt":  # the default mode takes SIMT for tiny problems
+            assert binding.last_kernel_name().endswith(",slab_t>"), binding.last_kernel_name()
+        within(got[:, channels], ref, S, TOL[mode], f"conv {CONV_T[idx]} {mode}")
 
 
 @pytest.mark.parametrize("idx", range(0, len(LINEAR), 4))
