@@ -137,33 +137,40 @@ __global__ __launch_bounds__(THREADS) void k_simt(const Ops ops) {
   }
 }
 
-// Small problems (few outputs, short K): one thread per output, the k loop
-// unrolled so that its loads are in flight together, no shared-memory staging
-// (whose load / barrier rounds per k-tile are the whole cost at this size).
-// Consecutive threads take consecutive n: mat2 loads are coalesced, mat1
-// loads broadcast.  fp32 FMA in k order.
+// Small problems (few outputs, short K): T = 1, 2, 4 or 8 consecutive threads
+// per output (T = ceil(K / 32) rounded up to a power of two), each summing one
+// contiguous run of at most 32 k in k order with all of its loads in flight
+// together; the T partial sums are then added pairwise by shuffles (xor 1,
+// then 2, then 4: a fixed order).  No shared-memory staging (whose load /
+// barrier rounds per k-tile are the whole cost at this size).
+template <int T>
 __global__ void __launch_bounds__(256) k_simt_small(const GemmArgs a) {
-  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= a.M * a.N) return;
-  const int64_t m = e / a.N, n = e - m * a.N;
-  const float* ar = a.mat1 + m * a.K;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t e = tid / T;
+  const int t = (int)(tid % T);
+  const bool live = e < a.M * a.N;
   float acc = 0.0f;
-  const int K = (int)a.K;  // <= kSmallK
-  int k = 0;
-  for (; k + 32 <= K; k += 32) {  // 64 loads in flight, then 32 FMAs in k order
+  if (live) {
+    const int64_t m = e / a.N, n = e - m * a.N;
+    const int K = (int)a.K;  // <= kSmallK = 32 * 8
+    const int kc = (K + T - 1) / T, k0 = t * kc, k1 = k0 + kc < K ? k0 + kc : K;
+    const float* ar = a.mat1 + m * a.K;
     float av[32], bv[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      av[j] = __ldg(ar + k + j);
-      bv[j] = a.b_kmajor ? __ldg(a.mat2 + n * a.K + k + j) : __ldg(a.mat2 + (int64_t)(k + j) * a.N + n);
+      const int k = k0 + j;
+      av[j] = k < k1 ? __ldg(ar + k) : 0.0f;
+      bv[j] = k < k1 ? (a.b_kmajor ? __ldg(a.mat2 + n * a.K + k) : __ldg(a.mat2 + (int64_t)k * a.N + n))
+                     : 0.0f;
     }
 #pragma unroll
-    for (int j = 0; j < 32; ++j) acc = fmaf(av[j], bv[j], acc);
+    for (int j = 0; j < 32; ++j)
+      if (k0 + j < k1) acc = fmaf(av[j], bv[j], acc);
   }
-  for (; k < K; ++k) {
-    const float b = a.b_kmajor ? __ldg(a.mat2 + n * a.K + k) : __ldg(a.mat2 + (int64_t)k * a.N + n);
-    acc = fmaf(__ldg(ar + k), b, acc);
-  }
+#pragma unroll
+  for (int x = 1; x < T; x <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
+  if (!live || t != 0) return;
+  const int64_t n = e % a.N;
   const float v = a.read_self ? fmaf(a.alpha, acc, a.beta * a.self[a.self_2d ? e : n])
                               : a.alpha * acc;
   a.out[e] = a.relu ? fmaxf(v, 0.f) : v;
@@ -261,7 +268,14 @@ static bool simt_grid(int64_t M, int64_t N, unsigned* blocks) {
 
 cudaError_t launch_simt_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.M * a.N <= kSmallOutputs && a.K <= kSmallK) {
-    k_simt_small<<<(unsigned)((a.M * a.N + 255) / 256), 256, 0, s>>>(a);
+    const int T = a.K <= 32 ? 1 : (a.K <= 64 ? 2 : (a.K <= 128 ? 4 : 8));
+    const unsigned blocks = (unsigned)((a.M * a.N * T + 255) / 256);
+    switch (T) {
+      case 1: k_simt_small<1><<<blocks, 256, 0, s>>>(a); break;
+      case 2: k_simt_small<2><<<blocks, 256, 0, s>>>(a); break;
+      case 4: k_simt_small<4><<<blocks, 256, 0, s>>>(a); break;
+      default: k_simt_small<8><<<blocks, 256, 0, s>>>(a); break;
+    }
     note_launch();
     note_kernel_name("k_simt_small");
     return cudaGetLastError();
