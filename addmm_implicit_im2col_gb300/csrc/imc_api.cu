@@ -67,7 +67,9 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 constexpr int64_t kMaxDim = 0x7fffffffLL;
 // Problems smaller than this many multiply-adds run on the SIMT kernel: the
 // tensor-core kernel's fixed set-up (TMEM allocation, pipeline fill) is
-// larger than the whole job there.
+// larger than the whole job there.  Above it the tensor path measured faster
+// (addmm 256x256x64: 10.2 against 12.3 us; 256x256x256: 13.3 against 41 us
+// for the small SIMT kernel).
 constexpr int64_t kTinyMacs = int64_t(1) << 22;
 
 int finish(cudaError_t e, int kernel) {
