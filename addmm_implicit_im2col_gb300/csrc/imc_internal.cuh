@@ -112,10 +112,14 @@ void note_launch();
 // reports it once the call succeeds); a static string.
 void note_kernel_name(const char* name);
 
-// Launches `kernel` so that it may start while the previous kernel of the
-// stream (issued by the same call) is still running; the kernel calls
-// ptx::griddep_wait() before it reads that kernel's output.  Used only for a
-// call's second and later kernels.
+// Launches `kernel` as the programmatic dependent of the previous kernel of
+// the stream: it may start once that kernel's blocks have all executed
+// griddepcontrol.launch_dependents, while that kernel is still running, and
+// calls ptx::griddep_wait() before any global access that kernel could
+// conflict with.  A call's first kernel (a pre-pass) waits at its first
+// instruction and only then lets its own dependent launch, so that the call's
+// later kernels may read the call's inputs from their start; the kernels the
+// library launches plainly (no pre-pass before them) are not dependents.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_after_previous(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                                   cudaStream_t s, Args... args) {

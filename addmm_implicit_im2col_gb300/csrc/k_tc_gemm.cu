@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(256) k_prep_b(const float* __restrict__ mat2, 
                                                 int64_t N, int64_t ldk, float* __restrict__ bt_hi,
                                                 float* __restrict__ bt_lo) {
   __shared__ float tile[32][33];
+  ptx::griddep_wait();    // the kernel before this one has completed
   ptx::griddep_launch();  // the main kernel may start its prologue
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int64_t tiles_n = (N + 31) / 32, tiles = tiles_n * ((K + 31) / 32);
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(256) k_prep_b4(const float* __restrict__ mat2,
                                                  float* __restrict__ bt_hi,
                                                  float* __restrict__ bt_lo) {
   __shared__ float tile[64][65];
+  ptx::griddep_wait();    // the kernel before this one has completed
   ptx::griddep_launch();  // the main kernel may start its prologue
   const int t = threadIdx.x, r0 = t >> 4, q4 = t & 15;
   const int64_t tiles_n = (N + 63) / 64, tiles = tiles_n * ((K + 63) / 64);
@@ -178,6 +180,7 @@ __global__ void __launch_bounds__(256) k_prep_b4(const float* __restrict__ mat2,
 // launched as its dependent, starts without waiting for pre-pass blocks.
 __global__ void __launch_bounds__(256) k_prep_blo(const float4* __restrict__ w, int64_t total4,
                                                   float4* __restrict__ w_lo) {
+  ptx::griddep_wait();  // the kernel before this one has completed
   ptx::griddep_launch();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total4; i += 4 * stride) {
@@ -200,6 +203,7 @@ __global__ void __launch_bounds__(256) k_prep_blo(const float4* __restrict__ w, 
 __global__ void __launch_bounds__(256) k_pad_rows(const float* __restrict__ src, int64_t rows,
                                                   int64_t K, int64_t ld, float* __restrict__ dst,
                                                   float* __restrict__ dst_lo) {
+  ptx::griddep_wait();  // the kernel before this one has completed
   ptx::griddep_launch();
   const int64_t cols_blocks = (K + 255) / 256;
   for (int64_t b = blockIdx.x; b < rows * cols_blocks; b += gridDim.x) {
@@ -415,7 +419,6 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
   int* wd = &g_watchdog_gemm;
 
   if (threadIdx.x == 0) init_barriers(ctl, L.stages, 1, TS ? 4 : 128);
-  ptx::griddep_launch();  // the split-K sum kernel may launch (it waits for this one)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmBh);
@@ -456,6 +459,11 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
           }
         }
       }
+      // the split-K sum kernel may launch now (it waits for this kernel).  The
+      // next call's first kernel is not released early: launched then, its
+      // blocks land on the SMs this kernel frees first, and a pre-pass spread
+      // over few SMs measured slower than one launched when this kernel ends
+      if (splits > 1) ptx::griddep_launch();
       // Every copy issued must have landed before the CTA's shared memory is released.
       for (int j = (issued > L.stages ? issued - L.stages : 0); j < issued; ++j)
         drain_wait(&ctl->full[j % L.stages], (uint32_t)((j / L.stages) & 1));
@@ -905,9 +913,11 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
   if (pad_a) {  // mat1 rows to 16-byte aligned rows of ld floats
     float* a_copy = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.a_offset);
     const int64_t blocks = g.M * ((g.K + 255) / 256);
-    k_pad_rows<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(g.mat1, g.M, g.K, ld,
-                                                                          a_copy, nullptr);
+    const cudaError_t e = launch_after_previous(k_pad_rows, dim3((unsigned)(blocks < cap ? blocks : cap)),
+                                                dim3(256), 0, s, g.mat1, g.M, g.K, ld, a_copy,
+                                                (float*)nullptr);
     note_launch();
+    if (e != cudaSuccess) return e;
     a = a_copy;
     lda = ld;
     prep = true;
@@ -916,9 +926,11 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
     b_hi = ws;
     b_lo = three_pass ? ws + g.N * ld : nullptr;
     const int64_t blocks = g.N * ((g.K + 255) / 256);
-    k_pad_rows<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(
-        g.mat2, g.N, g.K, ld, ws, three_pass ? ws + g.N * ld : nullptr);
+    const cudaError_t e = launch_after_previous(k_pad_rows, dim3((unsigned)(blocks < cap ? blocks : cap)),
+                                                dim3(256), 0, s, g.mat2, g.N, g.K, ld, ws,
+                                                three_pass ? ws + g.N * ld : (float*)nullptr);
     note_launch();
+    if (e != cudaSuccess) return e;
     prep = true;
   } else if (g.b_kmajor) {  // w[N,K] is B_hi; 3xTF32 adds w_lo in the scratch
     b_hi = g.mat2;
@@ -928,9 +940,11 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
       // K % 4 == 0 and 16-byte aligned rows here: whole float4s
       const int64_t total4 = g.N * g.K / 4, blocks = (total4 + 255) / 256;
       const int64_t cap2 = 2 * (int64_t)device_sm_count();
-      k_prep_blo<<<(unsigned)(blocks < cap2 ? blocks : cap2), 256, 0, s>>>(
+      const cudaError_t e = launch_after_previous(
+          k_prep_blo, dim3((unsigned)(blocks < cap2 ? blocks : cap2)), dim3(256), 0, s,
           reinterpret_cast<const float4*>(g.mat2), total4, reinterpret_cast<float4*>(ws));
       note_launch();
+      if (e != cudaSuccess) return e;
       prep = true;
     }
   } else {  // transpose mat2[K,N] into Bt_hi[N,ld] (+ Bt_lo)
@@ -938,12 +952,16 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
     b_lo = three_pass ? ws + g.N * ld : nullptr;
     if (g.N % 4 == 0 && (reinterpret_cast<uintptr_t>(g.mat2) & 15u) == 0) {
       const int64_t tiles = ((g.N + 63) / 64) * ((g.K + 63) / 64);
-      k_prep_b4<<<(unsigned)(tiles < cap ? tiles : cap), 256, 0, s>>>(
-          g.mat2, g.K, g.N, ld, ws, three_pass ? ws + g.N * ld : nullptr);
+      const cudaError_t e = launch_after_previous(
+          k_prep_b4, dim3((unsigned)(tiles < cap ? tiles : cap)), dim3(256), 0, s, g.mat2, g.K,
+          g.N, ld, ws, three_pass ? ws + g.N * ld : (float*)nullptr);
+      if (e != cudaSuccess) return e;
     } else {
       const int64_t tiles = ((g.N + 31) / 32) * ((g.K + 31) / 32);
-      k_prep_b<<<(unsigned)(tiles < cap ? tiles : cap), dim3(32, 8), 0, s>>>(
-          g.mat2, g.K, g.N, ld, ws, three_pass ? ws + g.N * ld : nullptr);
+      const cudaError_t e = launch_after_previous(
+          k_prep_b, dim3((unsigned)(tiles < cap ? tiles : cap)), dim3(32, 8), 0, s, g.mat2, g.K,
+          g.N, ld, ws, three_pass ? ws + g.N * ld : (float*)nullptr);
+      if (e != cudaSuccess) return e;
     }
     note_launch();
     prep = true;
