@@ -116,10 +116,11 @@ void note_kernel_name(const char* name);
 // the stream: it may start once that kernel's blocks have all executed
 // griddepcontrol.launch_dependents, while that kernel is still running, and
 // calls ptx::griddep_wait() before any global access that kernel could
-// conflict with.  A call's first kernel (a pre-pass) waits at its first
-// instruction and only then lets its own dependent launch, so that the call's
-// later kernels may read the call's inputs from their start; the kernels the
-// library launches plainly (no pre-pass before them) are not dependents.
+// conflict with.  Every compute kernel of the library is launched this way.  A
+// pre-pass waits at its first instruction and only then lets its own dependent
+// (the call's main kernel) launch, so that a main kernel that follows its
+// pre-pass may read the call's inputs from its start; a main kernel that
+// begins a call (no pre-pass) has every global access after its wait.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_after_previous(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                                   cudaStream_t s, Args... args) {

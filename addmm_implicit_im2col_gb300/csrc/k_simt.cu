@@ -10,6 +10,7 @@
 // the "et_vk conv2d ... im2col tiled GEMM" page's Implementation paragraph
 // describes (n -> (b, oh, ow), kk -> (ic, kh, kw), out-of-range taps read 0).
 #include "imc_internal.cuh"
+#include "ptx.cuh"
 
 namespace imc {
 namespace {
@@ -88,6 +89,7 @@ struct ConvOperands {
 
 template <class Ops>
 __global__ __launch_bounds__(THREADS) void k_simt(const Ops ops) {
+  ptx::griddep_wait();  // dependent launch: the kernel before this one has completed
   __shared__ __align__(16) float As[BK][BM];
   __shared__ __align__(16) float Bs[BK][BN];
   const int t = threadIdx.x;
@@ -145,6 +147,7 @@ __global__ __launch_bounds__(THREADS) void k_simt(const Ops ops) {
 // barrier rounds per k-tile are the whole cost at this size).
 template <int T>
 __global__ void __launch_bounds__(256) k_simt_small(const GemmArgs a) {
+  ptx::griddep_wait();  // dependent launch: the kernel before this one has completed
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t e = tid / T;
   const int t = (int)(tid % T);
@@ -177,6 +180,7 @@ __global__ void __launch_bounds__(256) k_simt_small(const GemmArgs a) {
 }
 
 __global__ void k_fill_gemm(const GemmArgs a) {
+  ptx::griddep_wait();  // dependent launch: the kernel before this one has completed
   const int64_t total = a.M * a.N;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
@@ -188,6 +192,7 @@ __global__ void k_fill_gemm(const GemmArgs a) {
 }
 
 __global__ void k_fill_conv(const ConvArgs c) {
+  ptx::griddep_wait();  // dependent launch: the kernel before this one has completed
   const int64_t P = (int64_t)c.OH * c.OW;
   const int64_t total = (int64_t)c.B * c.OC * P;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
@@ -208,6 +213,7 @@ __global__ void k_fill_conv(const ConvArgs c) {
 // stay scalar).
 template <bool VEC4>
 __global__ void __launch_bounds__(256) k_direct_conv(const ConvArgs c) {
+  ptx::griddep_wait();  // dependent launch: the kernel before this one has completed
   const int64_t P = (int64_t)c.OH * c.OW;
   const int64_t total = (int64_t)c.B * c.OC * P;
   const int64_t HW = (int64_t)c.H * c.W, taps = (int64_t)c.KH * c.KW;
@@ -270,58 +276,61 @@ cudaError_t launch_simt_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.M * a.N <= kSmallOutputs && a.K <= kSmallK) {
     const int T = a.K <= 32 ? 1 : (a.K <= 64 ? 2 : (a.K <= 128 ? 4 : 8));
     const unsigned blocks = (unsigned)((a.M * a.N * T + 255) / 256);
+    cudaError_t e;
     switch (T) {
-      case 1: k_simt_small<1><<<blocks, 256, 0, s>>>(a); break;
-      case 2: k_simt_small<2><<<blocks, 256, 0, s>>>(a); break;
-      case 4: k_simt_small<4><<<blocks, 256, 0, s>>>(a); break;
-      default: k_simt_small<8><<<blocks, 256, 0, s>>>(a); break;
+      case 1: e = launch_after_previous(k_simt_small<1>, dim3(blocks), dim3(256), 0, s, a); break;
+      case 2: e = launch_after_previous(k_simt_small<2>, dim3(blocks), dim3(256), 0, s, a); break;
+      case 4: e = launch_after_previous(k_simt_small<4>, dim3(blocks), dim3(256), 0, s, a); break;
+      default: e = launch_after_previous(k_simt_small<8>, dim3(blocks), dim3(256), 0, s, a); break;
     }
     note_launch();
     note_kernel_name("k_simt_small");
-    return cudaGetLastError();
+    return e;
   }
   unsigned grid;
   if (!simt_grid(a.M, a.N, &grid)) return cudaErrorInvalidConfiguration;
-  k_simt<GemmOperands><<<grid, THREADS, 0, s>>>(GemmOperands{a});
+  const cudaError_t e =
+      launch_after_previous(k_simt<GemmOperands>, dim3(grid), dim3(THREADS), 0, s, GemmOperands{a});
   note_launch();
   note_kernel_name("k_simt<gemm>");
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_simt_conv(const ConvArgs& c, cudaStream_t s) {
   unsigned grid;
   if (!simt_grid(c.M, c.N, &grid)) return cudaErrorInvalidConfiguration;
-  k_simt<ConvOperands><<<grid, THREADS, 0, s>>>(ConvOperands{c});
+  const cudaError_t e =
+      launch_after_previous(k_simt<ConvOperands>, dim3(grid), dim3(THREADS), 0, s, ConvOperands{c});
   note_launch();
   note_kernel_name("k_simt<conv>");
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_fill_gemm(const GemmArgs& a, cudaStream_t s) {
-  k_fill_gemm<<<fill_blocks(a.M * a.N), 256, 0, s>>>(a);
+  const cudaError_t e = launch_after_previous(k_fill_gemm, dim3(fill_blocks(a.M * a.N)), dim3(256), 0, s, a);
   note_launch();
   note_kernel_name("k_fill_gemm");
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_direct_conv(const ConvArgs& c, cudaStream_t s) {
   const int64_t total = (int64_t)c.B * c.OC * c.OH * c.OW;
   const int64_t cap = (int64_t)device_sm_count() * 16, blocks = (total + 255) / 256;
   // as in the pages' direct kernel: the 4-channel form when IC % 4 == 0
-  if (c.IC % 4 == 0)
-    k_direct_conv<true><<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(c);
-  else
-    k_direct_conv<false><<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(c);
+  const dim3 grid((unsigned)(blocks < cap ? blocks : cap));
+  const cudaError_t e = c.IC % 4 == 0 ? launch_after_previous(k_direct_conv<true>, grid, dim3(256), 0, s, c)
+                                      : launch_after_previous(k_direct_conv<false>, grid, dim3(256), 0, s, c);
   note_launch();
   note_kernel_name("k_direct_conv");
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_fill_conv(const ConvArgs& c, cudaStream_t s) {
-  k_fill_conv<<<fill_blocks((int64_t)c.B * c.OC * c.OH * c.OW), 256, 0, s>>>(c);
+  const cudaError_t e = launch_after_previous(
+      k_fill_conv, dim3(fill_blocks((int64_t)c.B * c.OC * c.OH * c.OW)), dim3(256), 0, s, c);
   note_launch();
   note_kernel_name("k_fill_conv");
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace imc

@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      ptx::griddep_wait();  // mat2^T (or w_lo) comes from the pre-pass
+      ptx::griddep_wait();  // mat2^T (or w_lo) comes from the pre-pass, or the kernel before
       const uint32_t tx = (uint32_t)(A_BYTES + (THREE ? 2 : 1) * bn * BK * 4);
       int s = 0, issued = 0;
       uint32_t ph = 0;
@@ -539,6 +539,9 @@ __global__ void __launch_bounds__(THREE ? 320 : 192, 1)
     __syncwarp();
   } else if (warp < 6) {
     // ----------------------------------------------------------- epilogue
+    // self is read ahead of the first accumulator: not before the kernel
+    // before this one (a dependent launch) has completed
+    ptx::griddep_wait();
     const int q = warp & 3;  // TMEM lane quadrant this warp may read
     float* stage = epi + (warp - 2) * 32 * EPI_PITCH;
     int tl = 0;
@@ -828,7 +831,7 @@ constexpr int kMaxDev = 64;
 // ldb: the row length of the B operand (bt_hi / bt_lo).
 template <bool THREE, bool TS>
 cudaError_t run(const GemmArgs& g, const Plan& p, const float* a, int64_t lda, const float* bt_hi,
-                const float* bt_lo, int64_t ldb, float* part, bool after_prep, cudaStream_t s) {
+                const float* bt_lo, int64_t ldb, float* part, cudaStream_t s) {
   constexpr int smem = smem_bytes(TS ? kLts : (THREE ? kL3 : kL1));
   static std::atomic<bool> ready[kMaxDev];  // per device: the attribute is set (calls may race)
   auto k = k_tc_gemm<THREE, TS>;
@@ -856,14 +859,10 @@ cudaError_t run(const GemmArgs& g, const Plan& p, const float* a, int64_t lda, c
   CUtensorMap tout;
   const int tma_out = p.splits == 1 && g.vec_out && encode_out(&tout, g) ? 1 : 0;
   if (!tma_out) tout = ta;  // not read
-  if (after_prep) {
-    e = launch_after_previous(k, dim3(grid), block, (size_t)smem, s, ta, tbh, tbl, tout, tma_out,
-                              g, p.num_m, p.num_n, group, p.bn, p.splits, p.kps, part);
-  } else {
-    k<<<grid, block, smem, s>>>(ta, tbh, tbl, tout, tma_out, g, p.num_m, p.num_n, group, p.bn,
-                                p.splits, p.kps, part);
-    e = cudaGetLastError();
-  }
+  // a dependent launch whether or not a pre-pass comes first: every global
+  // access of the kernel follows a griddepcontrol.wait
+  e = launch_after_previous(k, dim3(grid), block, (size_t)smem, s, ta, tbh, tbl, tout, tma_out, g,
+                            p.num_m, p.num_n, group, p.bn, p.splits, p.kps, part);
   note_launch();
   note_kernel_name(TS ? "k_tc_gemm<3xtf32,a_tmem>" : (THREE ? "k_tc_gemm<3xtf32>" : "k_tc_gemm<1xtf32>"));
   if (e != cudaSuccess || p.splits == 1) return e;
@@ -909,7 +908,6 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
   const float *b_hi, *b_lo, *a = g.mat1;
   int64_t lda = g.K, ldb = ld;
   const int64_t cap = (int64_t)device_sm_count() * 8;
-  bool prep = false;
   if (pad_a) {  // mat1 rows to 16-byte aligned rows of ld floats
     float* a_copy = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.a_offset);
     const int64_t blocks = g.M * ((g.K + 255) / 256);
@@ -920,7 +918,6 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
     if (e != cudaSuccess) return e;
     a = a_copy;
     lda = ld;
-    prep = true;
   }
   if (g.b_kmajor && pad_b) {  // w[N,K] to aligned rows, hi (+ lo)
     b_hi = ws;
@@ -931,7 +928,6 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
                                                 three_pass ? ws + g.N * ld : (float*)nullptr);
     note_launch();
     if (e != cudaSuccess) return e;
-    prep = true;
   } else if (g.b_kmajor) {  // w[N,K] is B_hi; 3xTF32 adds w_lo in the scratch
     b_hi = g.mat2;
     b_lo = three_pass ? ws : nullptr;
@@ -945,8 +941,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
           reinterpret_cast<const float4*>(g.mat2), total4, reinterpret_cast<float4*>(ws));
       note_launch();
       if (e != cudaSuccess) return e;
-      prep = true;
-    }
+      }
   } else {  // transpose mat2[K,N] into Bt_hi[N,ld] (+ Bt_lo)
     b_hi = ws;
     b_lo = three_pass ? ws + g.N * ld : nullptr;
@@ -964,15 +959,14 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
       if (e != cudaSuccess) return e;
     }
     note_launch();
-    prep = true;
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (!three_pass) return run<false, false>(g, p, a, lda, b_hi, nullptr, ldb, part, prep, s);
+  if (!three_pass) return run<false, false>(g, p, a, lda, b_hi, nullptr, ldb, part, s);
   const bool light = !(g.read_self && g.self_2d) || p.splits > 1;  // no [M,N] self read per tile
   const bool ts = p.kps >= kTsMinKb || (light && p.kps >= kTsMinKbLightEpilogue);
-  return ts ? run<true, true>(g, p, a, lda, b_hi, b_lo, ldb, part, prep, s)
-            : run<true, false>(g, p, a, lda, b_hi, b_lo, ldb, part, prep, s);
+  return ts ? run<true, true>(g, p, a, lda, b_hi, b_lo, ldb, part, s)
+            : run<true, false>(g, p, a, lda, b_hi, b_lo, ldb, part, s);
 }
 
 namespace {
