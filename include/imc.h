@@ -19,6 +19,16 @@
  *    (calls on different streams never wait for each other through it).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *    enqueued asynchronously on it; no entry point synchronises the host.
+ *  - Every kernel is launched as the programmatic dependent of the kernel
+ *    before it on `stream` (cudaLaunchAttributeProgrammaticStreamSerialization)
+ *    and executes griddepcontrol.wait before any global access that kernel
+ *    could conflict with, so stream order holds exactly as for plain launches,
+ *    also after a caller's kernel that releases its dependents early; a call
+ *    that follows another library call on the same stream starts sooner.  The
+ *    conv kernels release the stream's next kernel once their last loads are
+ *    out: a caller's kernel launched as a programmatic dependent after a conv
+ *    call must execute griddepcontrol.wait before it reads the conv's output
+ *    (as every programmatic dependent must); plain launches are unaffected.
  *  - The *_ws entry points enqueue only kernels on `stream` (no allocation,
  *    no host synchronisation), so they can be captured into a CUDA graph and
  *    replayed on new data written into the same buffers; make one call on the
