@@ -307,7 +307,8 @@ cudaError_t launch_simt_conv(const ConvArgs& c, cudaStream_t s) {
 }
 
 cudaError_t launch_fill_gemm(const GemmArgs& a, cudaStream_t s) {
-  const cudaError_t e = launch_after_previous(k_fill_gemm, dim3(fill_blocks(a.M * a.N)), dim3(256), 0, s, a);
+  const cudaError_t e =
+      launch_after_previous(k_fill_gemm, dim3(fill_blocks(a.M * a.N)), dim3(256), 0, s, a);
   note_launch();
   note_kernel_name("k_fill_gemm");
   return e;
@@ -318,8 +319,9 @@ cudaError_t launch_direct_conv(const ConvArgs& c, cudaStream_t s) {
   const int64_t cap = (int64_t)device_sm_count() * 16, blocks = (total + 255) / 256;
   // as in the pages' direct kernel: the 4-channel form when IC % 4 == 0
   const dim3 grid((unsigned)(blocks < cap ? blocks : cap));
-  const cudaError_t e = c.IC % 4 == 0 ? launch_after_previous(k_direct_conv<true>, grid, dim3(256), 0, s, c)
-                                      : launch_after_previous(k_direct_conv<false>, grid, dim3(256), 0, s, c);
+  const cudaError_t e =
+      c.IC % 4 == 0 ? launch_after_previous(k_direct_conv<true>, grid, dim3(256), 0, s, c)
+                    : launch_after_previous(k_direct_conv<false>, grid, dim3(256), 0, s, c);
   note_launch();
   note_kernel_name("k_direct_conv");
   return e;

@@ -1463,8 +1463,9 @@ cudaError_t launch_tc_conv(const ConvArgs& c, bool three_pass, void* workspace,
   const int gx = (int)((Kp + 255) / 256 < 64 ? (Kp + 255) / 256 : 64);
   const int gy_cap = 2 * device_sm_count() / gx > 1 ? 2 * device_sm_count() / gx : 1;
   const int gy = std::max(1, (int)((c.OC + 3) / 4 < gy_cap ? (c.OC + 3) / 4 : gy_cap));
-  cudaError_t e = launch_after_previous(k_prep_w, dim3(gx, gy), dim3(256), 0, s, c.w, c.OC, (int)c.K,
-                                        (int)Kp, c.IC, c.KH * c.KW, ic_fastest(c) ? 1 : 0, w_hi, w_lo);
+  cudaError_t e = launch_after_previous(k_prep_w, dim3(gx, gy), dim3(256), 0, s, c.w, c.OC,
+                                        (int)c.K, (int)Kp, c.IC, c.KH * c.KW,
+                                        ic_fastest(c) ? 1 : 0, w_hi, w_lo);
   note_launch();
   if (e != cudaSuccess) return e;
   Sched qt;

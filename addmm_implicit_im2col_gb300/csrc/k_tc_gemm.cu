@@ -911,9 +911,9 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
   if (pad_a) {  // mat1 rows to 16-byte aligned rows of ld floats
     float* a_copy = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.a_offset);
     const int64_t blocks = g.M * ((g.K + 255) / 256);
-    const cudaError_t e = launch_after_previous(k_pad_rows, dim3((unsigned)(blocks < cap ? blocks : cap)),
-                                                dim3(256), 0, s, g.mat1, g.M, g.K, ld, a_copy,
-                                                (float*)nullptr);
+    const dim3 grid((unsigned)(blocks < cap ? blocks : cap));
+    const cudaError_t e = launch_after_previous(k_pad_rows, grid, dim3(256), 0, s, g.mat1, g.M,
+                                                g.K, ld, a_copy, (float*)nullptr);
     note_launch();
     if (e != cudaSuccess) return e;
     a = a_copy;
@@ -923,8 +923,9 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
     b_hi = ws;
     b_lo = three_pass ? ws + g.N * ld : nullptr;
     const int64_t blocks = g.N * ((g.K + 255) / 256);
-    const cudaError_t e = launch_after_previous(k_pad_rows, dim3((unsigned)(blocks < cap ? blocks : cap)),
-                                                dim3(256), 0, s, g.mat2, g.N, g.K, ld, ws,
+    const dim3 grid((unsigned)(blocks < cap ? blocks : cap));
+    const cudaError_t e = launch_after_previous(k_pad_rows, grid, dim3(256), 0, s, g.mat2, g.N,
+                                                g.K, ld, ws,
                                                 three_pass ? ws + g.N * ld : (float*)nullptr);
     note_launch();
     if (e != cudaSuccess) return e;
@@ -941,7 +942,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, bool three_pass, void* workspace,
           reinterpret_cast<const float4*>(g.mat2), total4, reinterpret_cast<float4*>(ws));
       note_launch();
       if (e != cudaSuccess) return e;
-      }
+    }
   } else {  // transpose mat2[K,N] into Bt_hi[N,ld] (+ Bt_lo)
     b_hi = ws;
     b_lo = three_pass ? ws + g.N * ld : nullptr;
