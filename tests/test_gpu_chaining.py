@@ -1,14 +1,13 @@
 """Calls issued back to back on one stream, with no host synchronisation between
 them, against the same calls run one at a time.
 
-A call's first kernel (the weight / mat2 pre-pass or the mat1 row copy) is a
-dependent launch: it may be placed while the kernel before it still runs and
-waits for that kernel before it touches memory.  These cases make a missing or
-misplaced wait visible: the second call's pre-pass rewrites the scratch the
-first call's main kernel reads (one workspace for both), a call reads what the
-call before it wrote, or writes what the call before it reads.  The kernels
-are deterministic, so the chained results must equal the one-at-a-time
-results bit for bit.
+Every kernel is a dependent launch: it may be placed while the kernel before
+it still runs, and waits for that kernel before it touches memory.  These
+cases make a missing or misplaced wait visible: the second call's pre-pass
+rewrites the scratch the first call's main kernel reads (one workspace for
+both), a call reads what the call before it wrote, or writes what the call
+before it reads.  The kernels are deterministic, so the chained results must
+equal the one-at-a-time results bit for bit.
 """
 import numpy as np
 import pytest
@@ -39,36 +38,36 @@ def _stream():
     return torch.cuda.current_stream().cuda_stream
 
 
-def conv_ws(x, w, b, out, shape, ws):
+def conv_ws(x, w, b, out, shape, ws, mode="default"):
     B_, IC, H, W, OC, KH, KW, st, pd, dl = shape
     rc = binding.conv2d_gemm_f32_ws(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(), B_,
                                     IC, H, W, OC, KH, KW, st, st, pd, pd, dl, dl,
-                                    binding.MODES["default"], ws.data_ptr(), ws.numel(), _stream())
+                                    binding.MODES[mode], ws.data_ptr(), ws.numel(), _stream())
     assert rc == binding.IMC_OK, binding.status_string(rc)
     return binding.last_kernel_name()
 
 
-def addmm_ws(s, a, b, out, ws):
+def addmm_ws(s, a, b, out, ws, mode="default"):
     (M, K), N = a.shape, b.shape[1]
     rc = binding.gemm_addmm_f32_ws(s.data_ptr(), 0, a.data_ptr(), b.data_ptr(), out.data_ptr(), M,
-                                   N, K, 1.0, 1.0, binding.MODES["default"], ws.data_ptr(),
-                                   ws.numel(), _stream())
+                                   N, K, 1.0, 1.0, binding.MODES[mode], ws.data_ptr(), ws.numel(),
+                                   _stream())
     assert rc == binding.IMC_OK, binding.status_string(rc)
     return binding.last_kernel_name()
 
 
-def linear_ws(x, w, b, out, ws):
+def linear_ws(x, w, b, out, ws, mode="default"):
     (M, K), N = x.shape, w.shape[0]
     rc = binding.linear_f32_ws(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K,
-                               binding.MODES["default"], ws.data_ptr(), ws.numel(), _stream())
+                               binding.MODES[mode], ws.data_ptr(), ws.numel(), _stream())
     assert rc == binding.IMC_OK, binding.status_string(rc)
     return binding.last_kernel_name()
 
 
-def conv_bytes(shape):
+def conv_bytes(shape, mode="default"):
     B_, IC, H, W, OC, KH, KW, st, pd, dl = shape
     return binding.conv2d_gemm_f32_workspace_bytes(B_, IC, H, W, OC, KH, KW, st, st, pd, pd, dl,
-                                                   dl, binding.MODES["default"])
+                                                   dl, binding.MODES[mode])
 
 
 def out_hw(n, k, st, pd, dl):
@@ -104,8 +103,9 @@ CONV_PAIRS = [
 ]
 
 
+@pytest.mark.parametrize("mode", ["default", "tf32"])
 @pytest.mark.parametrize("shape", CONV_PAIRS)
-def test_conv_pair_sharing_one_workspace(shape):
+def test_conv_pair_sharing_one_workspace(shape, mode):
     # the second call's weight pre-pass rewrites the split weight the first
     # call's main kernel reads
     x, w1, b1 = synth.conv_inputs(*shape[:7], workload=700)
@@ -115,11 +115,11 @@ def test_conv_pair_sharing_one_workspace(shape):
         out_hw(shape[3], shape[6], shape[7], shape[8], shape[9])
     o1 = torch.empty((shape[0], shape[4], OH, OW), device="cuda")
     o2 = torch.empty_like(o1)
-    ws = torch.empty(max(conv_bytes(shape), 16), dtype=torch.uint8, device="cuda")
-    kern = conv_ws(X, W1, B1, o1, shape, ws)
+    ws = torch.empty(max(conv_bytes(shape, mode), 16), dtype=torch.uint8, device="cuda")
+    kern = conv_ws(X, W1, B1, o1, shape, ws, mode)
     assert kern.startswith("k_tc_conv"), kern
-    calls = [(lambda: conv_ws(X, W1, B1, o1, shape, ws), o1),
-             (lambda: conv_ws(X, W2, B2, o2, shape, ws), o2)]
+    calls = [(lambda: conv_ws(X, W1, B1, o1, shape, ws, mode), o1),
+             (lambda: conv_ws(X, W2, B2, o2, shape, ws, mode), o2)]
     refs = one_at_a_time(calls)
     assert not torch.equal(refs[0], refs[1])
     chained(calls, refs, f"conv pair {shape}")
@@ -129,8 +129,9 @@ def test_conv_pair_sharing_one_workspace(shape):
 ADDMM_PAIRS = [(1024, 3072, 768), (577, 768, 3072)]
 
 
+@pytest.mark.parametrize("mode", ["default", "tf32"])
 @pytest.mark.parametrize("mnk", ADDMM_PAIRS)
-def test_addmm_pair_sharing_one_workspace(mnk):
+def test_addmm_pair_sharing_one_workspace(mnk, mode):
     # the second call's mat2 pre-pass rewrites the transposed, split mat2 the
     # first call's main kernel reads
     M, N, K = mnk
@@ -139,17 +140,20 @@ def test_addmm_pair_sharing_one_workspace(mnk):
     S, A, B1, B2 = dev(s), dev(a), dev(b1), dev(b2)
     o1 = torch.empty((M, N), device="cuda")
     o2 = torch.empty_like(o1)
-    nb = binding.gemm_addmm_f32_workspace_bytes(M, N, K, binding.MODES["default"])
+    nb = binding.gemm_addmm_f32_workspace_bytes(M, N, K, binding.MODES[mode])
     ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
-    kern = addmm_ws(S, A, B1, o1, ws)
-    assert kern.startswith("k_tc_gemm<3xtf32"), kern
-    calls = [(lambda: addmm_ws(S, A, B1, o1, ws), o1), (lambda: addmm_ws(S, A, B2, o2, ws), o2)]
+    kern = addmm_ws(S, A, B1, o1, ws, mode)
+    assert kern.startswith("k_tc_gemm<3xtf32" if mode == "default" else "k_tc_gemm<1xtf32"), kern
+    calls = [(lambda: addmm_ws(S, A, B1, o1, ws, mode), o1),
+             (lambda: addmm_ws(S, A, B2, o2, ws, mode), o2)]
     refs = one_at_a_time(calls)
     chained(calls, refs, f"addmm pair {mnk}")
 
 
-def test_linear_pair_sharing_one_workspace():
-    # the second call's w_lo pre-pass rewrites the first call's w_lo
+@pytest.mark.parametrize("mode", ["default", "tf32"])
+def test_linear_pair_sharing_one_workspace(mode):
+    # default: the second call's w_lo pre-pass rewrites the first call's w_lo;
+    # 1xTF32: no pre-pass, each call's main kernel is the dependent launch
     M, N, K = 1024, 3072, 768
     gen = torch.Generator().manual_seed(720)
     x = torch.randn(M, K, generator=gen).cuda()
@@ -158,9 +162,10 @@ def test_linear_pair_sharing_one_workspace():
     bias = (torch.randn(N, generator=gen) * 0.02).cuda()
     o1 = torch.empty((M, N), device="cuda")
     o2 = torch.empty_like(o1)
-    nb = binding.linear_f32_workspace_bytes(M, N, K, binding.MODES["default"])
+    nb = binding.linear_f32_workspace_bytes(M, N, K, binding.MODES[mode])
     ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
-    calls = [(lambda: linear_ws(x, w1, bias, o1, ws), o1), (lambda: linear_ws(x, w2, bias, o2, ws), o2)]
+    calls = [(lambda: linear_ws(x, w1, bias, o1, ws, mode), o1),
+             (lambda: linear_ws(x, w2, bias, o2, ws, mode), o2)]
     refs = one_at_a_time(calls)
     chained(calls, refs, "linear pair")
 
@@ -232,3 +237,40 @@ def test_stem_output_feeds_an_addmm():
     calls = [(lambda: conv_ws(X, W, Bias, y, shape, ws1), y), (lambda: addmm_ws(S, ym, B, z, ws2), z)]
     refs = one_at_a_time(calls)
     chained(calls, refs, "stem -> addmm")
+
+
+def test_simt_calls_feed_each_other():
+    # tiny addmm calls on the SIMT kernel (no scratch): y = s + A @ B, then
+    # z = s2 + y @ C, then A = s3 + D @ E (written while nothing may still read it)
+    M, N, K = 64, 80, 96
+    s, a, b = synth.addmm_inputs(M, N, K, self_2d=False, workload=760)
+    s2, _, c = synth.addmm_inputs(M, K, N, self_2d=False, workload=761)
+    s3, d, e = synth.addmm_inputs(M, K, 32, self_2d=False, workload=762)
+    S, B, S2, C, S3, D, E = (dev(v) for v in (s, b, s2, c, s3, d, e))
+    A = dev(a)
+    y = torch.empty((M, N), device="cuda")
+    z = torch.empty((M, K), device="cuda")
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    a0 = A.clone()
+
+    def run():
+        addmm_ws(S, A, B, y, ws, "simt")
+        addmm_ws(S2, y, C, z, ws, "simt")
+        addmm_ws(S3, D, E, A, ws, "simt")
+
+    for fn in (lambda: addmm_ws(S, A, B, y, ws, "simt"), lambda: addmm_ws(S2, y, C, z, ws, "simt"),
+               lambda: addmm_ws(S3, D, E, A, ws, "simt")):
+        fn()
+        torch.cuda.synchronize()
+    assert binding.last_kernel_name() == "k_simt_small", binding.last_kernel_name()
+    y_ref, z_ref, a_ref = y.clone(), z.clone(), A.clone()
+    for rep in range(REPS):
+        A.copy_(a0)
+        y.fill_(float("nan"))
+        z.fill_(float("nan"))
+        torch.cuda.synchronize()
+        for _ in range(4):  # the chain four times over: A is rewritten, then read again
+            A.copy_(a0)
+            run()
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref) and torch.equal(z, z_ref) and torch.equal(A, a_ref), rep
