@@ -274,3 +274,83 @@ def test_simt_calls_feed_each_other():
             run()
         torch.cuda.synchronize()
         assert torch.equal(y, y_ref) and torch.equal(z, z_ref) and torch.equal(A, a_ref), rep
+
+
+# ------------------------------------------------ a random mix, one workspace
+def _mixed_calls():
+    """About thirty calls drawn from the random-shape sweep's lists (addmm of
+    every size class, linear, convs of the gather, slab and transposed slab
+    forms), 3xTF32 and 1xTF32 alternating, in a seeded random order."""
+    from test_gpu_random_shapes import ADDMM, ADDMM_EXTREME, CONV, CONV_T, LINEAR
+    rng = np.random.RandomState(77)
+    picks = ([("addmm", int(i)) for i in rng.choice(len(ADDMM), 10, replace=False)]
+             + [("extreme", int(i)) for i in rng.choice(len(ADDMM_EXTREME), 4, replace=False)]
+             + [("conv", int(i)) for i in rng.choice(len(CONV), 9, replace=False)]
+             + [("conv_t", int(i)) for i in rng.choice(len(CONV_T), 2, replace=False)]
+             + [("linear", int(i)) for i in rng.choice(len(LINEAR), 6, replace=False)])
+    rng.shuffle(picks)
+    calls, need = [], 16
+    for n, (kind, i) in enumerate(picks):
+        mode = ("default", "tf32")[n % 2]
+        m = binding.MODES[mode]
+        if kind in ("addmm", "extreme"):
+            t = (ADDMM if kind == "addmm" else ADDMM_EXTREME)[i]
+            M, N, K, s2 = t[:4]
+            beta, alpha = (t[4], t[5]) if kind == "addmm" else (1.0, 1.0)
+            s, a, b = (dev(v) for v in synth.addmm_inputs(M, N, K, self_2d=s2, workload=800 + n))
+            out = torch.empty((M, N), device="cuda")
+            need = max(need, binding.gemm_addmm_f32_workspace_bytes(M, N, K, m))
+
+            def fn(ws, s=s, a=a, b=b, out=out, M=M, N=N, K=K, s2=s2, beta=beta, alpha=alpha, m=m):
+                return binding.gemm_addmm_f32_ws(s.data_ptr(), int(s2), a.data_ptr(), b.data_ptr(),
+                                                 out.data_ptr(), M, N, K, beta, alpha, m,
+                                                 ws.data_ptr(), ws.numel(), _stream())
+        elif kind == "linear":
+            M, N, K = LINEAR[i][:3]
+            gen = torch.Generator().manual_seed(800 + n)
+            x = torch.randn(M, K, generator=gen).cuda()
+            w = (torch.randn(N, K, generator=gen) / K ** 0.5).cuda()
+            bias = (torch.randn(N, generator=gen) * 0.02).cuda()
+            out = torch.empty((M, N), device="cuda")
+            need = max(need, binding.linear_f32_workspace_bytes(M, N, K, m))
+
+            def fn(ws, x=x, w=w, bias=bias, out=out, M=M, N=N, K=K, m=m):
+                return binding.linear_f32_ws(x.data_ptr(), w.data_ptr(), bias.data_ptr(),
+                                             out.data_ptr(), M, N, K, m, ws.data_ptr(), ws.numel(),
+                                             _stream())
+        else:
+            B_, IC, H, W, OC, KH, KW, s, p, d = (CONV if kind == "conv" else CONV_T)[i]
+            x, w, bias = (dev(v) for v in synth.conv_inputs(B_, IC, H, W, OC, KH, KW,
+                                                             workload=800 + n))
+            OH = (H + 2 * p[0] - d[0] * (KH - 1) - 1) // s[0] + 1
+            OW = (W + 2 * p[1] - d[1] * (KW - 1) - 1) // s[1] + 1
+            out = torch.empty((B_, OC, OH, OW), device="cuda")
+            geo = (B_, IC, H, W, OC, KH, KW, s[0], s[1], p[0], p[1], d[0], d[1])
+            need = max(need, binding.conv2d_gemm_f32_workspace_bytes(*geo, m))
+
+            def fn(ws, x=x, w=w, bias=bias, out=out, geo=geo, m=m):
+                return binding.conv2d_gemm_f32_ws(x.data_ptr(), w.data_ptr(), bias.data_ptr(),
+                                                  out.data_ptr(), *geo, m, ws.data_ptr(),
+                                                  ws.numel(), _stream())
+        calls.append((fn, out))
+    return calls, need
+
+
+def test_random_mix_chained_through_one_workspace():
+    # every call's scratch is the same buffer, so each pre-pass (or split-K
+    # partial sum) rewrites what the call before it read
+    calls, need = _mixed_calls()
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    names = set()
+
+    def run(fn):
+        rc = fn(ws)
+        assert rc == binding.IMC_OK, binding.status_string(rc)
+        names.add(binding.last_kernel_name())
+
+    wrapped = [(lambda fn=fn: run(fn), out) for fn, out in calls]
+    refs = one_at_a_time(wrapped)
+    assert any(n.startswith("k_tc_gemm<3x") for n in names), names
+    assert any(n.startswith("k_tc_gemm<1x") for n in names), names
+    assert any(n.startswith("k_tc_conv") for n in names), names
+    chained(wrapped, refs, "random mix")
